@@ -1,0 +1,227 @@
+/*
+ * fp64 CPU oracle for the selective scan (S6) and its single-token update.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the package's smoke check and
+ * the benchmark's CPU-baseline leg may load or call this code.  The CUDA
+ * library never links, includes or calls it, and it shares no code with it.
+ *
+ * What it computes (page "Mamba: linear-time sequence modeling with
+ * selective state spaces", section "What they did", the S6 bullet and its two
+ * sub-bullets; the recurrence, Euler input term, skip term and silu gate are
+ * the S6 layer's definition as restated in the workload description):
+ *
+ *   s_t      = delta[b,d,t] + dt_bias[d]                  (dt_bias may be absent)
+ *   Delta_t  = softplus(s_t)  if the softplus flag is set, else s_t
+ *   Abar     = exp(Delta_t * A[d,n])                      (A input-independent)
+ *   h[n]     = Abar * h[n] + Delta_t * B[b,n,t] * u[b,d,t]
+ *   y[b,d,t] = (sum_n C[b,n,t] * h[n] + D_skip[d] * u[b,d,t]) * silu(z[b,d,t])
+ *
+ * with h = h0[b,d,:] (zero when h0 is absent) before the first step, the gate
+ * skipped when z is absent, and the state after the last step returned in
+ * final_state.  The single-token update is one step of the same recurrence
+ * applied in place to a caller-held state, with softplus always applied (the
+ * generation mode of page "Mamba: Linear-Time Sequence Modeling with
+ * Selective State Spaces", section "Architecture": one state update per
+ * token).
+ *
+ * Everything is plain fp64, one (b, d) row at a time, time-sequential inside
+ * a row.  Rows are independent and are split statically over POSIX threads.
+ * Layouts are dense row-major: u, delta, z, y (batch, dim, L); B, C
+ * (batch, N, L); A (dim, N); dt_bias, D_skip (dim); h0, final_state
+ * (batch, dim, N).  Inputs arrive already widened to double by the caller.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* softplus(s) = log(1 + e^s), evaluated without overflow or cancellation. */
+double oracle_softplus_f64(double s)
+{
+    if (s > 0.0)
+        return s + log1p(exp(-s));
+    return log1p(exp(s));
+}
+
+/* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
+double oracle_silu_f64(double z)
+{
+    return z / (1.0 + exp(-z));
+}
+
+typedef struct {
+    int64_t batch, dim, dstate, seqlen;
+    const double *u, *delta, *dt_bias, *A, *B, *C, *D_skip, *z, *h0;
+    int softplus;
+    double *y, *final_state;
+    int64_t row_begin, row_end;
+    int status;
+} scan_job;
+
+static void scan_rows(scan_job *j)
+{
+    const int64_t N = j->dstate, L = j->seqlen, D = j->dim;
+    double *h = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    if (!h) {
+        j->status = -1;
+        return;
+    }
+    for (int64_t row = j->row_begin; row < j->row_end; ++row) {
+        const int64_t b = row / D, d = row % D;
+        const double *u = j->u + row * L;
+        const double *dl = j->delta + row * L;
+        const double *z = j->z ? j->z + row * L : NULL;
+        const double *Bb = j->B + b * N * L;
+        const double *Cb = j->C + b * N * L;
+        const double *Ad = j->A + d * N;
+        const double bias = j->dt_bias ? j->dt_bias[d] : 0.0;
+        const double dsk = j->D_skip ? j->D_skip[d] : 0.0;
+        double *y = j->y + row * L;
+
+        for (int64_t n = 0; n < N; ++n)
+            h[n] = j->h0 ? j->h0[row * N + n] : 0.0;
+
+        for (int64_t t = 0; t < L; ++t) {
+            const double s = dl[t] + bias;
+            const double dt = j->softplus ? oracle_softplus_f64(s) : s;
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                const double abar = exp(dt * Ad[n]);
+                h[n] = abar * h[n] + dt * Bb[n * L + t] * u[t];
+                acc += Cb[n * L + t] * h[n];
+            }
+            double out = acc + dsk * u[t];
+            if (z)
+                out *= oracle_silu_f64(z[t]);
+            y[t] = out;
+        }
+        if (j->final_state)
+            for (int64_t n = 0; n < N; ++n)
+                j->final_state[row * N + n] = h[n];
+    }
+    free(h);
+    j->status = 0;
+}
+
+static void *scan_thread(void *p)
+{
+    scan_rows((scan_job *)p);
+    return NULL;
+}
+
+static int pick_threads(int requested, int64_t rows)
+{
+    long n = requested > 0 ? requested : sysconf(_SC_NPROCESSORS_ONLN);
+    if (n < 1)
+        n = 1;
+    if (n > 512)
+        n = 512;
+    if ((int64_t)n > rows)
+        n = (long)(rows > 0 ? rows : 1);
+    return (int)n;
+}
+
+/* Returns the number of threads used (>0) or a negative error code. */
+int oracle_scan_f64(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                    const double *u, const double *delta, const double *dt_bias,
+                    const double *A, const double *B, const double *C,
+                    const double *D_skip, const double *z, int softplus,
+                    const double *h0, double *y, double *final_state,
+                    int nthreads)
+{
+    if (batch < 0 || dim < 0 || dstate < 0 || seqlen < 0)
+        return -2;
+    if (!u || !delta || !A || !B || !C || !y)
+        return -1;
+    const int64_t rows = batch * dim;
+    const int nt = pick_threads(nthreads, rows);
+    scan_job *jobs = (scan_job *)calloc((size_t)nt, sizeof(scan_job));
+    pthread_t *th = (pthread_t *)calloc((size_t)nt, sizeof(pthread_t));
+    if (!jobs || !th) {
+        free(jobs);
+        free(th);
+        return -3;
+    }
+    for (int i = 0; i < nt; ++i) {
+        scan_job *j = &jobs[i];
+        j->batch = batch;
+        j->dim = dim;
+        j->dstate = dstate;
+        j->seqlen = seqlen;
+        j->u = u;
+        j->delta = delta;
+        j->dt_bias = dt_bias;
+        j->A = A;
+        j->B = B;
+        j->C = C;
+        j->D_skip = D_skip;
+        j->z = z;
+        j->h0 = h0;
+        j->softplus = softplus;
+        j->y = y;
+        j->final_state = final_state;
+        j->row_begin = rows * i / nt;
+        j->row_end = rows * (i + 1) / nt;
+    }
+    int status = 0;
+    if (nt == 1) {
+        scan_rows(&jobs[0]);
+        status = jobs[0].status;
+    } else {
+        int started = 0;
+        for (int i = 0; i < nt; ++i) {
+            if (pthread_create(&th[i], NULL, scan_thread, &jobs[i]) != 0)
+                break;
+            ++started;
+        }
+        for (int i = 0; i < started; ++i)
+            pthread_join(th[i], NULL);
+        for (int i = started; i < nt; ++i)
+            scan_rows(&jobs[i]); /* thread creation failed: finish inline */
+        for (int i = 0; i < nt; ++i)
+            if (jobs[i].status)
+                status = jobs[i].status;
+    }
+    free(jobs);
+    free(th);
+    return status ? status : nt;
+}
+
+/*
+ * One generation step on a (batch, dim, N) state, in place:
+ *   Delta = softplus(delta[b,d] + dt_bias[d])
+ *   h[n]  = exp(Delta*A[d,n]) * h[n] + Delta*B[b,n]*x[b,d]
+ *   y     = (sum_n C[b,n]*h[n] + D_skip[d]*x[b,d]) * silu(z[b,d])
+ * x, delta, z, y are (batch, dim); B, C are (batch, N).
+ */
+int oracle_state_update_f64(int64_t batch, int64_t dim, int64_t dstate,
+                            double *state, const double *x, const double *delta,
+                            const double *dt_bias, const double *A,
+                            const double *B, const double *C,
+                            const double *D_skip, const double *z, double *y)
+{
+    if (batch < 0 || dim < 0 || dstate < 0)
+        return -2;
+    if (!state || !x || !delta || !A || !B || !C || !y)
+        return -1;
+    const int64_t N = dstate;
+    for (int64_t b = 0; b < batch; ++b) {
+        for (int64_t d = 0; d < dim; ++d) {
+            const int64_t row = b * dim + d;
+            const double dt = oracle_softplus_f64(delta[row] + (dt_bias ? dt_bias[d] : 0.0));
+            double *h = state + row * N;
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                h[n] = exp(dt * A[d * N + n]) * h[n] + dt * B[b * N + n] * x[row];
+                acc += C[b * N + n] * h[n];
+            }
+            double out = acc + (D_skip ? D_skip[d] : 0.0) * x[row];
+            if (z)
+                out *= oracle_silu_f64(z[row]);
+            y[row] = out;
+        }
+    }
+    return 0;
+}
