@@ -1,0 +1,162 @@
+/*
+ * mamba_scan.h - C ABI of the B300 (sm_103a) selective-scan library.
+ *
+ * The operation is the selective state space layer "S6" of Mamba
+ * (page "Mamba: linear-time sequence modeling with selective state spaces",
+ * section "What they did", S6 bullet): Delta, B and C depend on the input,
+ * Delta = softplus(parameter + Linear(x)), A is input-independent and enters
+ * through Abar = exp(Delta*A), and the time-varying model is evaluated as a
+ * recurrent scan over a D x N state per sequence (same page, "the recurrent
+ * state is D x N numbers per layer").  Per (b, d) row and time step t:
+ *
+ *     s        = delta[b,d,t] + dt_bias[d]
+ *     Delta    = softplus(s)   (or s when the softplus flag is 0)
+ *     h[n]     = exp(Delta*A[d,n]) * h[n] + Delta * B[b,n,t] * u[b,d,t]
+ *     y[b,d,t] = (sum_n C[b,n,t]*h[n] + D_skip[d]*u[b,d,t]) * silu(z[b,d,t])
+ *
+ * The input term is the Euler step Delta*B*u; the skip term and the silu
+ * gate are the Mamba block's (page "Mamba: linear-time sequence modeling
+ * with selective state spaces", "Architecture": the block merges H3 with a
+ * gated MLP).  mamba_state_update is the generation mode: one step of the
+ * same recurrence on a caller-held state (page "Mamba: Linear-Time Sequence
+ * Modeling with Selective State Spaces", "Architecture": producing a token
+ * needs only one update of the state).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device and
+ *     are dense row-major with the shapes given below.  The caller owns
+ *     every buffer; the library never frees or retains caller memory.
+ *   - io_dtype selects the storage type of u, delta, z, y, x, B and C:
+ *     MAMBA_F32 (float) or MAMBA_BF16 (bfloat16).  A, dt_bias, D_skip and
+ *     the state are always fp32; all arithmetic is fp32.  y is rounded to
+ *     the storage type with round-to-nearest-even.
+ *   - Nullable pointers: dt_bias (taken as 0), D_skip (taken as 0), z (no
+ *     gate), final_state (not written).
+ *   - Work is enqueued on `stream` and is asynchronous; a return of MAMBA_OK
+ *     means the launch was accepted.  Results are ready when the stream is.
+ *   - Argument errors are detected on the host before anything is launched
+ *     and nothing is written in that case.  Launch failures are reported as
+ *     MAMBA_ERR_CUDA.  A device-side wait that exceeds its time bound (1 s)
+ *     sets a per-device error word instead of hanging; mamba_device_status
+ *     reads and clears it.
+ *   - Outputs must not overlap inputs.  Concurrent calls on different
+ *     streams are safe; each call's scratch memory is stream-ordered.
+ *   - Limits: 1 <= dstate <= 16; batch, dim >= 1; seqlen >= 0 (0 is a
+ *     no-op that zeroes final_state).
+ *   - Rows whose length in bytes is a multiple of 16 (seqlen % 8 == 0 for
+ *     bf16, % 4 == 0 for fp32) with 16-byte aligned base pointers are
+ *     streamed with tensor-map bulk copies; any other shape runs through the
+ *     same kernels with element-wise, bounds-checked loads and stores.
+ */
+#ifndef MAMBA_SCAN_H
+#define MAMBA_SCAN_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MAMBA_F32 = 0,
+    MAMBA_BF16 = 1
+} mamba_dtype_t;
+
+typedef enum {
+    MAMBA_OK = 0,
+    MAMBA_ERR_NULL = -1,     /* a required pointer is NULL */
+    MAMBA_ERR_SHAPE = -2,    /* a size is out of range */
+    MAMBA_ERR_ALIGN = -3,    /* a pointer is not aligned to its element type */
+    MAMBA_ERR_CUDA = -4,     /* a CUDA runtime call or kernel launch failed */
+    MAMBA_ERR_TIMEOUT = -5,  /* a device-side wait ran out (mamba_device_status) */
+    MAMBA_ERR_ALLOC = -6,    /* scratch memory could not be obtained */
+    MAMBA_ERR_DTYPE = -7,    /* io_dtype is not one of mamba_dtype_t */
+    MAMBA_ERR_ALIAS = -8     /* an output overlaps an input */
+} mamba_status_t;
+
+/*
+ * Selective scan over a whole sequence, starting from a zero state.
+ *
+ *   u, delta, z : (batch, dim, seqlen)    io_dtype     z nullable
+ *   B, C        : (batch, dstate, seqlen) io_dtype     shared by all d
+ *   A           : (dim, dstate)           fp32         input-independent
+ *   dt_bias     : (dim)                   fp32         nullable
+ *   D_skip      : (dim)                   fp32         nullable
+ *   softplus    : nonzero -> Delta = softplus(delta + dt_bias)
+ *   y           : (batch, dim, seqlen)    io_dtype     written
+ *   final_state : (batch, dim, dstate)    fp32         nullable; h after the last step
+ *
+ * When the channels alone cannot fill the GPU, the sequence is split into
+ * time chunks that run in parallel; a carry pass composes their (decay,
+ * state) pairs.  The carry buffers are scratch memory obtained
+ * stream-ordered from a library-owned pool on `stream`.
+ */
+int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                   int io_dtype,
+                   const void *u, const void *delta, const float *dt_bias,
+                   const float *A, const void *B, const void *C,
+                   const float *D_skip, const void *z, int softplus,
+                   void *y, float *final_state, cudaStream_t stream);
+
+/*
+ * One generation step, updating `state` in place:
+ *
+ *   state       : (batch, dim, dstate)    fp32         read and written
+ *   x, delta, z : (batch, dim)            io_dtype     z nullable
+ *   B, C        : (batch, dstate)         io_dtype
+ *   A           : (dim, dstate)           fp32
+ *   dt_bias     : (dim)                   fp32         nullable
+ *   D_skip      : (dim)                   fp32         nullable
+ *   y           : (batch, dim)            io_dtype     written
+ *
+ * Delta = softplus(delta + dt_bias) always (the generation step has no flag).
+ * `state` must not overlap y or any input.  Allocates nothing.
+ */
+int mamba_state_update(int64_t batch, int64_t dim, int64_t dstate, int io_dtype,
+                       float *state, const void *x, const void *delta,
+                       const float *dt_bias, const float *A,
+                       const void *B, const void *C, const float *D_skip,
+                       const void *z, void *y, cudaStream_t stream);
+
+/* Static, human-readable name of a mamba_status_t value. */
+const char *mamba_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns MAMBA_OK, MAMBA_ERR_TIMEOUT (a bounded device wait gave up;
+ * the affected outputs are incomplete) or MAMBA_ERR_CUDA.
+ */
+int mamba_device_status(cudaStream_t stream);
+
+/* Library version as major*100 + minor. */
+int mamba_version(void);
+
+/*
+ * Tuning override for experiments, process-wide, affecting later calls of
+ * mamba_scan_fwd: split = lanes sharing one channel's state (1 or 2; used
+ * when dstate > 8), stages = depth of the shared-memory input ring (1..4),
+ * chunks = fixed number of time chunks for every channel tile.  0 restores
+ * the automatic choice for that knob.  Results do not depend on these
+ * settings beyond fp32 rounding order.  Returns MAMBA_ERR_SHAPE for values
+ * out of range.
+ */
+int mamba_scan_set_tuning(int split, int stages, int chunks);
+
+/*
+ * Per-launch timing (process-wide).  After mamba_profile_begin, every kernel
+ * the library launches is bracketed by two CUDA events on its stream.
+ * mamba_profile_end stops recording, waits for those events and writes, for
+ * each kernel kind k < nkinds, the summed device time in milliseconds
+ * (total_ms[k]) and the number of launches (launches[k]).  Kinds:
+ * 0 = scan, 1 = chunk summary, 2 = chunk carry, 3 = state update.
+ * Either output may be NULL.  Not meant for use during stream capture.
+ */
+int mamba_profile_begin(void);
+int mamba_profile_end(double *total_ms, int64_t *launches, int nkinds);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA_SCAN_H */

@@ -1,0 +1,26 @@
+"""Selective scan (S6) and single-token state update on B300 (sm_103a).
+
+Thin Python binding over the C ABI in ``include/mamba_scan.h``
+(``libmamba_scan.so``, built in-tree by ``build.py``).  The functions keep the
+C names and argument order; they only check tensor properties, pass device
+pointers and the current CUDA stream, and turn status codes into exceptions.
+Every step of the computation runs in the library's CUDA kernels: there is
+no CPU or PyTorch fallback, and calling without the built library raises.
+"""
+
+from ._lib import (  # noqa: F401
+    KIND_NAMES,
+    MAMBA_BF16,
+    MAMBA_F32,
+    MambaError,
+    lib_path,
+    load,
+    mamba_device_status,
+    mamba_profile_begin,
+    mamba_profile_end,
+    mamba_scan_fwd,
+    mamba_scan_set_tuning,
+    mamba_state_update,
+    mamba_status_string,
+    mamba_version,
+)

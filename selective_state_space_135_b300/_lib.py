@@ -1,0 +1,213 @@
+"""ctypes marshalling for libmamba_scan.so (see include/mamba_scan.h)."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = os.path.join(HERE, "libmamba_scan.so")
+_lock = threading.Lock()
+_lib = None
+
+MAMBA_F32 = 0
+MAMBA_BF16 = 1
+
+# every symbol the header declares
+EXPORTS = ("mamba_scan_fwd", "mamba_state_update", "mamba_status_string",
+           "mamba_device_status", "mamba_version", "mamba_scan_set_tuning",
+           "mamba_profile_begin", "mamba_profile_end")
+
+KIND_NAMES = ("scan", "chunk_summary", "chunk_carry", "state_update")
+
+
+class MambaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {mamba_status_string(status)} (status {status})")
+
+
+def lib_path() -> str:
+    return _LIB
+
+
+def load():
+    """Load the CUDA library; raise if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB):
+            raise ImportError(
+                f"{_LIB} is missing: build it with `python -m selective_state_space_135_b300.build`")
+        lib = ctypes.CDLL(_LIB)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        lib.mamba_scan_fwd.argtypes = [i64, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                       i32, vp, vp, vp]
+        lib.mamba_scan_fwd.restype = i32
+        lib.mamba_state_update.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                           vp, vp, vp]
+        lib.mamba_state_update.restype = i32
+        lib.mamba_status_string.argtypes = [i32]
+        lib.mamba_status_string.restype = ctypes.c_char_p
+        lib.mamba_device_status.argtypes = [vp]
+        lib.mamba_device_status.restype = i32
+        lib.mamba_version.argtypes = []
+        lib.mamba_version.restype = i32
+        lib.mamba_scan_set_tuning.argtypes = [i32, i32, i32]
+        lib.mamba_scan_set_tuning.restype = i32
+        lib.mamba_profile_begin.argtypes = []
+        lib.mamba_profile_begin.restype = i32
+        lib.mamba_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                          ctypes.POINTER(ctypes.c_int64), i32]
+        lib.mamba_profile_end.restype = i32
+        _lib = lib
+        return lib
+
+
+def mamba_status_string(status: int) -> str:
+    return load().mamba_status_string(int(status)).decode()
+
+
+def mamba_version() -> int:
+    return load().mamba_version()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _io_dtype(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return MAMBA_F32
+    if t.dtype == torch.bfloat16:
+        return MAMBA_BF16
+    raise TypeError(f"unsupported io dtype {t.dtype}; use float32 or bfloat16")
+
+
+def _ptr(t, name, dtype=None, shape=None, device=None):
+    if t is None:
+        return None
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr() or None
+
+
+def _stream_handle(stream, device):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+def mamba_scan_fwd(u, delta, dt_bias, A, B, C, D_skip, z, softplus: bool = True,
+                   y=None, final_state=None, stream=None):
+    """Selective scan.  u, delta, z: (batch, dim, L); B, C: (batch, N, L);
+    A: (dim, N) fp32; dt_bias, D_skip: (dim,) fp32 or None; z may be None.
+    y (allocated if None) gets the output; final_state (batch, dim, N) fp32,
+    if given, gets the state after the last step.  Returns y.
+    """
+    torch = _torch()
+    lib = load()
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    dev = u.device
+    io = _io_dtype(u)
+    if y is None:
+        y = torch.empty_like(u)
+    args = (
+        _ptr(u, "u", u.dtype, (batch, dim, L), dev),
+        _ptr(delta, "delta", u.dtype, (batch, dim, L), dev),
+        _ptr(dt_bias, "dt_bias", torch.float32, (dim,), dev),
+        _ptr(A, "A", torch.float32, (dim, N), dev),
+        _ptr(B, "B", u.dtype, (batch, N, L), dev),
+        _ptr(C, "C", u.dtype, (batch, N, L), dev),
+        _ptr(D_skip, "D_skip", torch.float32, (dim,), dev),
+        _ptr(z, "z", u.dtype, (batch, dim, L), dev),
+    )
+    yp = _ptr(y, "y", u.dtype, (batch, dim, L), dev)
+    fp = _ptr(final_state, "final_state", torch.float32, (batch, dim, N), dev)
+    with torch.cuda.device(dev):
+        st = _stream_handle(stream, dev)
+        rc = lib.mamba_scan_fwd(batch, dim, N, L, io, args[0], args[1], args[2], args[3],
+                                args[4], args[5], args[6], args[7], int(bool(softplus)),
+                                yp, fp, st)
+    if rc != 0:
+        raise MambaError(rc, "mamba_scan_fwd")
+    return y
+
+
+def mamba_state_update(state, x, delta, dt_bias, A, B, C, D_skip, z, y=None, stream=None):
+    """One decode step in place on state (batch, dim, N) fp32.  x, delta, z:
+    (batch, dim); B, C: (batch, N).  Returns y (batch, dim)."""
+    torch = _torch()
+    lib = load()
+    batch, dim, N = state.shape
+    dev = state.device
+    io = _io_dtype(x)
+    if y is None:
+        y = torch.empty_like(x)
+    sp = _ptr(state, "state", torch.float32, (batch, dim, N), dev)
+    args = (
+        _ptr(x, "x", x.dtype, (batch, dim), dev),
+        _ptr(delta, "delta", x.dtype, (batch, dim), dev),
+        _ptr(dt_bias, "dt_bias", torch.float32, (dim,), dev),
+        _ptr(A, "A", torch.float32, (dim, N), dev),
+        _ptr(B, "B", x.dtype, (batch, N), dev),
+        _ptr(C, "C", x.dtype, (batch, N), dev),
+        _ptr(D_skip, "D_skip", torch.float32, (dim,), dev),
+        _ptr(z, "z", x.dtype, (batch, dim), dev),
+    )
+    yp = _ptr(y, "y", x.dtype, (batch, dim), dev)
+    with torch.cuda.device(dev):
+        st = _stream_handle(stream, dev)
+        rc = lib.mamba_state_update(batch, dim, N, io, sp, args[0], args[1], args[2], args[3],
+                                    args[4], args[5], args[6], args[7], yp, st)
+    if rc != 0:
+        raise MambaError(rc, "mamba_state_update")
+    return y
+
+
+def mamba_device_status(stream=None) -> int:
+    """Synchronise the stream and read/clear the device error word (0 = ok)."""
+    torch = _torch()
+    lib = load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    return lib.mamba_device_status(_stream_handle(stream, dev))
+
+
+def mamba_scan_set_tuning(split: int = 0, stages: int = 0, chunks: int = 0) -> None:
+    rc = load().mamba_scan_set_tuning(int(split), int(stages), int(chunks))
+    if rc != 0:
+        raise MambaError(rc, "mamba_scan_set_tuning")
+
+
+def mamba_profile_begin() -> None:
+    rc = load().mamba_profile_begin()
+    if rc != 0:
+        raise MambaError(rc, "mamba_profile_begin")
+
+
+def mamba_profile_end() -> dict:
+    """Stop per-launch timing; return {kind: (total_ms, launches)}."""
+    n = len(KIND_NAMES)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    rc = load().mamba_profile_end(ms, cnt, n)
+    if rc != 0:
+        raise MambaError(rc, "mamba_profile_end")
+    return {KIND_NAMES[i]: (ms[i], cnt[i]) for i in range(n)}

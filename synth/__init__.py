@@ -68,6 +68,18 @@ def widen(arr: np.ndarray, dtype: str, to=np.float64) -> np.ndarray:
     return np.asarray(arr, dtype=np.float32).astype(to)
 
 
+def to_torch(arr, dtype: str, device="cuda"):
+    """Storage-form array (fp32 values or bf16 bits) -> torch tensor on `device`."""
+    if arr is None:
+        return None
+    import torch
+    if dtype == BF16 and arr.dtype == np.uint16:
+        t = torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32))
+    return t.to(device)
+
+
 def store(x: np.ndarray, dtype: str) -> np.ndarray:
     """Round an fp32 array to the storage dtype (fp32 values or bf16 bits)."""
     if dtype == BF16:

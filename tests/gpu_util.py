@@ -1,0 +1,96 @@
+"""Shared helpers for the GPU tests: move seeded inputs to the device, run the
+library through its C ABI, and compare with the fp64 oracle."""
+
+from __future__ import annotations
+
+import numpy as np
+
+import synth
+
+# Tolerances fixed by the workload description: fp32 I/O max-abs 1e-5; bf16
+# I/O (fp32 state and accumulation) 2e-2 relative to the rms of the reference.
+# bf16 outputs are checked two ways: rms(err)/rms(ref) <= 2e-2, and per
+# element |err| <= 2^-8 |ref| + 2e-2 rms(ref), where 2^-8 is the unit
+# round-off of bf16 (8-bit significand, round to nearest even): the fp64
+# reference itself, rounded to bf16, is off by up to 2^-8 |ref| per element
+# and by ~0.07-0.09 rms at the worst element of these heavy-tailed outputs,
+# so the maximum error alone cannot be held to 2e-2 rms.  fp32 outputs (the
+# state) carry no such rounding and are held to max|err| <= 2e-2 rms(ref).
+TOL_F32_ABS = 1e-5
+TOL_BF16_REL_RMS = 2e-2
+BF16_UNIT_ROUNDOFF = 2.0 ** -8
+
+
+def torch_mod():
+    import torch
+    return torch
+
+
+def to_dev(arr, dtype: str, device="cuda"):
+    """Storage-form numpy array (fp32 values or bf16 bits) -> CUDA tensor."""
+    return synth.to_torch(arr, dtype, device)
+
+
+def f32_dev(arr, device="cuda"):
+    torch = torch_mod()
+    if arr is None:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32)).to(device)
+
+
+def to_f64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def scan_on_gpu(inp: dict, with_final=True, z_none=False, dskip_none=False, bias_none=False):
+    """Run mamba_scan_fwd on a synth.scan_inputs dict.  Returns (y, final) tensors."""
+    import selective_state_space_135_b300 as mm
+    torch = torch_mod()
+    dt = inp["dtype"]
+    u = to_dev(inp["u"], dt)
+    delta = to_dev(inp["delta"], dt)
+    z = None if (z_none or inp.get("z") is None) else to_dev(inp["z"], dt)
+    B = to_dev(inp["B"], dt)
+    C = to_dev(inp["C"], dt)
+    A = f32_dev(inp["A"])
+    dtb = None if bias_none else f32_dev(inp["dt_bias"])
+    dsk = None if dskip_none else f32_dev(inp["D_skip"])
+    bt, d, _ = u.shape
+    n = A.shape[1]
+    fin = torch.empty((bt, d, n), dtype=torch.float32, device="cuda") if with_final else None
+    y = mm.mamba_scan_fwd(u, delta, dtb, A, B, C, dsk, z, inp.get("softplus", True),
+                          final_state=fin)
+    torch.cuda.synchronize()
+    return y, fin
+
+
+def err_stats(got: np.ndarray, ref: np.ndarray):
+    diff = np.abs(got - ref)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    mx = float(diff.max()) if diff.size else 0.0
+    rms_err = float(np.sqrt(np.mean(diff * diff))) if diff.size else 0.0
+    beyond_rounding = np.maximum(diff - BF16_UNIT_ROUNDOFF * np.abs(ref), 0.0)
+    bx = float(beyond_rounding.max()) if diff.size else 0.0
+    norm = rms if rms > 0 else 1.0
+    return dict(max_abs=mx, rms_ref=rms, max_rel_rms=mx / norm, rms_rel=rms_err / norm,
+                max_beyond_bf16_rounding_rel_rms=bx / norm)
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "y",
+                 bf16_output: bool = None):
+    """Parity check.  dtype is the I/O dtype of the call; bf16_output says
+    whether `got` was stored in bf16 (default: y in a bf16 call yes, the fp32
+    state no)."""
+    st = err_stats(got, ref)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    if dtype == synth.F32:
+        assert st["max_abs"] <= TOL_F32_ABS, f"{what}: {st}"
+        return st
+    if bf16_output is None:
+        bf16_output = not what.startswith(("final", "state", "decode state"))
+    assert st["rms_rel"] <= TOL_BF16_REL_RMS, f"{what}: {st}"
+    if bf16_output:
+        assert st["max_beyond_bf16_rounding_rel_rms"] <= TOL_BF16_REL_RMS, f"{what}: {st}"
+    else:
+        assert st["max_rel_rms"] <= TOL_BF16_REL_RMS, f"{what}: {st}"
+    return st

@@ -1,0 +1,146 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/mamba_scan.h declares, and rejects bad arguments on
+the host before touching the device."""
+
+import os
+import re
+
+import pytest
+
+import selective_state_space_135_b300 as mm
+from selective_state_space_135_b300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mamba_scan.h")
+
+OK, ENULL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EALLOC, EDTYPE, EALIAS = 0, -1, -2, -3, -4, -5, -6, -7, -8
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mamba_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("mamba_scan_fwd", "mamba_state_update", "mamba_status_string"):
+        assert n in names
+    assert set(names) == set(_lib.EXPORTS), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in (OK, ENULL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EALLOC, EDTYPE, EALIAS):
+        s = mm.mamba_status_string(code)
+        assert s and s != "unknown status"
+    assert mm.mamba_status_string(12345) == "unknown status"
+    assert mm.mamba_version() >= 100
+
+
+# Fake, well-aligned device addresses: validation must reject the call before
+# anything dereferences them.
+BASE = 1 << 40
+
+
+def addr(i, extra=0):
+    return BASE + i * (1 << 32) + extra
+
+
+def scan_call(lib, batch=2, dim=16, dstate=4, seqlen=64, io=1, u=1, delta=2, dtb=3, A=4, B=5,
+              C=6, Dk=7, z=8, softplus=1, y=9, fin=10, extra=None):
+    ptrs = dict(u=u, delta=delta, dtb=dtb, A=A, B=B, C=C, Dk=Dk, z=z, y=y, fin=fin)
+    vals = {k: (None if v is None else addr(v, (extra or {}).get(k, 0))) for k, v in ptrs.items()}
+    return lib.mamba_scan_fwd(batch, dim, dstate, seqlen, io, vals["u"], vals["delta"],
+                              vals["dtb"], vals["A"], vals["B"], vals["C"], vals["Dk"],
+                              vals["z"], softplus, vals["y"], vals["fin"], None)
+
+
+def test_scan_rejects_bad_shapes(lib):
+    assert scan_call(lib, dstate=0) == ESHAPE
+    assert scan_call(lib, dstate=17) == ESHAPE
+    assert scan_call(lib, batch=0) == ESHAPE
+    assert scan_call(lib, dim=0) == ESHAPE
+    assert scan_call(lib, seqlen=-1) == ESHAPE
+    assert scan_call(lib, io=5) == EDTYPE
+
+
+def test_scan_rejects_null_required(lib):
+    for k in ("u", "delta", "A", "B", "C", "y"):
+        assert scan_call(lib, **{k: None}) == ENULL, k
+
+
+def test_scan_rejects_misaligned(lib):
+    # bf16 tensors need 2-byte alignment, fp32 ones 4-byte alignment
+    assert scan_call(lib, extra={"u": 1}) == EALIGN
+    assert scan_call(lib, extra={"y": 1}) == EALIGN
+    assert scan_call(lib, io=0, extra={"B": 2}) == EALIGN
+    assert scan_call(lib, extra={"A": 2}) == EALIGN
+    assert scan_call(lib, extra={"fin": 2}) == EALIGN
+
+
+def test_scan_rejects_aliasing(lib):
+    assert scan_call(lib, y=1) == EALIAS        # y on top of u
+    assert scan_call(lib, fin=4) == EALIAS      # final_state on top of A
+    assert scan_call(lib, fin=9) == EALIAS      # final_state on top of y
+
+
+def test_scan_nullable_inputs_pass_validation(lib):
+    # with every nullable pointer absent the call gets past validation and, on a
+    # machine without a GPU, fails only at the CUDA layer
+    rc = scan_call(lib, dtb=None, Dk=None, z=None, fin=None)
+    assert rc in (ECUDA, OK)
+
+
+def step_call(lib, batch=2, dim=8, dstate=16, io=1, state=1, x=2, delta=3, dtb=4, A=5, B=6, C=7,
+              Dk=8, z=9, y=10, extra=None):
+    ptrs = dict(state=state, x=x, delta=delta, dtb=dtb, A=A, B=B, C=C, Dk=Dk, z=z, y=y)
+    vals = {k: (None if v is None else addr(v, (extra or {}).get(k, 0))) for k, v in ptrs.items()}
+    return lib.mamba_state_update(batch, dim, dstate, io, vals["state"], vals["x"], vals["delta"],
+                                  vals["dtb"], vals["A"], vals["B"], vals["C"], vals["Dk"],
+                                  vals["z"], vals["y"], None)
+
+
+def test_state_update_validation(lib):
+    assert step_call(lib, dstate=17) == ESHAPE
+    assert step_call(lib, batch=0) == ESHAPE
+    assert step_call(lib, io=2) == EDTYPE
+    for k in ("state", "x", "delta", "A", "B", "C", "y"):
+        assert step_call(lib, **{k: None}) == ENULL, k
+    assert step_call(lib, extra={"state": 2}) == EALIGN
+    assert step_call(lib, extra={"x": 1}) == EALIGN
+    assert step_call(lib, y=1) == EALIAS
+    assert step_call(lib, x=1) == EALIAS       # state overlaps x
+    assert step_call(lib, dtb=None, Dk=None, z=None) in (ECUDA, OK)
+
+
+def test_tuning_validation(lib):
+    assert lib.mamba_scan_set_tuning(3, 0, 0) == ESHAPE
+    assert lib.mamba_scan_set_tuning(4, 0, 0) == ESHAPE
+    assert lib.mamba_scan_set_tuning(0, 9, 0) == ESHAPE
+    assert lib.mamba_scan_set_tuning(0, 0, -1) == ESHAPE
+    assert lib.mamba_scan_set_tuning(0, 0, 0) == OK
+
+
+def test_profiler_without_launches(lib):
+    mm.mamba_profile_begin()
+    prof = mm.mamba_profile_end()
+    assert set(prof) == set(_lib.KIND_NAMES)
+    assert all(v == (0.0, 0) for v in prof.values())
+
+
+def test_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    u = torch.zeros(1, 4, 8)
+    with pytest.raises(ValueError):
+        mm.mamba_scan_fwd(u, u, None, torch.zeros(4, 2), torch.zeros(1, 2, 8),
+                          torch.zeros(1, 2, 8), None, None)
