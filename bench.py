@@ -41,9 +41,15 @@ UNIT = "elems/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "scan_traffic.json")
 KERNEL_SRC = os.path.join(ROOT, "selective_state_space_135_b300", "csrc", "mamba_scan.cu")
-# MUFU ex2 issue rate per SM per clock on B300, measured with a pipe
-# microbenchmark (profiles/pipes_b300.md); 148 SMs.
-MUFU_PER_CLK_SM = 32
+# Per-SM unit counts of B300 (sm_103): 128 fp32 lanes (one fp32 multiply or
+# FMA per lane per clock, packed f32x2 included) and 32 ex2 results per clock
+# on the special-function units; 148 SMs.  One state update of the scan
+# (one (b, d, t, n) element) needs 4 fp32 lane operations (Delta*A, Delta*u*B,
+# the state FMA, the C.h FMA) and one ex2, so both units give the same peak:
+# 148 * 32 * f_sm state updates per second.
+FP32_LANES_PER_SM = 128
+FP32_OPS_PER_UPDATE = 4
+EX2_PER_CLK_SM = 32
 N_SM = 148
 FALLBACK_HBM_GBS = 6400.0
 
@@ -290,29 +296,31 @@ def run_ours(args, shape):
     k_ms = scan_ms / max(1, scan_n)
     peaks, peak_src = load_peaks()
     smax = float(peaks.get("sm_max_mhz", 2032.0))
-    bdl = shape.batch * shape.dim * shape.seqlen
-    trans_per_launch = bdl * (shape.dstate + 3)   # exp(Delta*A) per state entry + softplus + silu
-    alu_peak = MUFU_PER_CLK_SM * N_SM * smax * 1e6   # transcendental evaluations / s
-    alu_achieved = trans_per_launch / (k_ms * 1e-3)
+    updates = shape.batch * shape.dim * shape.seqlen * shape.dstate
+    alu_peak = min(FP32_LANES_PER_SM / FP32_OPS_PER_UPDATE, EX2_PER_CLK_SM) * N_SM * smax * 1e6
+    alu_achieved = updates / (k_ms * 1e-3)
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     hbm_achieved = shape.io_bytes() / (k_ms * 1e-3) / 1e9
+    traffic = load_traffic(shape.name)
     roofline = {
         "bound": "alu",
-        "achieved": alu_achieved / 1e12, "peak": alu_peak / 1e12, "unit": "Texp/s",
-        "frac": alu_achieved / alu_peak, "traffic": load_traffic(shape.name),
+        "achieved": alu_achieved / 1e12, "peak": alu_peak / 1e12, "unit": "T state-updates/s",
+        "frac": alu_achieved / alu_peak, "traffic": traffic,
         "kernel": "scan_kernel (main pass)", "kernel_ms": k_ms,
-        "peak_source": f"MUFU ex2 {MUFU_PER_CLK_SM}/clk/SM measured x {N_SM} SMs x "
+        "peak_source": f"{N_SM} SMs x min({FP32_LANES_PER_SM} fp32 lanes / "
+                       f"{FP32_OPS_PER_UPDATE} ops, {EX2_PER_CLK_SM} ex2) per clock x "
                        f"{smax:.0f} MHz ({peak_src} sm_max)",
-        "work_per_launch": f"{trans_per_launch:.4g} exp/log evaluations (B*D*L*(N+3))",
+        "work_per_launch": f"{updates:.4g} state updates (B*D*L*N)",
         "hbm": {"achieved": hbm_achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": hbm_achieved / hbm_peak, "peak_source": peak_src,
-                "algorithmic_bytes_per_launch": shape.io_bytes()},
+                "algorithmic_bytes_per_launch": shape.io_bytes(),
+                "traffic_per_launch": traffic},
     }
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (bf16 I/O)", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_dict(shape, ws),
         "roofline": roofline,
         "gpu_launches": launches,

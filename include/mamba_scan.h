@@ -87,10 +87,13 @@ typedef enum {
  *   y           : (batch, dim, seqlen)    io_dtype     written
  *   final_state : (batch, dim, dstate)    fp32         nullable; h after the last step
  *
- * When the channels alone cannot fill the GPU, the sequence is split into
- * time chunks that run in parallel; a carry pass composes their (decay,
- * state) pairs.  The carry buffers are scratch memory obtained
- * stream-ordered from a library-owned pool on `stream`.
+ * Every call first packs B and C into an fp32 per-step table (batch *
+ * seqlen * 32 floats at most) that the scan kernel streams.  When the
+ * channels alone cannot fill the GPU, the sequence is also split into time
+ * chunks that run in parallel; a carry pass composes their (decay, state)
+ * pairs.  The table and the carry buffers are scratch memory obtained
+ * stream-ordered from a library-owned pool on `stream` and returned to it
+ * on the same stream.
  */
 int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
                    int io_dtype,
@@ -134,14 +137,15 @@ int mamba_version(void);
 
 /*
  * Tuning override for experiments, process-wide, affecting later calls of
- * mamba_scan_fwd: split = lanes sharing one channel's state (1 or 2; used
- * when dstate > 8), stages = depth of the shared-memory input ring (1..4),
+ * mamba_scan_fwd: tail = how channel tiles that do not fill a whole wave of
+ * SMs are scheduled (0 automatic, 1 whole-sequence units only, 2 cut into
+ * time chunks), stages = depth of the shared-memory input ring (1..4),
  * chunks = fixed number of time chunks for every channel tile.  0 restores
  * the automatic choice for that knob.  Results do not depend on these
  * settings beyond fp32 rounding order.  Returns MAMBA_ERR_SHAPE for values
  * out of range.
  */
-int mamba_scan_set_tuning(int split, int stages, int chunks);
+int mamba_scan_set_tuning(int tail, int stages, int chunks);
 
 /*
  * Per-launch timing (process-wide).  After mamba_profile_begin, every kernel
@@ -149,7 +153,8 @@ int mamba_scan_set_tuning(int split, int stages, int chunks);
  * mamba_profile_end stops recording, waits for those events and writes, for
  * each kernel kind k < nkinds, the summed device time in milliseconds
  * (total_ms[k]) and the number of launches (launches[k]).  Kinds:
- * 0 = scan, 1 = chunk summary, 2 = chunk carry, 3 = state update.
+ * 0 = scan, 1 = chunk summary, 2 = chunk carry, 3 = state update,
+ * 4 = B/C packing (one per scan call).
  * Either output may be NULL.  Not meant for use during stream capture.
  */
 int mamba_profile_begin(void);

@@ -19,7 +19,7 @@ EXPORTS = ("mamba_scan_fwd", "mamba_state_update", "mamba_status_string",
            "mamba_device_status", "mamba_version", "mamba_scan_set_tuning",
            "mamba_profile_begin", "mamba_profile_end")
 
-KIND_NAMES = ("scan", "chunk_summary", "chunk_carry", "state_update")
+KIND_NAMES = ("scan", "chunk_summary", "chunk_carry", "state_update", "pack_bc")
 
 
 class MambaError(RuntimeError):
@@ -190,8 +190,8 @@ def mamba_device_status(stream=None) -> int:
     return lib.mamba_device_status(_stream_handle(stream, dev))
 
 
-def mamba_scan_set_tuning(split: int = 0, stages: int = 0, chunks: int = 0) -> None:
-    rc = load().mamba_scan_set_tuning(int(split), int(stages), int(chunks))
+def mamba_scan_set_tuning(tail: int = 0, stages: int = 0, chunks: int = 0) -> None:
+    rc = load().mamba_scan_set_tuning(int(tail), int(stages), int(chunks))
     if rc != 0:
         raise MambaError(rc, "mamba_scan_set_tuning")
 

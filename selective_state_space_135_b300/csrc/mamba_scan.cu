@@ -9,33 +9,39 @@
 //   h[n]  = exp(Delta*A[d,n]) * h[n] + Delta*B[b,n,t]*u[b,d,t]
 //   y     = (sum_n C[b,n,t]*h[n] + D_skip[d]*u[b,d,t]) * silu(z[b,d,t])
 //
-// Design (one GPU, no tensor cores: the work is an elementwise recurrence):
-//   * A CTA (4 warps) owns a tile of channels of one batch entry and walks
-//     time.  Each thread keeps NT state entries of one channel in registers;
-//     with dstate > 8 two lanes share a channel (8 entries each) and split the
-//     per-step scalar work (Delta, Delta*u, skip term, gate) between them.
-//   * Inputs stream through a shared-memory ring filled by tensor-map bulk
-//     copies (cp.async.bulk.tensor, completion on an mbarrier): one
-//     [channels x 64 bytes of time] box per tensor per tile, 64-byte
-//     swizzled so every thread's 16-byte row reads are bank-conflict free.
-//     Output tiles leave the same way (double-buffered, bulk-group stores).
-//     Shapes whose rows are not 16-byte multiples run the same kernels with
-//     plain, bounds-checked element loads and stores into the same layout.
-//   * B and C (shared by all channels of a batch entry) are widened once per
-//     tile into an fp32 [t][n] table read with broadcast 128-bit loads.
+// Design (one GPU, no tensor cores: the work is an elementwise recurrence
+// whose cost is one exp and four fp32 multiply/adds per state entry and step):
+//   * A CTA is four warps (one per SM sub-partition) over 64 channels of
+//     one batch entry.  Two warps share each block of 32 channels, one lane
+//     per channel, each warp holding half of the N state entries in
+//     registers, so a B/C load of a warp is a single-address broadcast and
+//     the SM still gets two warps per sub-partition on the Mamba-2.8B layer.
+//     The CTA walks time in tiles of one 64-byte row per channel (32 bf16 or
+//     16 fp32 steps).
+//   * u, delta, z and y tiles move by tensor-map bulk copies
+//     (cp.async.bulk.tensor, completion on an mbarrier ring), 64-byte swizzled
+//     so that the per-lane 16-byte row accesses are bank-conflict free.
+//   * B and C (shared by all channels of a batch entry) are packed once per
+//     call by a small kernel into fp32 rows of (B pair, C pair) per step and
+//     staged by the same bulk copies.
+//   * Per tile each half computes Delta and Delta*u for half of the steps
+//     into shared memory, both halves run the recurrence over the tile, and
+//     each half finishes half of the outputs (both partial sums C.h, skip
+//     term, gate): no per-token work is done twice.
 //   * The expanded (b, d, t, n) tensor is never materialised: Abar and the
 //     input term live only in registers; the state leaves the SM only at the
 //     end of a work unit.
-//   * Work units are whole-sequence channel tiles; when the tiles cannot fill
-//     the SMs (few channels, very long sequences) every tile is cut into time
-//     chunks: a summary pass computes each chunk's (prod Abar, end state from
-//     zero), a carry pass composes them in order, and the main pass restarts
-//     every chunk from its exact carried-in state.
-//   * fp32 I/O uses the library expf/log1pf; bf16 I/O uses the hardware
-//     ex2/lg2 approximations (relative error ~2^-22), far inside the bf16
-//     output rounding.  State and accumulation are fp32 in both.
-//   * Packed fp32x2 multiply/FMA (sm_100+) halves the instruction count of
-//     the state update; exp2 runs on the MUFU pipe alongside.
+//   * Work units are channel tiles over the whole sequence, one wave per SM;
+//     tiles that do not fill a whole wave, and all tiles when there are fewer
+//     than SMs, are cut into time chunks: a summary pass computes each
+//     chunk's (prod Abar, end state from zero), a carry pass composes them in
+//     order, and the main pass restarts every chunk from its exact
+//     carried-in state.
+//   * bf16 I/O keeps Delta in log2 units (Delta' = Delta / ln 2, B scaled by
+//     ln 2 when packed) so that Abar = ex2(Delta' * A) needs one multiply and
+//     one hardware ex2; fp32 I/O uses the library expf/log1pf.  State and
+//     accumulation are fp32 in both.  Packed fp32x2 multiply/FMA (sm_100+)
+//     halves the instruction count of the state update.
 
 #include "mamba_scan.h"
 
@@ -60,7 +66,7 @@ namespace mamba {
 
 __device__ int g_error_word;  // nonzero once a bounded device wait gave up
 
-constexpr int kThreads = 128;        // threads per CTA (4 warps)
+constexpr int kThreads = 128;        // threads per CTA of the state-update kernel
 constexpr int kMaxStages = 4;
 constexpr int kMaxN = 16;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
@@ -128,11 +134,19 @@ __device__ __forceinline__ float softplus_f(float s) {
     return s > 20.0f ? s : r;
 }
 
-// silu(z) = z * sigmoid(z) = z / (1 + e^-z)
+// silu(z) = z * sigmoid(z).  Accurate path: z / (1 + e^-z).  Fast path:
+// sigmoid(z) = (1 + tanh(z/2)) / 2, so silu(z) = h + h * tanh(h) with h = z/2,
+// one hardware tanh (max relative error about 2^-11).
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 template <bool ACC>
 __device__ __forceinline__ float silu_f(float z) {
     if (ACC) return z / (1.0f + expf(-z));
-    return __fdividef(z, 1.0f + ex2_approx(-z * kLog2e));
+    const float h = 0.5f * z;
+    return fmaf(h, tanh_approx(h), h);
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -176,8 +190,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-__device__ __forceinline__ void bulk_wait_read_1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+__device__ __forceinline__ void bulk_wait_read_0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -186,12 +200,8 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// ---------------------------------------------------------------------------
-// scan kernels
-// ---------------------------------------------------------------------------
-
 // Tensor-map copies (cp.async.bulk.tensor): one instruction moves a whole
-// [channels x time] box between global and shared memory.
+// box between global and shared memory.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             int c2, uint32_t bar) {
     asm volatile(
@@ -211,13 +221,70 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// scan kernels
+// ---------------------------------------------------------------------------
+
+constexpr int kScanWarps = 4;                    // warps per CTA, one per SM sub-partition
+constexpr int kHalves = 2;                       // warps sharing a channel, half the state each
+constexpr int kCH = 32 * kScanWarps / kHalves;   // channels per CTA
+
+// One 16-byte chunk of a row <-> fp32 values (8 for bf16, 4 for fp32).
+template <typename T> struct Chunk;
+template <> struct Chunk<float> {
+    static constexpr int G = 4;
+    __device__ static void load(const unsigned char* p, float* v) {
+        const float4 r = *reinterpret_cast<const float4*>(p);
+        v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
+    }
+    __device__ static void store(unsigned char* p, const float* v) {
+        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+};
+template <> struct Chunk<__nv_bfloat16> {
+    static constexpr int G = 8;
+    __device__ static void load(const unsigned char* p, float* v) {
+        IO<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(p), v);
+    }
+    __device__ static void store(unsigned char* p, const float* v) {
+        *reinterpret_cast<uint4*>(p) = IO<__nv_bfloat16>::pack(v);
+    }
+};
+
+// Packs B and C of every step into one fp32 row of 2*NP values, in the order
+// the scan reads them: for each pair j of state entries the float4
+// (s*B[2j], s*B[2j+1], C[2j], C[2j+1]); entries n >= N are zero.  s is ln 2
+// when the scan keeps Delta in log2 units, else 1.  One thread per
+// (batch, step, pair); consecutive threads read consecutive steps.
+template <typename T>
+__global__ void pack_bc_kernel(const T* __restrict__ B, const T* __restrict__ C,
+                               float4* __restrict__ out, long long batch, long long L, int N,
+                               int NP, float scale) {
+    const int half = NP / 2;
+    const long long total = batch * L * half;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long bj = i / L, t = i - bj * L;   // bj = b * half + j
+        const long long b = bj / half;
+        const int j = (int)(bj - b * half);
+        const int n0 = 2 * j, n1 = 2 * j + 1;
+        const T* Bb = B + b * N * L + t;
+        const T* Cb = C + b * N * L + t;
+        float4 v;
+        v.x = n0 < N ? scale * IO<T>::to_f(Bb[(long long)n0 * L]) : 0.0f;
+        v.y = n1 < N ? scale * IO<T>::to_f(Bb[(long long)n1 * L]) : 0.0f;
+        v.z = n0 < N ? IO<T>::to_f(Cb[(long long)n0 * L]) : 0.0f;
+        v.w = n1 < N ? IO<T>::to_f(Cb[(long long)n1 * L]) : 0.0f;
+        out[(b * L + t) * half + j] = v;
+    }
+}
+
 struct ScanArgs {
-    CUtensorMap m_u, m_dl, m_z, m_y, m_B, m_C;   // valid when use_tma
+    CUtensorMap m_u, m_dl, m_z, m_y, m_bc;   // valid when use_tma
     const void* u;
     const void* delta;
     const void* z;
-    const void* B;
-    const void* C;
+    const float4* bc;  // packed B/C rows [batch][seqlen][NP / 2]
     const float* dt_bias;
     const float* A;
     const float* D_skip;
@@ -232,11 +299,11 @@ struct ScanArgs {
     int dstate;
     int use_tma;
     int stages;
-    int groups_per_batch;  // ceil(dim / CH)
+    int groups_per_batch;  // ceil(dim / kCH)
     int n_groups;          // batch * groups_per_batch
     int n_full;            // groups [0, n_full) run the whole sequence
     int nchunks;           // time chunks of each remaining ("tail") group
-    int tail_rows;         // (n_groups - n_full) * CH
+    int tail_rows;         // (n_groups - n_full) * kCH
 };
 
 // Work unit of one CTA.
@@ -250,7 +317,7 @@ struct Unit {
 // Units are numbered: [0, n_full) whole-sequence groups, then every chunk of
 // every tail group.  The summary pass numbers only the chunks that feed the
 // carry (all but the last of each tail group).
-template <int CH, bool STATE_ONLY>
+template <bool STATE_ONLY>
 __device__ __forceinline__ Unit decode_unit(const ScanArgs& a, int idx) {
     Unit w;
     int g;
@@ -267,7 +334,7 @@ __device__ __forceinline__ Unit decode_unit(const ScanArgs& a, int idx) {
         w.k = j % a.nchunks;
     }
     w.b = g / a.groups_per_batch;
-    w.d0 = (g % a.groups_per_batch) * CH;
+    w.d0 = (g % a.groups_per_batch) * kCH;
     if (g < a.n_full) {
         w.tail = -1;
         w.t0 = 0;
@@ -284,24 +351,29 @@ __device__ __forceinline__ Unit decode_unit(const ScanArgs& a, int idx) {
 // time tile is one 64-byte row; rows of the u/delta/z/y tiles are stored
 // with the 64-byte swizzle of the tensor-map copies: the 16-byte chunk j of
 // row r sits at r*64 + ((j ^ ((r >> 1) & 3)) << 4), which makes the
-// per-thread 16-byte row reads and writes bank-conflict free.
-//   [0, 1024)           stage mbarriers
-//   stage s             u | delta | z tiles (CH x 64 B each) | B raw | C raw (16 x 64 B each)
-//   BC table            TT x {B, C} x 16 fp32
-//   y tiles             2 x CH x 64 B
-template <int CH>
-struct Layout {
-    static constexpr int kTile = CH * 64;
-    static constexpr int kBoff = 3 * kTile;
-    static constexpr int kCoff = kBoff + kMaxN * 64;
-    static constexpr int kStage = (kCoff + kMaxN * 64 + 1023) / 1024 * 1024;
+// per-lane 16-byte row accesses of a warp bank-conflict free.
+//   [0, 1024)       stage mbarriers
+//   stage s         u | delta | z tiles (kCH x 64 B each) | packed B/C (TT x 2*NP fp32)
+//   y tile          kCH x 64 B
+//   du              (Delta, Delta*u) of every (step, channel) of a tile, float2
+//   part            sum_n C*h of each half of the state, [2][TT][kCH] fp32
+template <typename T, int NT>
+struct ScanLayout {
+    static constexpr int NP = kHalves * NT;           // padded state size
+    static constexpr int kTT = 64 / (int)sizeof(T);   // steps per tile
+    static constexpr int kG = 16 / (int)sizeof(T);    // steps per 16-byte chunk
+    static constexpr int kRows = kCH * 64;
+    static constexpr int kBCBytes = kTT * 2 * NP * 4;
+    static constexpr int kBC = (kBCBytes + 1023) / 1024 * 1024;
+    static constexpr int kStage = 3 * kRows + kBC;
+    static constexpr int kDU = kTT * kCH * 8;
+    static constexpr int kPart = kHalves * kTT * kCH * 4;
     __host__ __device__ static constexpr int stage(int s) { return 1024 + s * kStage; }
-    __host__ __device__ static constexpr int bct(int stages) { return 1024 + stages * kStage; }
-    __host__ __device__ static constexpr int ybuf(int stages, int tt) {
-        return (bct(stages) + tt * 2 * kMaxN * 4 + 1023) / 1024 * 1024;
-    }
-    __host__ __device__ static constexpr int bytes(int stages, int tt) {
-        return ybuf(stages, tt) + 2 * kTile + 1024;   // + slack to align the base
+    __host__ __device__ static constexpr int ybuf(int stages) { return stage(stages); }
+    __host__ __device__ static constexpr int du(int stages) { return ybuf(stages) + kRows; }
+    __host__ __device__ static constexpr int part(int stages) { return du(stages) + kDU; }
+    __host__ __device__ static constexpr int bytes(int stages) {
+        return part(stages) + kPart + 1024;   // + slack to align the base
     }
 };
 
@@ -309,94 +381,114 @@ __device__ __forceinline__ int swz(int row, int chunk) {
     return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
 }
 
-// One time step of NT state entries (NT/2 packed pairs) of one channel:
-//   h <- exp(Delta*A) * h + (Delta*u) * B ;  returns sum_n C*h over the NT entries.
-template <int NT, bool ACC, bool STATE_ONLY>
-__device__ __forceinline__ float ssm_step(float2 (&h2)[NT / 2], const float2 (&a2)[NT / 2],
-                                          float dt, float du, const float* brow,
-                                          const float* crow) {
+// Abar = exp(Delta * A) of one step for the NT state entries (NT/2 pairs).
+// Fast path: dt is Delta / ln 2, so Abar = ex2(dt * A).
+template <int NT, bool ACC>
+__device__ __forceinline__ void abar_step(float2 (&ab)[NT / 2], const float2 (&a2)[NT / 2],
+                                          float dt) {
     const float2 dt2 = make_float2(dt, dt);
-    const float2 du2 = make_float2(du, du);
-    float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
-    if constexpr (NT == 2) {
-        const float2 b2 = *reinterpret_cast<const float2*>(brow);
-        float2 dA;
+#pragma unroll
+    for (int i = 0; i < NT / 2; ++i) {
         if constexpr (ACC) {
-            dA = make_float2(expf(dt * a2[0].x), expf(dt * a2[0].y));
+            ab[i] = make_float2(expf(dt * a2[i].x), expf(dt * a2[i].y));
         } else {
-            const float2 arg = __fmul2_rn(dt2, a2[0]);
-            dA = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
-        }
-        h2[0] = __ffma2_rn(dA, h2[0], __fmul2_rn(du2, b2));
-        if constexpr (!STATE_ONLY) acc0 = __fmul2_rn(*reinterpret_cast<const float2*>(crow), h2[0]);
-    } else {
-#pragma unroll
-        for (int q = 0; q < NT / 4; ++q) {
-            const float4 b4 = *reinterpret_cast<const float4*>(brow + 4 * q);
-            float4 c4;
-            if constexpr (!STATE_ONLY) c4 = *reinterpret_cast<const float4*>(crow + 4 * q);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int i = 2 * q + j;
-                const float2 bp = j ? make_float2(b4.z, b4.w) : make_float2(b4.x, b4.y);
-                float2 dA;
-                if constexpr (ACC) {
-                    dA = make_float2(expf(dt * a2[i].x), expf(dt * a2[i].y));
-                } else {
-                    const float2 arg = __fmul2_rn(dt2, a2[i]);
-                    dA = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
-                }
-                h2[i] = __ffma2_rn(dA, h2[i], __fmul2_rn(du2, bp));
-                if constexpr (!STATE_ONLY) {
-                    const float2 cp = j ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
-                    if (j) acc1 = __ffma2_rn(cp, h2[i], acc1);
-                    else acc0 = __ffma2_rn(cp, h2[i], acc0);
-                }
-            }
+            const float2 arg = __fmul2_rn(dt2, a2[i]);
+            ab[i] = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
         }
     }
-    return (acc0.x + acc1.x) + (acc0.y + acc1.y);
 }
 
-// The scan over one work unit (CH channels x a time range).  STATE_ONLY is
-// the chunk-summary pass: no C, z or y; it returns (exp(A*sum Delta), h_end).
-template <typename T, int NT, int S, bool STATE_ONLY, bool SOFTPLUS, bool HAS_Z>
-__global__ void __launch_bounds__(kThreads)
+// One time step of the NT state entries of one channel given Abar:
+//   h <- Abar * h + (Delta*u) * B ;  returns sum_n C*h.
+// bc holds the step's NT/2 float4 (B pair, C pair), the same for every lane
+// of the warp (on the fast path B carries the factor ln 2 that turns the
+// log2-unit du back into Delta*u).  All input terms are formed before the
+// state updates, and two accumulators halve the dependent chain.
+template <int NT, bool STATE_ONLY>
+__device__ __forceinline__ float state_step(float2 (&h2)[NT / 2], const float2 (&ab)[NT / 2],
+                                            float du, const float4 (&bc)[NT / 2]) {
+    const float2 du2 = make_float2(du, du);
+    float2 bx[NT / 2];
+#pragma unroll
+    for (int i = 0; i < NT / 2; ++i) bx[i] = __fmul2_rn(du2, make_float2(bc[i].x, bc[i].y));
+#pragma unroll
+    for (int i = 0; i < NT / 2; ++i) h2[i] = __ffma2_rn(ab[i], h2[i], bx[i]);
+    if constexpr (STATE_ONLY) {
+        return 0.0f;
+    } else {
+        float2 acc0 = __fmul2_rn(make_float2(bc[0].z, bc[0].w), h2[0]);
+        if constexpr (NT == 2) {
+            return acc0.x + acc0.y;
+        } else {
+            float2 acc1 = __fmul2_rn(make_float2(bc[1].z, bc[1].w), h2[1]);
+#pragma unroll
+            for (int i = 2; i < NT / 2; i += 2) {
+                acc0 = __ffma2_rn(make_float2(bc[i].z, bc[i].w), h2[i], acc0);
+                acc1 = __ffma2_rn(make_float2(bc[i + 1].z, bc[i + 1].w), h2[i + 1], acc1);
+            }
+            const float2 acc = __fadd2_rn(acc0, acc1);
+            return acc.x + acc.y;
+        }
+    }
+}
+
+template <int NT>
+__device__ __forceinline__ void load_bc(float4 (&bc)[NT / 2], const float4* row) {
+#pragma unroll
+    for (int i = 0; i < NT / 2; ++i) bc[i] = row[i];
+}
+
+// The scan over one work unit (kCH channels x a time range).  Warp w holds
+// channels [32*(w & 1), 32*(w & 1) + 32) of the tile, one lane per channel,
+// and state entries [NT*(w >> 1), NT*(w >> 1) + NT) of each: the two warps of
+// a channel block split the state, so every B/C load of a warp is a
+// single-address broadcast.  Per tile:
+//   (1) each half computes Delta and Delta*u for half of the steps into
+//       shared memory (no per-token work is done twice);
+//   (2) both halves run the recurrence over all steps of the tile and store
+//       their partial sums sum_n C*h;
+//   (3) each half finishes half of the outputs: both partial sums, skip
+//       term and gate.
+// STATE_ONLY is the chunk-summary pass: no C, z or y; it returns
+// (exp(A*sum Delta), h_end).
+template <typename T, int NT, bool STATE_ONLY, bool SOFTPLUS, bool HAS_Z>
+__global__ void __launch_bounds__(32 * kScanWarps)
 scan_kernel(const __grid_constant__ ScanArgs a) {
-    constexpr int CH = kThreads / S;             // channels per CTA
-    constexpr int G = 16 / sizeof(T);            // time steps per 16-byte chunk
-    constexpr int TT = 64 / sizeof(T);           // time steps per tile
-    constexpr int NP = NT * S;                   // padded state size
+    using Lay = ScanLayout<T, NT>;
+    using CK = Chunk<T>;
+    constexpr int NP = Lay::NP;
+    constexpr int TT = Lay::kTT, G = Lay::kG, HT = TT / kHalves;
+    constexpr int kNThr = 32 * kScanWarps;
     constexpr bool ACC = IO<T>::kAccurate;
     constexpr int kNPair = NT / 2;
-    constexpr unsigned kFull = 0xffffffffu;
     constexpr bool has_z = !STATE_ONLY && HAS_Z;
-    static_assert(NT % 2 == 0 && NP <= kMaxN && (S == 1 || S == 2), "bad state split");
-    using Lay = Layout<CH>;
+    static_assert(NT % 2 == 0 && NP <= kMaxN, "bad state size");
+    static_assert(CK::G == G && HT == 2 * G, "a half tile is two 16-byte chunks");
 
     // Offset the __shared__ array itself (not a pointer rebuilt from an
     // integer) so that every access below stays a shared-memory access.
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
-    const int tid = threadIdx.x;
-    const int c = tid / S;       // channel within the tile
-    const int p = tid % S;       // which NT-slice of the state
-    const Unit w = decode_unit<CH, STATE_ONLY>(a, blockIdx.x);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hh = warp >> 1;                 // which half of the state
+    const int c = (warp & 1) * 32 + lane;     // channel within the tile
+    const Unit w = decode_unit<STATE_ONLY>(a, blockIdx.x);
     const long long dim = a.dim, L_ = a.seqlen;
     const int N = a.dstate;
     const int d = w.d0 + c;
     const bool chan_ok = d < dim;
-    const int rows_valid = (int)min((long long)CH, dim - w.d0);
+    const int rows_valid = (int)min((long long)kCH, dim - w.d0);
     const long long row = (long long)w.b * dim + d;
     const int stages = a.stages;
     const bool tma = a.use_tma != 0;
     const int ntiles = (int)((w.t1 - w.t0 + TT - 1) / TT);
-    const int wrow = (w.tail >= 0) ? w.tail * CH + c : 0;
+    const int wrow = (w.tail >= 0) ? w.tail * kCH + c : 0;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-    float* bct = reinterpret_cast<float*>(smem + Lay::bct(stages));
-    unsigned char* ybuf = smem + Lay::ybuf(stages, TT);
+    unsigned char* yt = smem + Lay::ybuf(stages);
+    float2* du_s = reinterpret_cast<float2*>(smem + Lay::du(stages));      // [TT][kCH]
+    float* part_s = reinterpret_cast<float*>(smem + Lay::part(stages));    // [2][TT][kCH]
 
     // ---- per-thread constants and initial state ----
     float2 h2[kNPair], a2[kNPair];
@@ -405,10 +497,9 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
         float av[2], hv[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const int n = p * NT + 2 * i + j;
+            const int n = hh * NT + 2 * i + j;
             const bool ok = chan_ok && n < N;
-            const float an = ok ? a.A[(long long)d * N + n] : 0.0f;
-            av[j] = ACC ? an : an * kLog2e;
+            av[j] = ok ? a.A[(long long)d * N + n] : 0.0f;
             float h0 = 0.0f;
             if (ok && w.tail >= 0 && w.k > 0 && !STATE_ONLY)
                 h0 = a.ws_h[((long long)(w.k - 1) * a.tail_rows + wrow) * N + n];
@@ -417,47 +508,45 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
         a2[i] = make_float2(av[0], av[1]);
         h2[i] = make_float2(hv[0], hv[1]);
     }
-    const float bias = (chan_ok && a.dt_bias) ? a.dt_bias[d] : 0.0f;
+    const float bias0 = (chan_ok && a.dt_bias) ? a.dt_bias[d] : 0.0f;
+    const float bias = ACC ? bias0 : bias0 * kLog2e;
     const float dsk = (chan_ok && a.D_skip) ? a.D_skip[d] : 0.0f;
     float dsum = 0.0f;  // sum of Delta over the unit (summary pass)
 
     const int ntens = has_z ? 3 : 2;
-    const int nbc = STATE_ONLY ? 1 : 2;
 
     // thread 0: tensor-map copies of tile `it` into stage `s`
     auto issue_tile = [&](int it, int s) {
         const int tt0 = (int)(w.t0 + (long long)it * TT);
         const uint32_t bar = smem_u32(&bars[s]);
         unsigned char* st = smem + Lay::stage(s);
-        mbar_arrive_expect_tx(bar, (uint32_t)(ntens * Lay::kTile + nbc * N * 64));
+        mbar_arrive_expect_tx(bar, (uint32_t)(ntens * Lay::kRows + Lay::kBCBytes));
         tma_load_3d(smem_u32(st), &a.m_u, tt0, w.d0, w.b, bar);
-        tma_load_3d(smem_u32(st + Lay::kTile), &a.m_dl, tt0, w.d0, w.b, bar);
-        if constexpr (has_z) tma_load_3d(smem_u32(st + 2 * Lay::kTile), &a.m_z, tt0, w.d0, w.b, bar);
-        tma_load_3d(smem_u32(st + Lay::kBoff), &a.m_B, tt0, 0, w.b, bar);
-        if (!STATE_ONLY) tma_load_3d(smem_u32(st + Lay::kCoff), &a.m_C, tt0, 0, w.b, bar);
+        tma_load_3d(smem_u32(st + Lay::kRows), &a.m_dl, tt0, w.d0, w.b, bar);
+        if constexpr (has_z)
+            tma_load_3d(smem_u32(st + 2 * Lay::kRows), &a.m_z, tt0, w.d0, w.b, bar);
+        tma_load_3d(smem_u32(st + 3 * Lay::kRows), &a.m_bc, 0, tt0, w.b, bar);
     };
 
     // all threads: element-wise, bounds-checked fill of stage 0 (any shape)
     auto plain_tile = [&](int it) {
         const long long tt0 = w.t0 + (long long)it * TT;
-        const int nv = (int)min((long long)TT, w.t1 - tt0);
+        const int nv = (int)min((long long)TT, L_ - tt0);
         unsigned char* st = smem + Lay::stage(0);
-        for (int e = tid; e < ntens * CH * TT; e += kThreads) {
-            const int tsr = e / (CH * TT), rem = e % (CH * TT);
+        for (int e = tid; e < ntens * kCH * TT; e += kNThr) {
+            const int tsr = e / (kCH * TT), rem = e % (kCH * TT);
             const int cc = rem / TT, t = rem % TT;
             const T* src = static_cast<const T*>(tsr == 0 ? a.u : (tsr == 1 ? a.delta : a.z));
             T v = IO<T>::from_f(0.0f);
             if (cc < rows_valid && t < nv) v = src[((long long)w.b * dim + w.d0 + cc) * L_ + tt0 + t];
             const int byte = t * (int)sizeof(T);
-            *reinterpret_cast<T*>(st + tsr * Lay::kTile + swz(cc, byte >> 4) + (byte & 15)) = v;
+            *reinterpret_cast<T*>(st + tsr * Lay::kRows + swz(cc, byte >> 4) + (byte & 15)) = v;
         }
-        for (int e = tid; e < nbc * N * TT; e += kThreads) {
-            const int which = e / (N * TT), rem = e % (N * TT);
-            const int n = rem / TT, t = rem % TT;
-            const T* src = static_cast<const T*>(which ? a.C : a.B);
-            T v = IO<T>::from_f(0.0f);
-            if (t < nv) v = src[((long long)w.b * N + n) * L_ + tt0 + t];
-            reinterpret_cast<T*>(st + (which ? Lay::kCoff : Lay::kBoff) + n * 64)[t] = v;
+        float4* bcs = reinterpret_cast<float4*>(st + 3 * Lay::kRows);
+        for (int e = tid; e < TT * (NP / 2); e += kNThr) {
+            const int t = e / (NP / 2), j = e % (NP / 2);
+            bcs[e] = t < nv ? a.bc[((long long)w.b * L_ + tt0 + t) * (NP / 2) + j]
+                            : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
     };
 
@@ -467,12 +556,9 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
             fence_mbar_init();
             prefetch_map(&a.m_u);
             prefetch_map(&a.m_dl);
-            prefetch_map(&a.m_B);
+            prefetch_map(&a.m_bc);
             if constexpr (has_z) prefetch_map(&a.m_z);
-            if (!STATE_ONLY) {
-                prefetch_map(&a.m_C);
-                prefetch_map(&a.m_y);
-            }
+            if (!STATE_ONLY) prefetch_map(&a.m_y);
         }
         __syncthreads();
         if (tid == 0)
@@ -485,116 +571,121 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     for (int it = 0; it < ntiles; ++it) {
         const int s = tma ? it % stages : 0;
         const long long tt0 = w.t0 + (long long)it * TT;
-        const int nv = (int)min((long long)TT, w.t1 - tt0);
-        unsigned char* st = smem + Lay::stage(s);
+        const int nv = (int)min((long long)TT, w.t1 - tt0);   // steps of this unit in the tile
+        const unsigned char* st = smem + Lay::stage(s);
 
         bool timed_out = false;
         if (tma) {
             timed_out = !mbar_wait_bounded(smem_u32(&bars[s]), (uint32_t)((it / stages) & 1));
-            if (!STATE_ONLY && tid == 0) bulk_wait_read_1();   // y tile (it & 1) free again
         } else {
             plain_tile(it);
-            __syncthreads();
         }
-
-        // widen B and C of this tile into the fp32 [t][{B,C}][n] table
-        for (int e = tid; e < TT * 2 * NP; e += kThreads) {
-            const int t = e / (2 * NP), which = (e / NP) & 1, n = e % NP;
-            float v = 0.0f;
-            if (n < N && t < nv && (which == 0 || !STATE_ONLY))
-                v = IO<T>::to_f(reinterpret_cast<const T*>(
-                    st + (which ? Lay::kCoff : Lay::kBoff) + n * 64)[t]);
-            bct[(t * 2 + which) * kMaxN + n] = v;
-        }
-        if (__syncthreads_or(timed_out)) {   // (A)
+        if (__syncthreads_or(timed_out)) {
             aborted = true;
             break;
         }
 
         const unsigned char* ut = st;
-        const unsigned char* dlt = st + Lay::kTile;
-        const unsigned char* zt = st + 2 * Lay::kTile;
-        unsigned char* yt = ybuf + (it & 1) * Lay::kTile;
+        const unsigned char* dlt = st + Lay::kRows;
+        const unsigned char* zt = st + 2 * Lay::kRows;
+        const float4* bct = reinterpret_cast<const float4*>(st + 3 * Lay::kRows) + hh * kNPair;
 
-        auto body = [&](auto masked) {
-            constexpr bool MASK = decltype(masked)::value;
-#pragma unroll 1
-            for (int grp = 0; grp < TT / G; ++grp) {
-                const int off = swz(c, grp);
-                float uv[G], dv[G], zv[G];
-                IO<T>::unpack(*reinterpret_cast<const uint4*>(ut + off), uv);
-                IO<T>::unpack(*reinterpret_cast<const uint4*>(dlt + off), dv);
-                if constexpr (has_z) IO<T>::unpack(*reinterpret_cast<const uint4*>(zt + off), zv);
-                float dtv[G], duv[G];
-                if constexpr (S == 1) {
+        // (1) Delta (log2 units on the fast path) and Delta*u of this half's
+        //     steps [hh*HT, hh*HT + HT): independent chains, back to back
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const float sarg = dv[g] + bias;
-                        float dt = SOFTPLUS ? softplus_f<ACC>(sarg) : sarg;
-                        if (MASK && grp * G + g >= nv) dt = 0.0f;
-                        dtv[g] = dt;
-                        duv[g] = dt * uv[g];
-                        if (STATE_ONLY) dsum += dt;
-                    }
+        for (int q = 0; q < 2; ++q) {
+            const int ck = hh * 2 + q;
+            const int off = swz(c, ck);
+            float uv[G], dv[G];
+            CK::load(dlt + off, dv);
+            CK::load(ut + off, uv);
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                float v;
+                if constexpr (ACC) {
+                    const float sarg = dv[j] + bias;
+                    v = SOFTPLUS ? (sarg > 20.0f ? sarg : log1pf(expf(sarg))) : sarg;
                 } else {
-                    // the two lanes of a channel each evaluate Delta for every
-                    // other step and swap results
+                    // s * log2(e); softplus in log2 units: log2(1 + 2^tl)
+                    const float tl = fmaf(dv[j], kLog2e, bias);
+                    v = SOFTPLUS ? (tl > 30.0f ? tl : lg2_approx(1.0f + ex2_approx(tl))) : tl;
+                }
+                const int t = ck * G + j;
+                if (t >= nv) v = 0.0f;   // past the end of the unit: the state is kept
+                du_s[t * kCH + c] = make_float2(v, v * uv[j]);
+            }
+        }
+        __syncthreads();
+
+        // (2) the recurrence over the tile for this half of the state; the
+        //     inputs and Abar of step t+1 are fetched while step t updates
+        float own[HT];   // partial sums of the steps this half finishes
+        (void)own;
+        {
+            float2 dd = du_s[c];
+            float2 ab[kNPair];
+            float4 bc[kNPair];
+            abar_step<NT, ACC>(ab, a2, dd.x);
+            load_bc<NT>(bc, bct);
 #pragma unroll
-                    for (int k = 0; k < G / 2; ++k) {
-                        const float sarg = (p ? dv[2 * k + 1] : dv[2 * k]) + bias;
-                        const float um = p ? uv[2 * k + 1] : uv[2 * k];
-                        float dtm = SOFTPLUS ? softplus_f<ACC>(sarg) : sarg;
-                        if (MASK && grp * G + 2 * k + p >= nv) dtm = 0.0f;
-                        const float dum = dtm * um;
-                        const float dto = __shfl_xor_sync(kFull, dtm, 1);
-                        const float duo = __shfl_xor_sync(kFull, dum, 1);
-                        dtv[2 * k] = p ? dto : dtm;
-                        dtv[2 * k + 1] = p ? dtm : dto;
-                        duv[2 * k] = p ? duo : dum;
-                        duv[2 * k + 1] = p ? dum : duo;
-                        if (STATE_ONLY) dsum += dtm + dto;
+            for (int t = 0; t < TT; ++t) {
+                float2 dn = dd;
+                float2 an[kNPair];
+                float4 bn[kNPair];
+                if (t + 1 < TT) {
+                    dn = du_s[(t + 1) * kCH + c];
+                    load_bc<NT>(bn, bct + (t + 1) * (NP / 2));
+                    abar_step<NT, ACC>(an, a2, dn.x);
+                }
+                const float pt = state_step<NT, STATE_ONLY>(h2, ab, dd.y, bc);
+                if constexpr (STATE_ONLY) {
+                    dsum += dd.x;
+                } else {
+                    part_s[(hh * TT + t) * kCH + c] = pt;
+                    // keep the own partial of the steps this half finishes
+                    if (t < HT) {
+                        if (hh == 0) own[t] = pt;
+                    } else {
+                        if (hh == 1) own[t - HT] = pt;
                     }
                 }
-                float yv[G];
+                if (t + 1 < TT) {
+                    dd = dn;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float* brow = bct + ((grp * G + g) * 2) * kMaxN + p * NT;
-                    yv[g] = ssm_step<NT, ACC, STATE_ONLY>(h2, a2, dtv[g], duv[g], brow,
-                                                         brow + kMaxN);
-                }
-                if constexpr (!STATE_ONLY) {
-                    if constexpr (S == 1) {
-                        float ov[G];
-#pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            float o = yv[g] + dsk * uv[g];
-                            if constexpr (has_z) o *= silu_f<ACC>(zv[g]);
-                            ov[g] = o;
-                        }
-                        *reinterpret_cast<uint4*>(yt + off) = IO<T>::pack(ov);
-                    } else {
-                        // each lane finishes every other step: add the partner's
-                        // partial sum, skip term and gate, store one element
-                        T* yrow = reinterpret_cast<T*>(yt + off);
-#pragma unroll
-                        for (int k = 0; k < G / 2; ++k) {
-                            const float send = p ? yv[2 * k] : yv[2 * k + 1];
-                            const float recv = __shfl_xor_sync(kFull, send, 1);
-                            const float mine = (p ? yv[2 * k + 1] : yv[2 * k]) + recv;
-                            const float um = p ? uv[2 * k + 1] : uv[2 * k];
-                            float o = mine + dsk * um;
-                            if constexpr (has_z) o *= silu_f<ACC>(p ? zv[2 * k + 1] : zv[2 * k]);
-                            yrow[2 * k + p] = IO<T>::from_f(o);
-                        }
+                    for (int i = 0; i < kNPair; ++i) {
+                        ab[i] = an[i];
+                        bc[i] = bn[i];
                     }
                 }
             }
-        };
-        if (nv == TT) body(std::false_type{});
-        else body(std::true_type{});
+        }
+        if (!STATE_ONLY && tma && tid == 0) bulk_wait_read_0();   // y tile free again
+        __syncthreads();
 
-        if (!STATE_ONLY && tma) fence_proxy_async_smem();
-        __syncthreads();   // (B): stage s consumed, y tile complete
+        // (3) outputs of this half's steps: both partial sums, skip term, gate
+        if constexpr (!STATE_ONLY) {
+            const float* other = part_s + (1 - hh) * TT * kCH;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int ck = hh * 2 + q;
+                const int off = swz(c, ck);
+                float uv[G], zv[G], ov[G];
+                (void)zv;
+                CK::load(ut + off, uv);
+                if constexpr (has_z) CK::load(zt + off, zv);
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    const int t = ck * G + j;
+                    float o = own[q * G + j] + other[t * kCH + c];
+                    o = fmaf(dsk, uv[j], o);
+                    if constexpr (has_z) o *= silu_f<ACC>(zv[j]);
+                    ov[j] = o;
+                }
+                CK::store(yt + off, ov);
+            }
+            if (tma) fence_proxy_async_smem();
+        }
+        __syncthreads();   // stage s consumed, y tile complete
 
         if (!STATE_ONLY) {
             if (tma) {
@@ -603,7 +694,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                     bulk_commit();
                 }
             } else {
-                for (int e = tid; e < CH * TT; e += kThreads) {
+                for (int e = tid; e < kCH * TT; e += kNThr) {
                     const int cc = e / TT, t = e % TT;
                     if (cc < rows_valid && t < nv) {
                         const int byte = t * (int)sizeof(T);
@@ -637,7 +728,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     for (int i = 0; i < kNPair; ++i) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const int n = p * NT + 2 * i + j;
+            const int n = hh * NT + 2 * i + j;
             if (n >= N) continue;
             const float hv = j ? h2[i].y : h2[i].x;
             if (STATE_ONLY) {
@@ -746,7 +837,7 @@ state_update_kernel(const StepArgs a) {
 // ---------------------------------------------------------------------------
 
 struct Tuning {
-    int split = 0;   // lanes per channel (0 = automatic)
+    int tail = 0;    // 0 = automatic, 1 = whole-sequence units only, 2 = chunk the tail
     int stages = 0;  // ring depth (0 = automatic)
     int chunks = 0;  // time chunks for every group (0 = automatic)
 };
@@ -756,7 +847,9 @@ std::vector<cudaMemPool_t> g_pools;
 
 // Optional per-launch timing: while enabled, every kernel launch is bracketed
 // by two CUDA events recorded on its own stream.
-enum LaunchKind { kKindScan = 0, kKindSummary = 1, kKindCarry = 2, kKindStep = 3, kKinds = 4 };
+enum LaunchKind {
+    kKindScan = 0, kKindSummary = 1, kKindCarry = 2, kKindStep = 3, kKindPack = 4, kKinds = 5
+};
 struct ProfRec {
     int kind;
     cudaEvent_t start, stop;
@@ -830,33 +923,32 @@ int sm_count(int dev) {
     return cache[dev];
 }
 
-template <typename T, int NT, int S, bool STATE_ONLY, bool SP, bool HZ>
+template <typename T, int NT, bool STATE_ONLY, bool SP, bool HZ>
 cudaError_t launch_scan(const ScanArgs& a, int grid, int smem, cudaStream_t st) {
-    auto k = scan_kernel<T, NT, S, STATE_ONLY, SP, HZ>;
+    auto k = scan_kernel<T, NT, STATE_ONLY, SP, HZ>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     ProfScope prof(STATE_ONLY ? kKindSummary : kKindScan, st);
-    k<<<grid, kThreads, smem, st>>>(a);
+    k<<<grid, 32 * kScanWarps, smem, st>>>(a);
     return cudaGetLastError();
 }
 
-// (NT, S) variants: S = 1 for dstate <= 8 (NT = 2, 4, 8) and on request for
-// dstate <= 16 (NT = 16); S = 2 (NT = 8) is the default for 8 < dstate <= 16.
-#define MAMBA_VARIANTS(X) X(2, 1) X(4, 1) X(8, 1) X(16, 1) X(8, 2)
+// State entries per lane NT (half of the padded state): 2, 4, 8.
+#define MAMBA_VARIANTS(X) X(2) X(4) X(8)
 
 template <typename T, bool STATE_ONLY>
-cudaError_t dispatch_scan(int nt, int s, bool sp, bool hz, const ScanArgs& a, int grid, int smem,
+cudaError_t dispatch_scan(int nt, bool sp, bool hz, const ScanArgs& a, int grid, int smem,
                           cudaStream_t st) {
-#define X(NT_, S_)                                                                          \
-    if (nt == NT_ && s == S_) {                                                              \
+#define X(NT_)                                                                              \
+    if (nt == NT_) {                                                                         \
         if (STATE_ONLY)                                                                      \
-            return sp ? launch_scan<T, NT_, S_, STATE_ONLY, true, false>(a, grid, smem, st)  \
-                      : launch_scan<T, NT_, S_, STATE_ONLY, false, false>(a, grid, smem, st); \
+            return sp ? launch_scan<T, NT_, STATE_ONLY, true, false>(a, grid, smem, st)      \
+                      : launch_scan<T, NT_, STATE_ONLY, false, false>(a, grid, smem, st);    \
         if (sp)                                                                              \
-            return hz ? launch_scan<T, NT_, S_, STATE_ONLY, true, true>(a, grid, smem, st)   \
-                      : launch_scan<T, NT_, S_, STATE_ONLY, true, false>(a, grid, smem, st); \
-        return hz ? launch_scan<T, NT_, S_, STATE_ONLY, false, true>(a, grid, smem, st)      \
-                  : launch_scan<T, NT_, S_, STATE_ONLY, false, false>(a, grid, smem, st);    \
+            return hz ? launch_scan<T, NT_, STATE_ONLY, true, true>(a, grid, smem, st)       \
+                      : launch_scan<T, NT_, STATE_ONLY, true, false>(a, grid, smem, st);     \
+        return hz ? launch_scan<T, NT_, STATE_ONLY, false, true>(a, grid, smem, st)          \
+                  : launch_scan<T, NT_, STATE_ONLY, false, false>(a, grid, smem, st);        \
     }
     MAMBA_VARIANTS(X)
 #undef X
@@ -864,23 +956,48 @@ cudaError_t dispatch_scan(int nt, int s, bool sp, bool hz, const ScanArgs& a, in
 }
 
 struct Plan {
-    int nt, s, ch, stages, tt;
+    int nt, np, stages, tt;
     int groups_per_batch, n_groups, n_full, nchunks;
     long long chunk_len;
     int smem;
 };
 
-int smem_bytes(int ch, int stages, int tt) {
-    return ch == 128 ? Layout<128>::bytes(stages, tt) : Layout<64>::bytes(stages, tt);
+template <typename T>
+int smem_bytes_t(int nt, int stages) {
+    if (nt == 2) return ScanLayout<T, 2>::bytes(stages);
+    if (nt == 4) return ScanLayout<T, 4>::bytes(stages);
+    return ScanLayout<T, 8>::bytes(stages);
+}
+int smem_bytes(int dt, int nt, int stages) {
+    return dt == MAMBA_BF16 ? smem_bytes_t<__nv_bfloat16>(nt, stages)
+                            : smem_bytes_t<float>(nt, stages);
 }
 
-// Work decomposition.  Channel tiles scan the whole sequence when there are
-// at least as many tiles as SMs: the kernel is bound by instruction issue
-// and latency within each CTA, so extra co-resident CTAs on some SMs cost
-// little, while time chunks would add a summary pass (about 3/4 of a main
-// pass).  With fewer tiles than SMs (few channels, very long sequences)
-// every tile is cut into K time chunks so that about two pieces land on
-// each SM.
+int smem_per_sm(int dev) {
+    static std::vector<int> cache;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((int)cache.size() <= dev) cache.resize(dev + 1, 0);
+    if (!cache[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        cache[dev] = v > 0 ? v : 228 * 1024;
+    }
+    return cache[dev];
+}
+
+// Work decomposition.  A unit is a tile of kCH channels of one batch entry
+// (one CTA, one warp per SM sub-partition) over a time range.  The kernel is
+// bound by the ex2 and fp32 issue rates of each sub-partition, so the aim is
+// an equal number of units per SM:
+//   * whole waves of channel tiles (one per SM) scan the whole sequence;
+//   * the tiles left over ("tail", fewer than one per SM) are cut into K time
+//     chunks, K*tail <= #SM, so that each SM takes at most one extra chunk;
+//   * with fewer tiles than SMs, every tile is cut into K chunks so that
+//     the chunks fill the resident CTA slots of all SMs.
+// A chunk that does not start at t = 0 gets its carried-in state from a
+// summary pass (state only, about 3/4 of the work of a main pass) and a
+// carry pass.  Tuning: tail = 1 keeps whole-sequence units only, tail = 2
+// forces the chunked tail; chunks > 0 cuts every tile into that many chunks.
 Plan make_plan(int dev, int dt, long long batch, long long dim, int N, long long L, bool tma) {
     Tuning tn;
     {
@@ -888,33 +1005,41 @@ Plan make_plan(int dev, int dt, long long batch, long long dim, int N, long long
         tn = g_tuning;
     }
     Plan p;
-    int s = 1, nt;
-    if (N <= 2) nt = 2;
-    else if (N <= 4) nt = 4;
-    else if (N <= 8) nt = 8;
-    else {
-        s = (tn.split == 1) ? 1 : 2;
-        nt = 16 / s;
-    }
-    p.nt = nt;
-    p.s = s;
-    p.ch = kThreads / s;
+    p.nt = N <= 4 ? 2 : (N <= 8 ? 4 : 8);
+    p.np = kHalves * p.nt;
     p.tt = 64 / esize(dt);
-    p.stages = tma ? (tn.stages > 0 ? std::min(tn.stages, kMaxStages) : 2) : 1;
-    p.smem = smem_bytes(p.ch, p.stages, p.tt);
-    p.groups_per_batch = (int)((dim + p.ch - 1) / p.ch);
-    p.n_groups = (int)(batch * p.groups_per_batch);
     const int sms = sm_count(dev);
+    int stages = tma ? (tn.stages > 0 ? std::min(tn.stages, kMaxStages) : 2) : 1;
+    int per_sm = smem_per_sm(dev) / (smem_bytes(dt, p.nt, stages) + 1024);
+    per_sm = std::max(1, std::min(per_sm, 16));
+    p.stages = stages;
+    p.smem = smem_bytes(dt, p.nt, stages);
+    p.groups_per_batch = (int)((dim + kCH - 1) / kCH);
+    p.n_groups = (int)(batch * p.groups_per_batch);
     const long long tiles = (L + p.tt - 1) / p.tt;
-    const long long min_chunk_tiles = 8;
-    int K = 1;
+    const long long min_chunk_tiles = 4;
+    const long long max_k = std::max<long long>(1, tiles / min_chunk_tiles);
+    int n_chunked = 0, K = 1;
     if (tn.chunks > 0) {
+        n_chunked = p.n_groups;
         K = tn.chunks;
-    } else if (p.n_groups < sms && tiles >= 2 * min_chunk_tiles) {
-        K = (2 * sms + p.n_groups - 1) / p.n_groups;
-        K = (int)std::min<long long>(K, tiles / min_chunk_tiles);
+    } else if (p.n_groups >= sms) {
+        const int tail = p.n_groups % sms;
+        if (tail > 0 && tn.tail != 1) {
+            const int k = (int)std::min<long long>(sms / tail, max_k);
+            if (k >= 2 || tn.tail == 2) {
+                n_chunked = tail;
+                K = std::max(2, k);
+            }
+        }
+    } else if (tn.tail != 1) {
+        const int k = (int)std::min<long long>((long long)sms * per_sm / p.n_groups, max_k);
+        if (k >= 2) {
+            n_chunked = p.n_groups;
+            K = k;
+        }
     }
-    if (K <= 1) {
+    if (n_chunked == 0 || K <= 1) {
         p.n_full = p.n_groups;
         p.nchunks = 1;
         p.chunk_len = L;
@@ -922,7 +1047,7 @@ Plan make_plan(int dev, int dt, long long batch, long long dim, int N, long long
         const long long per = (tiles + K - 1) / K;
         p.chunk_len = per * p.tt;
         p.nchunks = (int)((L + p.chunk_len - 1) / p.chunk_len);
-        p.n_full = p.nchunks > 1 ? 0 : p.n_groups;
+        p.n_full = p.nchunks > 1 ? p.n_groups - n_chunked : p.n_groups;
     }
     return p;
 }
@@ -943,18 +1068,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// 3-D map over a (d2, d1, d0) row-major tensor, box {b0, b1, 1}.
-bool encode_map(CUtensorMap* m, const void* ptr, int dt, long long d0, long long d1, long long d2,
-                int b0, int b1, bool swizzle) {
+// 3-D map over a (d2, d1, d0) row-major tensor of `es`-byte elements, box
+// {b0, b1, 1}.
+bool encode_map(CUtensorMap* m, const void* ptr, int es, bool is_bf16, long long d0,
+                long long d1, long long d2, int b0, int b1, bool swizzle) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    const int es = esize(dt);
     cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
     cuuint64_t strides[2] = {(cuuint64_t)(d0 * es), (cuuint64_t)(d0 * d1 * es)};
     cuuint32_t box[3] = {(cuuint32_t)b0, (cuuint32_t)b1, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = enc(m, dt == MAMBA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+    const CUresult r = enc(m, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                            3, const_cast<void*>(ptr), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE,
                            swizzle ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -968,7 +1093,7 @@ using namespace mamba;
 
 extern "C" {
 
-int mamba_version(void) { return 200; }
+int mamba_version(void) { return 300; }
 
 const char* mamba_status_string(int status) {
     switch (status) {
@@ -1033,11 +1158,11 @@ int mamba_profile_end(double* total_ms, int64_t* launches, int nkinds) {
     return rc;
 }
 
-int mamba_scan_set_tuning(int split, int stages, int chunks) {
-    if (split < 0 || split > 2 || stages < 0 || stages > kMaxStages || chunks < 0)
+int mamba_scan_set_tuning(int tail, int stages, int chunks) {
+    if (tail < 0 || tail > 2 || stages < 0 || stages > kMaxStages || chunks < 0)
         return MAMBA_ERR_SHAPE;
     std::lock_guard<std::mutex> lk(g_mu);
-    g_tuning.split = split;
+    g_tuning.tail = tail;
     g_tuning.stages = stages;
     g_tuning.chunks = chunks;
     return MAMBA_OK;
@@ -1083,62 +1208,83 @@ int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, i
     // tensor-map path: 16-byte aligned bases and rows, coordinates within int32
     bool tma = ((seqlen * es) % 16) == 0 && seqlen < (1ll << 31) && dim < (1ll << 31) &&
                (double)dim * seqlen * es < 1.0e12;
-    for (const void* q : {u, delta, z, B, C, (const void*)y})
+    for (const void* q : {u, delta, z, (const void*)y})
         if (q && !aligned(q, 16)) tma = false;
 
     Plan pl = make_plan(dev, io_dtype, batch, dim, (int)dstate, seqlen, tma);
+    const bool chunked = pl.n_full < pl.n_groups && pl.nchunks > 1;
+    const bool acc = io_dtype == MAMBA_F32;
+
+    // scratch: packed B/C rows, then the chunk summaries
+    const size_t bc_bytes = (size_t)batch * (size_t)seqlen * (size_t)pl.np * 2 * sizeof(float);
+    const size_t tail_rows = (size_t)(pl.n_groups - pl.n_full) * kCH;
+    const size_t entries = tail_rows * (size_t)dstate;
+    const size_t ws_bytes = chunked ? 2 * entries * (size_t)(pl.nchunks - 1) * sizeof(float) : 0;
+    cudaMemPool_t pool = nullptr;
+    int rc = get_pool(dev, &pool);
+    if (rc != MAMBA_OK) return rc;
+    void* scratch = nullptr;
+    if (cudaMallocFromPoolAsync(&scratch, bc_bytes + ws_bytes, pool, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MAMBA_ERR_ALLOC;
+    }
 
     ScanArgs a;
     std::memset(&a, 0, sizeof(a));
+    a.bc = static_cast<const float4*>(scratch);
+    if (chunked) {
+        a.ws_P = reinterpret_cast<float*>(static_cast<char*>(scratch) + bc_bytes);
+        a.ws_h = a.ws_P + entries * (pl.nchunks - 1);
+    }
     if (tma) {
-        const int ch = pl.ch, tt = pl.tt;
-        tma = encode_map(&a.m_u, u, io_dtype, seqlen, dim, batch, tt, ch, true) &&
-              encode_map(&a.m_dl, delta, io_dtype, seqlen, dim, batch, tt, ch, true) &&
-              (!z || encode_map(&a.m_z, z, io_dtype, seqlen, dim, batch, tt, ch, true)) &&
-              encode_map(&a.m_y, y, io_dtype, seqlen, dim, batch, tt, ch, true) &&
-              encode_map(&a.m_B, B, io_dtype, seqlen, dstate, batch, tt, (int)dstate, false) &&
-              encode_map(&a.m_C, C, io_dtype, seqlen, dstate, batch, tt, (int)dstate, false);
+        const bool bf = io_dtype == MAMBA_BF16;
+        const int tt = pl.tt;
+        tma = encode_map(&a.m_u, u, es, bf, seqlen, dim, batch, tt, kCH, true) &&
+              encode_map(&a.m_dl, delta, es, bf, seqlen, dim, batch, tt, kCH, true) &&
+              (!z || encode_map(&a.m_z, z, es, bf, seqlen, dim, batch, tt, kCH, true)) &&
+              encode_map(&a.m_y, y, es, bf, seqlen, dim, batch, tt, kCH, true) &&
+              encode_map(&a.m_bc, scratch, 4, false, 2 * pl.np, seqlen, batch, 2 * pl.np, tt,
+                         false);
         if (!tma) pl = make_plan(dev, io_dtype, batch, dim, (int)dstate, seqlen, false);
     }
-    a.u = u; a.delta = delta; a.z = z; a.B = B; a.C = C;
+    a.u = u; a.delta = delta; a.z = z;
     a.dt_bias = dt_bias; a.A = A; a.D_skip = D_skip; a.y = y; a.final_state = final_state;
     a.dim = dim; a.seqlen = seqlen; a.chunk_len = pl.chunk_len;
     a.batch = (int)batch; a.dstate = (int)dstate;
     a.use_tma = tma ? 1 : 0; a.stages = pl.stages;
     a.groups_per_batch = pl.groups_per_batch; a.n_groups = pl.n_groups;
     a.n_full = pl.n_full; a.nchunks = pl.nchunks;
-    a.tail_rows = (pl.n_groups - pl.n_full) * pl.ch;
+    a.tail_rows = (int)tail_rows;
 
-    const bool chunked = pl.n_full < pl.n_groups && pl.nchunks > 1;
-    void* ws = nullptr;
-    if (chunked) {
-        const size_t entries = (size_t)a.tail_rows * dstate;
-        const size_t bytes = 2 * entries * (size_t)(pl.nchunks - 1) * sizeof(float);
-        cudaMemPool_t pool = nullptr;
-        int rc = get_pool(dev, &pool);
-        if (rc != MAMBA_OK) return rc;
-        if (cudaMallocFromPoolAsync(&ws, bytes, pool, stream) != cudaSuccess) {
-            cudaGetLastError();
-            return MAMBA_ERR_ALLOC;
-        }
-        a.ws_P = static_cast<float*>(ws);
-        a.ws_h = a.ws_P + entries * (pl.nchunks - 1);
+    cudaError_t e;
+    {
+        const long long items = batch * seqlen * (pl.np / 2);
+        const int blocks = (int)std::min<long long>((items + 255) / 256, 16LL * sm_count(dev));
+        ProfScope prof(kKindPack, stream);
+        const float scale = acc ? 1.0f : kLn2;
+        float4* out = static_cast<float4*>(scratch);
+        if (io_dtype == MAMBA_BF16)
+            pack_bc_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+                static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), out,
+                batch, seqlen, (int)dstate, pl.np, scale);
+        else
+            pack_bc_kernel<float><<<blocks, 256, 0, stream>>>(
+                static_cast<const float*>(B), static_cast<const float*>(C), out, batch, seqlen,
+                (int)dstate, pl.np, scale);
+        e = cudaGetLastError();
     }
-
-    cudaError_t e = cudaSuccess;
-    if (chunked) {
+    if (e == cudaSuccess && chunked) {
         const int grid1 = (pl.n_groups - pl.n_full) * (pl.nchunks - 1);
         e = io_dtype == MAMBA_BF16
-                ? dispatch_scan<__nv_bfloat16, true>(pl.nt, pl.s, softplus, false, a, grid1,
-                                                     pl.smem, stream)
-                : dispatch_scan<float, true>(pl.nt, pl.s, softplus, false, a, grid1, pl.smem,
-                                             stream);
+                ? dispatch_scan<__nv_bfloat16, true>(pl.nt, softplus, false, a, grid1, pl.smem,
+                                                     stream)
+                : dispatch_scan<float, true>(pl.nt, softplus, false, a, grid1, pl.smem, stream);
         if (e == cudaSuccess) {
-            const long long entries = (long long)a.tail_rows * dstate;
+            const long long n_ent = (long long)entries;
             {
                 ProfScope prof(kKindCarry, stream);
-                carry_kernel<<<(unsigned)((entries + 255) / 256), 256, 0, stream>>>(
-                    a.ws_P, a.ws_h, entries, pl.nchunks);
+                carry_kernel<<<(unsigned)((n_ent + 255) / 256), 256, 0, stream>>>(
+                    a.ws_P, a.ws_h, n_ent, pl.nchunks);
             }
             e = cudaGetLastError();
         }
@@ -1146,12 +1292,12 @@ int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, i
     if (e == cudaSuccess) {
         const int grid = pl.n_full + (chunked ? (pl.n_groups - pl.n_full) * pl.nchunks : 0);
         e = io_dtype == MAMBA_BF16
-                ? dispatch_scan<__nv_bfloat16, false>(pl.nt, pl.s, softplus, z != nullptr, a,
-                                                      grid, pl.smem, stream)
-                : dispatch_scan<float, false>(pl.nt, pl.s, softplus, z != nullptr, a, grid,
-                                              pl.smem, stream);
+                ? dispatch_scan<__nv_bfloat16, false>(pl.nt, softplus, z != nullptr, a, grid,
+                                                      pl.smem, stream)
+                : dispatch_scan<float, false>(pl.nt, softplus, z != nullptr, a, grid, pl.smem,
+                                              stream);
     }
-    if (ws) cudaFreeAsync(ws, stream);
+    cudaFreeAsync(scratch, stream);
     return e == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
 

@@ -3,7 +3,7 @@
 Element-by-element on the same seeded inputs: every workload at its full size
 (sampled rows where the oracle would take minutes), odd shapes with ragged
 tails, every nullable argument, the chunked (summary + carry) path, both
-state splits, and guard bands around the outputs.
+tail scheduling modes, and guard bands around the outputs.
 """
 
 import numpy as np
@@ -171,17 +171,18 @@ def test_zero_length_writes_zero_state():
 
 
 # --------------------------------------------------------------------------
-# chunked path and state splits (same results up to fp32 rounding order)
+# chunked path and tail modes (same results up to fp32 rounding order)
 
 @pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
-@pytest.mark.parametrize("split,chunks,stages", [(0, 3, 0), (0, 7, 3), (2, 0, 0), (1, 0, 4),
-                                                 (2, 5, 2), (1, 9, 1), (1, 2, 0), (2, 1, 3)])
-def test_chunks_and_splits(dtype, split, chunks, stages):
+@pytest.mark.parametrize("tail,chunks,stages", [(0, 3, 0), (0, 7, 3), (2, 0, 0), (1, 0, 4),
+                                                (2, 5, 2), (1, 9, 1), (1, 2, 0), (2, 1, 3),
+                                                (0, 1, 2)])
+def test_chunks_and_tails(dtype, tail, chunks, stages):
     import selective_state_space_135_b300 as mm
     shp = synth.ScanShape("chunks", 2, 150, 16, 1000 if dtype == synth.F32 else 1024,
                           dtype=dtype, seed=11)
     inp = synth.scan_inputs(shp)
-    mm.mamba_scan_set_tuning(split, stages, chunks)
+    mm.mamba_scan_set_tuning(tail, stages, chunks)
     y, fin = scan_on_gpu(inp)
     yr, hr = oracle_full(inp)
     assert_close(to_f64(y), yr, dtype)
