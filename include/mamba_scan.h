@@ -72,8 +72,12 @@ typedef enum {
     MAMBA_ERR_TIMEOUT = -5,  /* a device-side wait ran out (mamba_device_status) */
     MAMBA_ERR_ALLOC = -6,    /* scratch memory could not be obtained */
     MAMBA_ERR_DTYPE = -7,    /* io_dtype is not one of mamba_dtype_t */
-    MAMBA_ERR_ALIAS = -8     /* an output overlaps an input */
+    MAMBA_ERR_ALIAS = -8,    /* an output overlaps an input */
+    MAMBA_ERR_TOO_BIG = -9   /* needs more than MAMBA_NOALLOC_SCRATCH_BYTES of scratch */
 } mamba_status_t;
+
+/* Size of the fixed scratch array used by mamba_scan_fwd_noalloc (16 MiB). */
+#define MAMBA_NOALLOC_SCRATCH_BYTES (16ll << 20)
 
 /*
  * Selective scan over a whole sequence, starting from a zero state.
@@ -101,6 +105,39 @@ int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
                    const float *A, const void *B, const void *C,
                    const float *D_skip, const void *z, int softplus,
                    void *y, float *final_state, cudaStream_t stream);
+
+/*
+ * mamba_scan_fwd without any memory allocation.  The paper has no
+ * counterpart to this entry point; it exists for callers that cannot call
+ * cudaMalloc or a stream-ordered allocator, for example code running under a
+ * runtime that owns all device memory in a fixed arena, or a latency-critical
+ * path where an allocation may block, synchronise or fail under
+ * fragmentation.  Arguments, layouts, results and error codes are those of
+ * mamba_scan_fwd.
+ *
+ * Its scratch (the packed B/C table and, for time-chunked plans, the chunk
+ * summaries) lives in one fixed array of MAMBA_NOALLOC_SCRATCH_BYTES bytes
+ * in the library's device memory, held by every GPU that loads the library
+ * until the process exits.  A call whose scratch would exceed it returns
+ * MAMBA_ERR_TOO_BIG and launches nothing; the packed table alone needs
+ * batch * seqlen * 128 bytes when dstate > 8 (64 bytes for dstate <= 8,
+ * 32 for dstate <= 4), so batch * seqlen up to 131072 fits at dstate 16
+ * when no time chunks are needed.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array: calls whose
+ * work overlaps on the GPU (different streams, or different host threads)
+ * race on it and must be serialised by the caller.  Every byte a call reads
+ * from the array is written earlier in the same call, so nothing needs
+ * clearing between calls.
+ */
+int mamba_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                           int io_dtype,
+                           const void *u, const void *delta, const float *dt_bias,
+                           const float *A, const void *B, const void *C,
+                           const float *D_skip, const void *z, int softplus,
+                           void *y, float *final_state, cudaStream_t stream);
 
 /*
  * One generation step, updating `state` in place:

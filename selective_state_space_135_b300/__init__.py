@@ -19,6 +19,7 @@ from ._lib import (  # noqa: F401
     mamba_profile_begin,
     mamba_profile_end,
     mamba_scan_fwd,
+    mamba_scan_fwd_noalloc,
     mamba_scan_set_tuning,
     mamba_state_update,
     mamba_status_string,

@@ -15,7 +15,7 @@ MAMBA_F32 = 0
 MAMBA_BF16 = 1
 
 # every symbol the header declares
-EXPORTS = ("mamba_scan_fwd", "mamba_state_update", "mamba_status_string",
+EXPORTS = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_state_update", "mamba_status_string",
            "mamba_device_status", "mamba_version", "mamba_scan_set_tuning",
            "mamba_profile_begin", "mamba_profile_end")
 
@@ -46,6 +46,8 @@ def load():
         lib.mamba_scan_fwd.argtypes = [i64, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                        i32, vp, vp, vp]
         lib.mamba_scan_fwd.restype = i32
+        lib.mamba_scan_fwd_noalloc.argtypes = lib.mamba_scan_fwd.argtypes
+        lib.mamba_scan_fwd_noalloc.restype = i32
         lib.mamba_state_update.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                            vp, vp, vp]
         lib.mamba_state_update.restype = i32
@@ -114,13 +116,8 @@ def _stream_handle(stream, device):
     return stream.cuda_stream
 
 
-def mamba_scan_fwd(u, delta, dt_bias, A, B, C, D_skip, z, softplus: bool = True,
-                   y=None, final_state=None, stream=None):
-    """Selective scan.  u, delta, z: (batch, dim, L); B, C: (batch, N, L);
-    A: (dim, N) fp32; dt_bias, D_skip: (dim,) fp32 or None; z may be None.
-    y (allocated if None) gets the output; final_state (batch, dim, N) fp32,
-    if given, gets the state after the last step.  Returns y.
-    """
+def _scan_call(fn_name, u, delta, dt_bias, A, B, C, D_skip, z, softplus, y, final_state,
+               stream):
     torch = _torch()
     lib = load()
     batch, dim, L = u.shape
@@ -143,12 +140,33 @@ def mamba_scan_fwd(u, delta, dt_bias, A, B, C, D_skip, z, softplus: bool = True,
     fp = _ptr(final_state, "final_state", torch.float32, (batch, dim, N), dev)
     with torch.cuda.device(dev):
         st = _stream_handle(stream, dev)
-        rc = lib.mamba_scan_fwd(batch, dim, N, L, io, args[0], args[1], args[2], args[3],
-                                args[4], args[5], args[6], args[7], int(bool(softplus)),
-                                yp, fp, st)
+        rc = getattr(lib, fn_name)(batch, dim, N, L, io, args[0], args[1], args[2], args[3],
+                                   args[4], args[5], args[6], args[7], int(bool(softplus)),
+                                   yp, fp, st)
     if rc != 0:
-        raise MambaError(rc, "mamba_scan_fwd")
+        raise MambaError(rc, fn_name)
     return y
+
+
+def mamba_scan_fwd(u, delta, dt_bias, A, B, C, D_skip, z, softplus: bool = True,
+                   y=None, final_state=None, stream=None):
+    """Selective scan.  u, delta, z: (batch, dim, L); B, C: (batch, N, L);
+    A: (dim, N) fp32; dt_bias, D_skip: (dim,) fp32 or None; z may be None.
+    y (allocated if None) gets the output; final_state (batch, dim, N) fp32,
+    if given, gets the state after the last step.  Returns y.
+    """
+    return _scan_call("mamba_scan_fwd", u, delta, dt_bias, A, B, C, D_skip, z, softplus, y,
+                      final_state, stream)
+
+
+def mamba_scan_fwd_noalloc(u, delta, dt_bias, A, B, C, D_skip, z, softplus: bool = True,
+                           y=None, final_state=None, stream=None):
+    """mamba_scan_fwd through the entry point that allocates no scratch: the
+    library uses its fixed device array (MAMBA_NOALLOC_SCRATCH_BYTES) instead.
+    Same arguments; pass y to keep the call free of allocations here as well.
+    Calls that overlap on the GPU share that array and must be serialised."""
+    return _scan_call("mamba_scan_fwd_noalloc", u, delta, dt_bias, A, B, C, D_skip, z, softplus,
+                      y, final_state, stream)
 
 
 def mamba_state_update(state, x, delta, dt_bias, A, B, C, D_skip, z, y=None, stream=None):

@@ -723,7 +723,9 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     }
 
     // ---- results that leave the SM: final state or chunk summary ----
-    if (!chan_ok) return;
+    // (the summary also covers the tile's channels past `dim`, whose state
+    // stays zero, so that the carry pass reads only written entries)
+    if (!chan_ok && !STATE_ONLY) return;
 #pragma unroll
     for (int i = 0; i < kNPair; ++i) {
 #pragma unroll
@@ -1087,6 +1089,42 @@ bool encode_map(CUtensorMap* m, const void* ptr, int es, bool is_bf16, long long
     return r == CUDA_SUCCESS;
 }
 
+// ---------------------------------------------------------------------------
+// fixed scratch of the no-allocation entry point
+// ---------------------------------------------------------------------------
+
+// Scratch of mamba_scan_fwd_noalloc: a fixed array in the module's global
+// memory, so that call never allocates.  Every GPU that loads the library
+// holds it until the process exits.  In host code the name is only a
+// stand-in for the symbol; its device address comes from
+// cudaGetSymbolAddress (noalloc_scratch below).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MAMBA_NOALLOC_SCRATCH_BYTES];
+
+std::vector<void*> g_noalloc_ptr;   // device address of g_noalloc_scratch, per device
+
+// Device address of the fixed scratch on `dev` (the current device).  The
+// first call on a device looks it up; later calls reuse it.
+int noalloc_scratch(int dev, void** out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((int)g_noalloc_ptr.size() <= dev) g_noalloc_ptr.resize(dev + 1, nullptr);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return MAMBA_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MAMBA_OK;
+}
+
+// Bytes of packed B/C rows per (batch entry, step): 2 * padded state * fp32.
+long long packed_row_bytes(int64_t dstate) {
+    const int nt = dstate <= 4 ? 2 : (dstate <= 8 ? 4 : 8);
+    return 2LL * kHalves * nt * (long long)sizeof(float);
+}
+
 }  // namespace mamba
 
 using namespace mamba;
@@ -1106,6 +1144,8 @@ const char* mamba_status_string(int status) {
         case MAMBA_ERR_ALLOC: return "scratch memory could not be obtained";
         case MAMBA_ERR_DTYPE: return "unsupported io dtype";
         case MAMBA_ERR_ALIAS: return "an output overlaps an input";
+        case MAMBA_ERR_TOO_BIG:
+            return "the call needs more scratch than the fixed MAMBA_NOALLOC_SCRATCH_BYTES";
         default: return "unknown status";
     }
 }
@@ -1168,10 +1208,13 @@ int mamba_scan_set_tuning(int tail, int stages, int chunks) {
     return MAMBA_OK;
 }
 
-int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io_dtype,
-                   const void* u, const void* delta, const float* dt_bias, const float* A,
-                   const void* B, const void* C, const float* D_skip, const void* z,
-                   int softplus, void* y, float* final_state, cudaStream_t stream) {
+// Shared body of mamba_scan_fwd (scratch from the stream-ordered pool) and
+// mamba_scan_fwd_noalloc (the fixed scratch array, no allocation).
+static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                           int io_dtype, const void* u, const void* delta,
+                           const float* dt_bias, const float* A, const void* B, const void* C,
+                           const float* D_skip, const void* z, int softplus, void* y,
+                           float* final_state, cudaStream_t stream, bool no_alloc) {
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
     if (batch < 1 || dim < 1 || dstate < 1 || dstate > kMaxN || seqlen < 0) return MAMBA_ERR_SHAPE;
     if (batch > INT32_MAX / 2 || dim > (1ll << 40) || seqlen > (1ll << 40) ||
@@ -1203,6 +1246,12 @@ int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, i
         return MAMBA_OK;
     }
 
+    // the packed B/C rows alone must fit the fixed scratch (checked before
+    // any CUDA call; the chunk summaries are checked once the plan is known)
+    if (no_alloc && (double)batch * (double)seqlen * (double)packed_row_bytes(dstate) >
+                        (double)MAMBA_NOALLOC_SCRATCH_BYTES)
+        return MAMBA_ERR_TOO_BIG;
+
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MAMBA_ERR_CUDA;
     // tensor-map path: 16-byte aligned bases and rows, coordinates within int32
@@ -1220,13 +1269,19 @@ int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, i
     const size_t tail_rows = (size_t)(pl.n_groups - pl.n_full) * kCH;
     const size_t entries = tail_rows * (size_t)dstate;
     const size_t ws_bytes = chunked ? 2 * entries * (size_t)(pl.nchunks - 1) * sizeof(float) : 0;
-    cudaMemPool_t pool = nullptr;
-    int rc = get_pool(dev, &pool);
-    if (rc != MAMBA_OK) return rc;
     void* scratch = nullptr;
-    if (cudaMallocFromPoolAsync(&scratch, bc_bytes + ws_bytes, pool, stream) != cudaSuccess) {
-        cudaGetLastError();
-        return MAMBA_ERR_ALLOC;
+    if (no_alloc) {
+        if (bc_bytes + ws_bytes > (size_t)MAMBA_NOALLOC_SCRATCH_BYTES) return MAMBA_ERR_TOO_BIG;
+        const int rc = noalloc_scratch(dev, &scratch);
+        if (rc != MAMBA_OK) return rc;
+    } else {
+        cudaMemPool_t pool = nullptr;
+        const int rc = get_pool(dev, &pool);
+        if (rc != MAMBA_OK) return rc;
+        if (cudaMallocFromPoolAsync(&scratch, bc_bytes + ws_bytes, pool, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return MAMBA_ERR_ALLOC;
+        }
     }
 
     ScanArgs a;
@@ -1297,8 +1352,25 @@ int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, i
                 : dispatch_scan<float, false>(pl.nt, softplus, z != nullptr, a, grid, pl.smem,
                                               stream);
     }
-    cudaFreeAsync(scratch, stream);
+    if (!no_alloc) cudaFreeAsync(scratch, stream);
     return e == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
+}
+
+int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io_dtype,
+                   const void* u, const void* delta, const float* dt_bias, const float* A,
+                   const void* B, const void* C, const float* D_skip, const void* z,
+                   int softplus, void* y, float* final_state, cudaStream_t stream) {
+    return scan_fwd_common(batch, dim, dstate, seqlen, io_dtype, u, delta, dt_bias, A, B, C,
+                           D_skip, z, softplus, y, final_state, stream, false);
+}
+
+int mamba_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                           int io_dtype, const void* u, const void* delta,
+                           const float* dt_bias, const float* A, const void* B, const void* C,
+                           const float* D_skip, const void* z, int softplus, void* y,
+                           float* final_state, cudaStream_t stream) {
+    return scan_fwd_common(batch, dim, dstate, seqlen, io_dtype, u, delta, dt_bias, A, B, C,
+                           D_skip, z, softplus, y, final_state, stream, true);
 }
 
 int mamba_state_update(int64_t batch, int64_t dim, int64_t dstate, int io_dtype, float* state,

@@ -14,6 +14,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "mamba_scan.h")
 
 OK, ENULL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EALLOC, EDTYPE, EALIAS = 0, -1, -2, -3, -4, -5, -6, -7, -8
+ETOOBIG = -9
 
 
 def declared_functions():
@@ -40,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in (OK, ENULL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EALLOC, EDTYPE, EALIAS):
+    for code in (OK, ENULL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EALLOC, EDTYPE, EALIAS, ETOOBIG):
         s = mm.mamba_status_string(code)
         assert s and s != "unknown status"
     assert mm.mamba_status_string(12345) == "unknown status"
@@ -57,12 +58,12 @@ def addr(i, extra=0):
 
 
 def scan_call(lib, batch=2, dim=16, dstate=4, seqlen=64, io=1, u=1, delta=2, dtb=3, A=4, B=5,
-              C=6, Dk=7, z=8, softplus=1, y=9, fin=10, extra=None):
+              C=6, Dk=7, z=8, softplus=1, y=9, fin=10, extra=None, fn="mamba_scan_fwd"):
     ptrs = dict(u=u, delta=delta, dtb=dtb, A=A, B=B, C=C, Dk=Dk, z=z, y=y, fin=fin)
     vals = {k: (None if v is None else addr(v, (extra or {}).get(k, 0))) for k, v in ptrs.items()}
-    return lib.mamba_scan_fwd(batch, dim, dstate, seqlen, io, vals["u"], vals["delta"],
-                              vals["dtb"], vals["A"], vals["B"], vals["C"], vals["Dk"],
-                              vals["z"], softplus, vals["y"], vals["fin"], None)
+    return getattr(lib, fn)(batch, dim, dstate, seqlen, io, vals["u"], vals["delta"],
+                            vals["dtb"], vals["A"], vals["B"], vals["C"], vals["Dk"],
+                            vals["z"], softplus, vals["y"], vals["fin"], None)
 
 
 def test_scan_rejects_bad_shapes(lib):
@@ -99,6 +100,23 @@ def test_scan_nullable_inputs_pass_validation(lib):
     # machine without a GPU, fails only at the CUDA layer
     rc = scan_call(lib, dtb=None, Dk=None, z=None, fin=None)
     assert rc in (ECUDA, OK)
+
+
+def test_noalloc_validates_like_the_scan(lib):
+    fn = "mamba_scan_fwd_noalloc"
+    assert scan_call(lib, dstate=17, fn=fn) == ESHAPE
+    assert scan_call(lib, u=None, fn=fn) == ENULL
+    assert scan_call(lib, extra={"u": 1}, fn=fn) == EALIGN
+    assert scan_call(lib, y=1, fn=fn) == EALIAS
+
+
+def test_noalloc_rejects_oversize_before_any_cuda_call(lib):
+    # 2 x 70000 steps of packed B/C rows (128 bytes each at dstate 16) exceed
+    # the 16 MiB fixed scratch; the check precedes every CUDA call
+    fn = "mamba_scan_fwd_noalloc"
+    assert scan_call(lib, dstate=16, seqlen=70000, fn=fn) == ETOOBIG
+    assert scan_call(lib, dstate=4, seqlen=300000, fn=fn) == ETOOBIG
+    assert "MAMBA_NOALLOC_SCRATCH_BYTES" in mm.mamba_status_string(ETOOBIG)
 
 
 def step_call(lib, batch=2, dim=8, dstate=16, io=1, state=1, x=2, delta=3, dtb=4, A=5, B=6, C=7,
