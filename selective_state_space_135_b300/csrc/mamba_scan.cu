@@ -162,11 +162,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// Non-blocking test of phase completion (mbarrier.test_wait): unlike
+// try_wait it never suspends the thread, so a phase that has already
+// completed is seen at once.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred P1;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
         "selp.b32 %0, 1, 0, P1;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -179,11 +182,14 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 // Bounded wait: true when the phase completed, false after kWaitLimitNs.
+// The global timer is read only after 4096 unsuccessful polls: reading it is
+// slow, and a wait that ends within a few microseconds never needs it.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 4096; ++i)
+        if (mbar_test_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (unsigned it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_test_wait(bar, parity)) return true;
         if ((it & 255u) == 255u && global_ns() - t0 > kWaitLimitNs) return false;
     }
 }
@@ -432,6 +438,44 @@ __device__ __forceinline__ float state_step(float2 (&h2)[NT / 2], const float2 (
     }
 }
 
+// One time step of the state (as state_step) fused with Abar of the next
+// step (as abar_step), pair by pair, so that the ex2 work of step t+1 sits
+// between the multiply/adds of step t in the instruction stream instead of
+// stalling the warp in one burst.
+template <int NT, bool ACC, bool STATE_ONLY>
+__device__ __forceinline__ float fused_step(float2 (&h2)[NT / 2], const float2 (&ab)[NT / 2],
+                                            float2 (&an)[NT / 2], const float2 (&a2)[NT / 2],
+                                            float dt_next, float du,
+                                            const float4 (&bc)[NT / 2]) {
+    const float2 du2 = make_float2(du, du);
+    const float2 dt2 = make_float2(dt_next, dt_next);
+    float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int i = 0; i < NT / 2; ++i) {
+        if constexpr (ACC) {
+            an[i] = make_float2(expf(dt_next * a2[i].x), expf(dt_next * a2[i].y));
+        } else {
+            const float2 arg = __fmul2_rn(dt2, a2[i]);
+            an[i] = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
+        }
+        const float2 bx = __fmul2_rn(du2, make_float2(bc[i].x, bc[i].y));
+        h2[i] = __ffma2_rn(ab[i], h2[i], bx);
+        if constexpr (!STATE_ONLY) {
+            const float2 cp = make_float2(bc[i].z, bc[i].w);
+            if (i & 1) acc1 = (i == 1) ? __fmul2_rn(cp, h2[i]) : __ffma2_rn(cp, h2[i], acc1);
+            else acc0 = (i == 0) ? __fmul2_rn(cp, h2[i]) : __ffma2_rn(cp, h2[i], acc0);
+        }
+    }
+    if constexpr (STATE_ONLY) {
+        return 0.0f;
+    } else if constexpr (NT == 2) {
+        return acc0.x + acc0.y;
+    } else {
+        const float2 acc = __fadd2_rn(acc0, acc1);
+        return acc.x + acc.y;
+    }
+}
+
 template <int NT>
 __device__ __forceinline__ void load_bc(float4 (&bc)[NT / 2], const float4* row) {
 #pragma unroll
@@ -528,11 +572,11 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
         tma_load_3d(smem_u32(st + 3 * Lay::kRows), &a.m_bc, 0, tt0, w.b, bar);
     };
 
-    // all threads: element-wise, bounds-checked fill of stage 0 (any shape)
-    auto plain_tile = [&](int it) {
+    // all threads: element-wise, bounds-checked fill of stage `sidx` (any shape)
+    auto plain_tile = [&](int it, int sidx) {
         const long long tt0 = w.t0 + (long long)it * TT;
         const int nv = (int)min((long long)TT, L_ - tt0);
-        unsigned char* st = smem + Lay::stage(0);
+        unsigned char* st = smem + Lay::stage(sidx);
         for (int e = tid; e < ntens * kCH * TT; e += kNThr) {
             const int tsr = e / (kCH * TT), rem = e % (kCH * TT);
             const int cc = rem / TT, t = rem % TT;
@@ -568,78 +612,98 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     int issued = tma ? min(stages, ntiles) : 0;
     bool aborted = false;
 
-    for (int it = 0; it < ntiles; ++it) {
-        const int s = tma ? it % stages : 0;
-        const long long tt0 = w.t0 + (long long)it * TT;
-        const int nv = (int)min((long long)TT, w.t1 - tt0);   // steps of this unit in the tile
-        const unsigned char* st = smem + Lay::stage(s);
-
-        bool timed_out = false;
+    // Wait for the data of tile `it_` in stage `st_`.  Only lane 0 of each
+    // warp polls the mbarrier (polling by every thread of the SM is slow);
+    // __syncwarp then orders the other lanes after it.  The plain path fills
+    // the stage cooperatively instead.  Returns true when the wait ran out.
+    auto acquire = [&](int it_, int st_, uint32_t par_) -> bool {
         if (tma) {
-            timed_out = !mbar_wait_bounded(smem_u32(&bars[s]), (uint32_t)((it / stages) & 1));
+            int to = 0;
+            if (lane == 0) to = mbar_wait_bounded(smem_u32(&bars[st_]), par_) ? 0 : 1;
+            __syncwarp();
+            return __shfl_sync(0xffffffffu, to, 0) != 0;
+        }
+        plain_tile(it_, st_);
+        __syncthreads();
+        return false;
+    };
+
+    // Delta (log2 units on the fast path) of one step from the raw delta value
+    auto delta_of = [&](float dv) -> float {
+        if constexpr (ACC) {
+            const float sarg = dv + bias;
+            return SOFTPLUS ? (sarg > 20.0f ? sarg : log1pf(expf(sarg))) : sarg;
         } else {
-            plain_tile(it);
+            // s * log2(e); softplus in log2 units: log2(1 + 2^tl)
+            const float tl = fmaf(dv, kLog2e, bias);
+            return SOFTPLUS ? (tl > 30.0f ? tl : lg2_approx(1.0f + ex2_approx(tl))) : tl;
         }
-        if (__syncthreads_or(timed_out)) {
-            aborted = true;
-            break;
-        }
+    };
 
-        const unsigned char* ut = st;
-        const unsigned char* dlt = st + Lay::kRows;
-        const unsigned char* zt = st + 2 * Lay::kRows;
-        const float4* bct = reinterpret_cast<const float4*>(st + 3 * Lay::kRows) + hh * kNPair;
-
-        // (1) Delta (log2 units on the fast path) and Delta*u of this half's
-        //     steps [hh*HT, hh*HT + HT): independent chains, back to back
+    // (1) Delta and Delta*u of this half's steps [hh*HT, hh*HT + HT) of a
+    //     tile into du_s: independent chains, back to back
+    auto phase1 = [&](const unsigned char* st_, int nv_) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int ck = hh * 2 + q;
             const int off = swz(c, ck);
             float uv[G], dv[G];
-            CK::load(dlt + off, dv);
-            CK::load(ut + off, uv);
+            CK::load(st_ + Lay::kRows + off, dv);
+            CK::load(st_ + off, uv);
 #pragma unroll
             for (int j = 0; j < G; ++j) {
-                float v;
-                if constexpr (ACC) {
-                    const float sarg = dv[j] + bias;
-                    v = SOFTPLUS ? (sarg > 20.0f ? sarg : log1pf(expf(sarg))) : sarg;
-                } else {
-                    // s * log2(e); softplus in log2 units: log2(1 + 2^tl)
-                    const float tl = fmaf(dv[j], kLog2e, bias);
-                    v = SOFTPLUS ? (tl > 30.0f ? tl : lg2_approx(1.0f + ex2_approx(tl))) : tl;
-                }
+                float v = delta_of(dv[j]);
                 const int t = ck * G + j;
-                if (t >= nv) v = 0.0f;   // past the end of the unit: the state is kept
+                if (t >= nv_) v = 0.0f;   // past the end of the unit: the state is kept
                 du_s[t * kCH + c] = make_float2(v, v * uv[j]);
             }
         }
-        __syncthreads();
+    };
 
-        // (2) the recurrence over the tile for this half of the state; the
-        //     inputs and Abar of step t+1 are fetched while step t updates
+    int stage = 0;          // stage of tile `it`
+    uint32_t parity = 0;    // mbarrier phase parity of tile `it`
+    if (ntiles > 0) {
+        const bool to = acquire(0, 0, 0);
+        phase1(smem + Lay::stage(0), (int)min((long long)TT, w.t1 - w.t0));
+        aborted = __syncthreads_or(to);
+    }
+
+    for (int it = 0; it < ntiles && !aborted; ++it) {
+        const long long tt0 = w.t0 + (long long)it * TT;
+        const int nv = (int)min((long long)TT, w.t1 - tt0);   // steps of this unit in the tile
+        const unsigned char* st = smem + Lay::stage(stage);
+        const unsigned char* ut = st;
+        const unsigned char* zt = st + 2 * Lay::kRows;
+        const float4* bct = reinterpret_cast<const float4*>(st + 3 * Lay::kRows) + hh * kNPair;
+
+        // (2) the recurrence over the tile for this half of the state, as a
+        //     three-deep pipeline: at step t the (Delta, Delta*u) of step t+2
+        //     and the B/C row of step t+1 are loaded, Abar of step t+1 is
+        //     formed, and step t updates the state
         float own[HT];   // partial sums of the steps this half finishes
         (void)own;
         {
-            float2 dd = du_s[c];
+            float2 d0 = du_s[c];
+            float2 d1 = du_s[kCH + c];
             float2 ab[kNPair];
             float4 bc[kNPair];
-            abar_step<NT, ACC>(ab, a2, dd.x);
+            abar_step<NT, ACC>(ab, a2, d0.x);
             load_bc<NT>(bc, bct);
 #pragma unroll
             for (int t = 0; t < TT; ++t) {
-                float2 dn = dd;
+                float2 d2 = d1;
                 float2 an[kNPair];
                 float4 bn[kNPair];
+                if (t + 2 < TT) d2 = du_s[(t + 2) * kCH + c];
+                float pt;
                 if (t + 1 < TT) {
-                    dn = du_s[(t + 1) * kCH + c];
                     load_bc<NT>(bn, bct + (t + 1) * (NP / 2));
-                    abar_step<NT, ACC>(an, a2, dn.x);
+                    pt = fused_step<NT, ACC, STATE_ONLY>(h2, ab, an, a2, d1.x, d0.y, bc);
+                } else {
+                    pt = state_step<NT, STATE_ONLY>(h2, ab, d0.y, bc);
                 }
-                const float pt = state_step<NT, STATE_ONLY>(h2, ab, dd.y, bc);
                 if constexpr (STATE_ONLY) {
-                    dsum += dd.x;
+                    dsum += d0.x;
                 } else {
                     part_s[(hh * TT + t) * kCH + c] = pt;
                     // keep the own partial of the steps this half finishes
@@ -650,7 +714,8 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                     }
                 }
                 if (t + 1 < TT) {
-                    dd = dn;
+                    d0 = d1;
+                    d1 = d2;
 #pragma unroll
                     for (int i = 0; i < kNPair; ++i) {
                         ab[i] = an[i];
@@ -660,9 +725,19 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
             }
         }
         if (!STATE_ONLY && tma && tid == 0) bulk_wait_read_0();   // y tile free again
-        __syncthreads();
+        __syncthreads();   // partial sums complete; every read of du_s done
 
-        // (3) outputs of this half's steps: both partial sums, skip term, gate
+        // next tile's data, then (3) the outputs of this tile together with
+        // (1) for the next tile: independent work, issued side by side
+        const bool has_next = it + 1 < ntiles;
+        const int next_stage = stage + 1 == stages ? 0 : stage + 1;
+        const uint32_t next_parity = stage + 1 == stages ? parity ^ 1u : parity;
+        bool to = false;
+        if (has_next) {
+            to = acquire(it + 1, next_stage, next_parity);
+            const long long tn0 = tt0 + TT;
+            phase1(smem + Lay::stage(next_stage), (int)min((long long)TT, w.t1 - tn0));
+        }
         if constexpr (!STATE_ONLY) {
             const float* other = part_s + (1 - hh) * TT * kCH;
 #pragma unroll
@@ -685,7 +760,8 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
             }
             if (tma) fence_proxy_async_smem();
         }
-        __syncthreads();   // stage s consumed, y tile complete
+        // stage consumed, y tile complete, next tile's du_s ready
+        aborted = __syncthreads_or(to);
 
         if (!STATE_ONLY) {
             if (tma) {
@@ -704,10 +780,12 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                 }
             }
         }
-        if (tma && tid == 0 && issued < ntiles) {
-            issue_tile(issued, issued % stages);
+        if (tma && tid == 0 && issued < ntiles && !aborted) {
+            issue_tile(issued, stage);
             ++issued;
         }
+        stage = next_stage;
+        parity = next_parity;
     }
 
     if (tma) {
@@ -1011,7 +1089,8 @@ Plan make_plan(int dev, int dt, long long batch, long long dim, int N, long long
     p.np = kHalves * p.nt;
     p.tt = 64 / esize(dt);
     const int sms = sm_count(dev);
-    int stages = tma ? (tn.stages > 0 ? std::min(tn.stages, kMaxStages) : 2) : 1;
+    // at least two stages: the next tile is filled while this one finishes
+    int stages = tma ? (tn.stages > 1 ? std::min(tn.stages, kMaxStages) : 2) : 2;
     int per_sm = smem_per_sm(dev) / (smem_bytes(dt, p.nt, stages) + 1024);
     per_sm = std::max(1, std::min(per_sm, 16));
     p.stages = stages;
