@@ -912,6 +912,83 @@ state_update_kernel(const StepArgs a) {
     }
 }
 
+// Vectorised generation step for dstate == 16.  Two lanes per (b, d) row,
+// lane q holding state entries [8q, 8q + 8) as two float4.  A block covers
+// 32 channels x 4 batch entries, so the rows of one batch entry are
+// contiguous in memory (coalesced state access) and each A row is read by
+// four rows of the block (L1 hits).  B and C of a row's half are one 16-byte
+// (bf16) or two 16-byte (fp32) loads.  Fast path as in the scan: Delta is
+// kept in log2 units and Abar = ex2(Delta' * A).
+constexpr int kStepDims = 32, kStepBatches = 4;   // block = 32 x 4 rows x 2 lanes
+template <typename T>
+__global__ void __launch_bounds__(2 * kStepDims * kStepBatches)
+state_update16_kernel(const StepArgs a) {
+    constexpr bool ACC = IO<T>::kAccurate;
+    constexpr int N = 16, H = 8;
+    const int tid = threadIdx.x;
+    const int q = tid & 1;
+    const int di = (tid >> 1) % kStepDims, bi = (tid >> 1) / kStepDims;
+    const long long d = (long long)blockIdx.x * kStepDims + di;
+    const long long b = (long long)blockIdx.y * kStepBatches + bi;
+    const long long batch = a.rows / a.dim;
+    const bool ok = d < a.dim && b < batch;
+    float acc = 0.0f, xv = 0.0f, zv = 0.0f, dsk = 0.0f;
+    if (ok) {
+        const long long row = b * a.dim + d;
+        xv = IO<T>::to_f(static_cast<const T*>(a.x)[row]);
+        const float dv = IO<T>::to_f(static_cast<const T*>(a.delta)[row]);
+        const float bias = a.dt_bias ? a.dt_bias[d] : 0.0f;
+        if (a.z) zv = IO<T>::to_f(static_cast<const T*>(a.z)[row]);
+        dsk = a.D_skip ? a.D_skip[d] : 0.0f;
+        float dt, du;   // Delta (log2 units on the fast path) and Delta*u (natural units)
+        if constexpr (ACC) {
+            dt = softplus_f<true>(dv + bias);
+            du = dt * xv;
+        } else {
+            const float tl = fmaf(dv, kLog2e, bias * kLog2e);
+            dt = tl > 30.0f ? tl : lg2_approx(1.0f + ex2_approx(tl));
+            du = dt * kLn2 * xv;
+        }
+        float Bv[H], Cv[H], Av[H];
+        const T* Bb = static_cast<const T*>(a.B) + b * N + H * q;
+        const T* Cb = static_cast<const T*>(a.C) + b * N + H * q;
+        if constexpr (sizeof(T) == 2) {
+            IO<T>::unpack(*reinterpret_cast<const uint4*>(Bb), Bv);
+            IO<T>::unpack(*reinterpret_cast<const uint4*>(Cb), Cv);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                IO<T>::unpack(reinterpret_cast<const uint4*>(Bb)[k], Bv + 4 * k);
+                IO<T>::unpack(reinterpret_cast<const uint4*>(Cb)[k], Cv + 4 * k);
+            }
+        }
+        const float4* Ad = reinterpret_cast<const float4*>(a.A + d * N + H * q);
+        float4* hp = reinterpret_cast<float4*>(a.state + row * N + H * q);
+        const float4 a0 = Ad[0], a1 = Ad[1];
+        float4 h0 = hp[0], h1 = hp[1];
+        Av[0] = a0.x; Av[1] = a0.y; Av[2] = a0.z; Av[3] = a0.w;
+        Av[4] = a1.x; Av[5] = a1.y; Av[6] = a1.z; Av[7] = a1.w;
+        float hs[H] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+        float acc1 = 0.0f;
+#pragma unroll
+        for (int k = 0; k < H; ++k) {
+            const float dA = ACC ? expf(dt * Av[k]) : ex2_approx(dt * Av[k]);
+            hs[k] = fmaf(dA, hs[k], du * Bv[k]);
+            if (k & 1) acc1 = fmaf(Cv[k], hs[k], acc1);
+            else acc = fmaf(Cv[k], hs[k], acc);
+        }
+        acc += acc1;
+        hp[0] = make_float4(hs[0], hs[1], hs[2], hs[3]);
+        hp[1] = make_float4(hs[4], hs[5], hs[6], hs[7]);
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    if (ok && q == 0) {
+        float o = acc + dsk * xv;
+        if (a.z) o *= silu_f<ACC>(zv);
+        static_cast<T*>(a.y)[b * a.dim + d] = IO<T>::from_f(o);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -1484,6 +1561,19 @@ int mamba_state_update(int64_t batch, int64_t dim, int64_t dstate, int io_dtype,
     a.dt_bias = dt_bias; a.A = A; a.D_skip = D_skip; a.y = y;
     a.rows = rows; a.dim = dim; a.dstate = (int)dstate;
     a.vec_state = (dstate % 4 == 0) && aligned(state, 16);
+    // dstate 16 with 16-byte aligned rows: the vectorised two-lane kernel
+    const bool vec16 = dstate == 16 && aligned(state, 16) && aligned(A, 16) && aligned(B, 16) &&
+                       aligned(C, 16) && batch <= 65535LL * kStepBatches;
+    if (vec16) {
+        const dim3 grid((unsigned)((dim + kStepDims - 1) / kStepDims),
+                        (unsigned)((batch + kStepBatches - 1) / kStepBatches));
+        ProfScope prof(kKindStep, stream);
+        if (io_dtype == MAMBA_BF16)
+            state_update16_kernel<__nv_bfloat16><<<grid, 2 * kStepDims * kStepBatches, 0, stream>>>(a);
+        else
+            state_update16_kernel<float><<<grid, 2 * kStepDims * kStepBatches, 0, stream>>>(a);
+        return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
+    }
     const long long threads = rows * 4;
     const unsigned grid = (unsigned)((threads + kThreads - 1) / kThreads);
     {
