@@ -1147,8 +1147,9 @@ int smem_per_sm(int dev) {
 // bound by the ex2 and fp32 issue rates of each sub-partition, so the aim is
 // an equal number of units per SM:
 //   * whole waves of channel tiles (one per SM) scan the whole sequence;
-//   * the tiles left over ("tail", fewer than one per SM) are cut into K time
-//     chunks, K*tail <= #SM, so that each SM takes at most one extra chunk;
+//   * the tiles left over ("tail", fewer than one per SM) also scan the whole
+//     sequence by default; tail = 2 cuts them into K time chunks,
+//     K*tail <= #SM, so that each SM takes at most one extra chunk;
 //   * with fewer tiles than SMs, every tile is cut into K chunks so that
 //     the chunks fill the resident CTA slots of all SMs.
 // A chunk that does not start at t = 0 gets its carried-in state from a
@@ -1182,13 +1183,14 @@ Plan make_plan(int dev, int dt, long long batch, long long dim, int N, long long
         n_chunked = p.n_groups;
         K = tn.chunks;
     } else if (p.n_groups >= sms) {
+        // Whole-sequence units only, unless asked (tail = 2): measured on
+        // B300, the summary pass of a chunked tail costs more than the
+        // imbalance it removes, because each CTA is bound by its own
+        // dependency chain more than by its SM's throughput.
         const int tail = p.n_groups % sms;
-        if (tail > 0 && tn.tail != 1) {
-            const int k = (int)std::min<long long>(sms / tail, max_k);
-            if (k >= 2 || tn.tail == 2) {
-                n_chunked = tail;
-                K = std::max(2, k);
-            }
+        if (tail > 0 && tn.tail == 2) {
+            n_chunked = tail;
+            K = (int)std::max<long long>(2, std::min<long long>(sms / tail, max_k));
         }
     } else if (tn.tail != 1) {
         const int k = (int)std::min<long long>((long long)sms * per_sm / p.n_groups, max_k);
