@@ -176,7 +176,9 @@ int mamba_version(void);
  * Tuning override for experiments, process-wide, affecting later calls of
  * mamba_scan_fwd: tail = how channel tiles that do not fill a whole wave of
  * SMs are scheduled (0 automatic, 1 whole-sequence units only, 2 cut into
- * time chunks), stages = depth of the shared-memory input ring (1..4),
+ * time chunks, 3 cut into time chunks whose passes run on a library-owned
+ * side stream beside the whole-sequence units; mamba_scan_fwd_noalloc
+ * treats 3 as 2), stages = depth of the shared-memory input ring (1..4),
  * chunks = fixed number of time chunks for every channel tile.  0 restores
  * the automatic choice for that knob.  Results do not depend on these
  * settings beyond fp32 rounding order.  Returns MAMBA_ERR_SHAPE for values

@@ -310,6 +310,7 @@ struct ScanArgs {
     int n_full;            // groups [0, n_full) run the whole sequence
     int nchunks;           // time chunks of each remaining ("tail") group
     int tail_rows;         // (n_groups - n_full) * kCH
+    int unit_offset;       // first unit of this launch (main pass)
 };
 
 // Work unit of one CTA.
@@ -517,7 +518,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hh = warp >> 1;                 // which half of the state
     const int c = (warp & 1) * 32 + lane;     // channel within the tile
-    const Unit w = decode_unit<STATE_ONLY>(a, blockIdx.x);
+    const Unit w = decode_unit<STATE_ONLY>(a, (int)blockIdx.x + (STATE_ONLY ? 0 : a.unit_offset));
     const long long dim = a.dim, L_ = a.seqlen;
     const int N = a.dstate;
     const int d = w.d0 + c;
@@ -994,7 +995,7 @@ state_update16_kernel(const StepArgs a) {
 // ---------------------------------------------------------------------------
 
 struct Tuning {
-    int tail = 0;    // 0 = automatic, 1 = whole-sequence units only, 2 = chunk the tail
+    int tail = 0;    // 0 automatic, 1 whole units only, 2 chunk the tail, 3 ... on a side stream
     int stages = 0;  // ring depth (0 = automatic)
     int chunks = 0;  // time chunks for every group (0 = automatic)
 };
@@ -1068,6 +1069,32 @@ int get_pool(int dev, cudaMemPool_t* out) {
     return MAMBA_OK;
 }
 
+// Library-owned side stream and fork/join events of one device, created on
+// first use.  The launch sequence that uses them holds g_side_mu.
+struct Side {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::vector<Side> g_side;
+std::mutex g_side_mu;
+
+int get_side(int dev, Side* out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if ((int)g_side.size() <= dev) g_side.resize(dev + 1);
+    Side& sd = g_side[dev];
+    if (!sd.stream) {
+        if (cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            sd = Side();
+            return MAMBA_ERR_CUDA;
+        }
+    }
+    *out = sd;
+    return MAMBA_OK;
+}
+
 int sm_count(int dev) {
     static std::vector<int> cache;
     std::lock_guard<std::mutex> lk(g_mu);
@@ -1113,6 +1140,7 @@ cudaError_t dispatch_scan(int nt, bool sp, bool hz, const ScanArgs& a, int grid,
 }
 
 struct Plan {
+    bool concurrent;   // chunked tail on a side stream beside the whole-sequence units
     int nt, np, stages, tt;
     int groups_per_batch, n_groups, n_full, nchunks;
     long long chunk_len;
@@ -1147,22 +1175,26 @@ int smem_per_sm(int dev) {
 // bound by the ex2 and fp32 issue rates of each sub-partition, so the aim is
 // an equal number of units per SM:
 //   * whole waves of channel tiles (one per SM) scan the whole sequence;
-//   * the tiles left over ("tail", fewer than one per SM) also scan the whole
-//     sequence by default; tail = 2 cuts them into K time chunks,
-//     K*tail <= #SM, so that each SM takes at most one extra chunk;
+//   * the tiles left over ("tail", fewer than one per SM) are cut into K
+//     time chunks, K*tail <= #SM, whose passes run on a side stream beside
+//     the whole waves, so that each SM takes at most one extra chunk;
 //   * with fewer tiles than SMs, every tile is cut into K chunks so that
 //     the chunks fill the resident CTA slots of all SMs.
 // A chunk that does not start at t = 0 gets its carried-in state from a
 // summary pass (state only, about 3/4 of the work of a main pass) and a
 // carry pass.  Tuning: tail = 1 keeps whole-sequence units only, tail = 2
-// forces the chunked tail; chunks > 0 cuts every tile into that many chunks.
-Plan make_plan(int dev, int dt, long long batch, long long dim, int N, long long L, bool tma) {
+// chunks the tail on the caller's stream, tail = 3 on the side stream;
+// chunks > 0 cuts every tile into that many chunks.  side_ok is false for
+// the no-allocation entry point, which uses the caller's stream only.
+Plan make_plan(int dev, int dt, long long batch, long long dim, int N, long long L, bool tma,
+               bool side_ok) {
     Tuning tn;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         tn = g_tuning;
     }
     Plan p;
+    p.concurrent = false;
     p.nt = N <= 4 ? 2 : (N <= 8 ? 4 : 8);
     p.np = kHalves * p.nt;
     p.tt = 64 / esize(dt);
@@ -1183,14 +1215,18 @@ Plan make_plan(int dev, int dt, long long batch, long long dim, int N, long long
         n_chunked = p.n_groups;
         K = tn.chunks;
     } else if (p.n_groups >= sms) {
-        // Whole-sequence units only, unless asked (tail = 2): measured on
-        // B300, the summary pass of a chunked tail costs more than the
-        // imbalance it removes, because each CTA is bound by its own
-        // dependency chain more than by its SM's throughput.
+        // The leftover tiles are cut into time chunks whose summary, carry
+        // and main passes run on a side stream beside the whole-sequence
+        // units (measured on B300: 278 -> 239 us for the Mamba-2.8B layer).
+        // Run serially on one stream, the summary pass costs more than the
+        // imbalance it removes, so without the side stream (the
+        // no-allocation entry point) the tail scans whole sequences.
         const int tail = p.n_groups % sms;
-        if (tail > 0 && tn.tail == 2) {
+        const int mode = tn.tail != 0 ? tn.tail : (side_ok ? 3 : 1);
+        if (tail > 0 && (mode == 2 || mode == 3)) {
             n_chunked = tail;
             K = (int)std::max<long long>(2, std::min<long long>(sms / tail, max_k));
+            p.concurrent = mode == 3 && side_ok;
         }
     } else if (tn.tail != 1) {
         const int k = (int)std::min<long long>((long long)sms * per_sm / p.n_groups, max_k);
@@ -1200,6 +1236,7 @@ Plan make_plan(int dev, int dt, long long batch, long long dim, int N, long long
         }
     }
     if (n_chunked == 0 || K <= 1) {
+        p.concurrent = false;
         p.n_full = p.n_groups;
         p.nchunks = 1;
         p.chunk_len = L;
@@ -1208,6 +1245,7 @@ Plan make_plan(int dev, int dt, long long batch, long long dim, int N, long long
         p.chunk_len = per * p.tt;
         p.nchunks = (int)((L + p.chunk_len - 1) / p.chunk_len);
         p.n_full = p.nchunks > 1 ? p.n_groups - n_chunked : p.n_groups;
+        p.concurrent = p.concurrent && p.n_full > 0 && p.nchunks > 1;
     }
     return p;
 }
@@ -1357,7 +1395,7 @@ int mamba_profile_end(double* total_ms, int64_t* launches, int nkinds) {
 }
 
 int mamba_scan_set_tuning(int tail, int stages, int chunks) {
-    if (tail < 0 || tail > 2 || stages < 0 || stages > kMaxStages || chunks < 0)
+    if (tail < 0 || tail > 3 || stages < 0 || stages > kMaxStages || chunks < 0)
         return MAMBA_ERR_SHAPE;
     std::lock_guard<std::mutex> lk(g_mu);
     g_tuning.tail = tail;
@@ -1418,7 +1456,7 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     for (const void* q : {u, delta, z, (const void*)y})
         if (q && !aligned(q, 16)) tma = false;
 
-    Plan pl = make_plan(dev, io_dtype, batch, dim, (int)dstate, seqlen, tma);
+    Plan pl = make_plan(dev, io_dtype, batch, dim, (int)dstate, seqlen, tma, !no_alloc);
     const bool chunked = pl.n_full < pl.n_groups && pl.nchunks > 1;
     const bool acc = io_dtype == MAMBA_F32;
 
@@ -1458,7 +1496,7 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
               encode_map(&a.m_y, y, es, bf, seqlen, dim, batch, tt, kCH, true) &&
               encode_map(&a.m_bc, scratch, 4, false, 2 * pl.np, seqlen, batch, 2 * pl.np, tt,
                          false);
-        if (!tma) pl = make_plan(dev, io_dtype, batch, dim, (int)dstate, seqlen, false);
+        if (!tma) pl = make_plan(dev, io_dtype, batch, dim, (int)dstate, seqlen, false, !no_alloc);
     }
     a.u = u; a.delta = delta; a.z = z;
     a.dt_bias = dt_bias; a.A = A; a.D_skip = D_skip; a.y = y; a.final_state = final_state;
@@ -1486,29 +1524,52 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
                 (int)dstate, pl.np, scale);
         e = cudaGetLastError();
     }
-    if (e == cudaSuccess && chunked) {
+    const bool bf = io_dtype == MAMBA_BF16;
+    const bool hz = z != nullptr;
+    auto summary_and_carry = [&](cudaStream_t st) -> cudaError_t {
         const int grid1 = (pl.n_groups - pl.n_full) * (pl.nchunks - 1);
-        e = io_dtype == MAMBA_BF16
-                ? dispatch_scan<__nv_bfloat16, true>(pl.nt, softplus, false, a, grid1, pl.smem,
-                                                     stream)
-                : dispatch_scan<float, true>(pl.nt, softplus, false, a, grid1, pl.smem, stream);
-        if (e == cudaSuccess) {
-            const long long n_ent = (long long)entries;
-            {
-                ProfScope prof(kKindCarry, stream);
-                carry_kernel<<<(unsigned)((n_ent + 255) / 256), 256, 0, stream>>>(
-                    a.ws_P, a.ws_h, n_ent, pl.nchunks);
-            }
-            e = cudaGetLastError();
+        cudaError_t r = bf ? dispatch_scan<__nv_bfloat16, true>(pl.nt, softplus, false, a, grid1,
+                                                               pl.smem, st)
+                           : dispatch_scan<float, true>(pl.nt, softplus, false, a, grid1,
+                                                        pl.smem, st);
+        if (r != cudaSuccess) return r;
+        const long long n_ent = (long long)entries;
+        {
+            ProfScope prof(kKindCarry, st);
+            carry_kernel<<<(unsigned)((n_ent + 255) / 256), 256, 0, st>>>(a.ws_P, a.ws_h, n_ent,
+                                                                          pl.nchunks);
         }
-    }
-    if (e == cudaSuccess) {
-        const int grid = pl.n_full + (chunked ? (pl.n_groups - pl.n_full) * pl.nchunks : 0);
-        e = io_dtype == MAMBA_BF16
-                ? dispatch_scan<__nv_bfloat16, false>(pl.nt, softplus, z != nullptr, a, grid,
-                                                      pl.smem, stream)
-                : dispatch_scan<float, false>(pl.nt, softplus, z != nullptr, a, grid, pl.smem,
-                                              stream);
+        return cudaGetLastError();
+    };
+    auto main_pass = [&](int first, int count, cudaStream_t st) -> cudaError_t {
+        ScanArgs m = a;
+        m.unit_offset = first;
+        return bf ? dispatch_scan<__nv_bfloat16, false>(pl.nt, softplus, hz, m, count, pl.smem, st)
+                  : dispatch_scan<float, false>(pl.nt, softplus, hz, m, count, pl.smem, st);
+    };
+    const int n_chunk_units = chunked ? (pl.n_groups - pl.n_full) * pl.nchunks : 0;
+    if (e == cudaSuccess && pl.concurrent && chunked && !no_alloc) {
+        // whole-sequence units on the caller's stream; the chunked tail
+        // (summary, carry, its main pass) on the side stream beside them
+        Side sd;
+        int rc2 = get_side(dev, &sd);
+        if (rc2 != MAMBA_OK) {
+            cudaFreeAsync(scratch, stream);
+            return rc2;
+        }
+        std::lock_guard<std::mutex> lk(g_side_mu);
+        if (cudaEventRecord(sd.fork, stream) != cudaSuccess ||
+            cudaStreamWaitEvent(sd.stream, sd.fork, 0) != cudaSuccess)
+            e = cudaErrorUnknown;
+        if (e == cudaSuccess) e = main_pass(0, pl.n_full, stream);
+        if (e == cudaSuccess) e = summary_and_carry(sd.stream);
+        if (e == cudaSuccess) e = main_pass(pl.n_full, n_chunk_units, sd.stream);
+        if (cudaEventRecord(sd.join, sd.stream) != cudaSuccess ||
+            cudaStreamWaitEvent(stream, sd.join, 0) != cudaSuccess)
+            e = cudaErrorUnknown;
+    } else {
+        if (e == cudaSuccess && chunked) e = summary_and_carry(stream);
+        if (e == cudaSuccess) e = main_pass(0, pl.n_full + n_chunk_units, stream);
     }
     if (!no_alloc) cudaFreeAsync(scratch, stream);
     return e == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;

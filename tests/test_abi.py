@@ -142,9 +142,9 @@ def test_state_update_validation(lib):
 
 
 def test_tuning_validation(lib):
-    assert lib.mamba_scan_set_tuning(3, 0, 0) == ESHAPE
+    assert lib.mamba_scan_set_tuning(4, 0, 0) == ESHAPE
     assert lib.mamba_scan_set_tuning(-1, 0, 0) == ESHAPE
-    assert lib.mamba_scan_set_tuning(2, 0, 0) == OK
+    assert lib.mamba_scan_set_tuning(3, 0, 0) == OK
     assert lib.mamba_scan_set_tuning(0, 9, 0) == ESHAPE
     assert lib.mamba_scan_set_tuning(0, 0, -1) == ESHAPE
     assert lib.mamba_scan_set_tuning(0, 0, 0) == OK

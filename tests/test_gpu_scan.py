@@ -189,6 +189,24 @@ def test_chunks_and_tails(dtype, tail, chunks, stages):
     assert_close(to_f64(fin), hr, dtype, "final_state")
 
 
+@pytest.mark.parametrize("tail", [1, 2, 3])
+def test_tail_modes_on_a_full_wave(tail):
+    # 3 x 50 channel tiles of 64 fill one wave of 148 SMs with 2 tiles left
+    # over: tail 2 and 3 cut those two into time chunks (3: on the side stream)
+    import selective_state_space_135_b300 as mm
+    shp = synth.ScanShape("tail", 3, 3200, 16, 1024, seed=15)
+    inp = synth.scan_inputs(shp)
+    mm.mamba_scan_set_tuning(tail, 0, 0)
+    y, fin = scan_on_gpu(inp)
+    rows = synth.sample_rows(16, shp.batch, shp.dim, 512)
+    # include every channel of the last tile (the one that is chunked)
+    rows = np.unique(np.concatenate([rows, np.arange(shp.batch * shp.dim - 128, shp.batch * shp.dim)]))
+    ys, hs = oracle.scan_rows(inp, rows)
+    assert_close(to_f64(y.reshape(-1, shp.seqlen)[rows]), ys, shp.dtype)
+    assert_close(to_f64(fin.reshape(-1, shp.dstate)[rows]), hs, shp.dtype, "final_state")
+    assert mm.mamba_device_status() == 0
+
+
 def test_chunk_boundary_reset():
     # A huge Delta at the first step of a chunk resets the state there; the
     # outputs after it must not depend on anything earlier, across the carry.
