@@ -94,6 +94,29 @@ def load_traffic(workload_name):
     return None
 
 
+# --------------------------------------------------------------------------
+# multi-rank bookkeeping (weak scaling: every rank scans its own batch)
+
+def rank_seed(shape, rank):
+    """Seed of rank `rank`'s independent copy of the workload."""
+    return shape.seed + 7919 * rank
+
+
+def max_over_ranks(x, dist_mod=None, device=None):
+    """The largest value of `x` over all ranks (x itself on one rank)."""
+    if dist_mod is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(elems_per_step, steps, world, ms):
+    """Elements per second summed over all ranks, timed by the slowest rank."""
+    return elems_per_step * steps * world / (ms * 1e-3)
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons every 200 ms."""
 
@@ -241,7 +264,7 @@ def run_ours(args, shape):
         pg = dist
     import selective_state_space_135_b300 as mm
 
-    seed = shape.seed + 7919 * rank
+    seed = rank_seed(shape, rank)
     inp = synth.scan_inputs(shape, seed=seed)
     dt = shape.dtype
     u, delta, z, B, C = (synth.to_torch(inp[k], dt, dev) for k in ("u", "delta", "z", "B", "C"))
@@ -281,13 +304,8 @@ def run_ours(args, shape):
     barrier()
     prof = mm.mamba_profile_end()
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-    elems = shape.elems * args.steps * ws
-    value = elems / (ms * 1e-3)
+    ms = max_over_ranks(e0.elapsed_time(e1), pg, dev)
+    value = whole_job_rate(shape.elems, args.steps, ws, ms)
     ms_per_step = ms / args.steps
 
     # The roofline is taken over the whole scan call: its main pass may run
@@ -389,12 +407,8 @@ def e2e_leg(args, shape, inp, dev, stream, mm, ws, pg):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1)
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": shape.elems * k * ws / (ms * 1e-3), "unit": UNIT,
+    ms = max_over_ranks(e0.elapsed_time(e1), pg, dev)
+    return {"value": whole_job_rate(shape.elems, k, ws, ms), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k,
             "ms_per_step": ms / k}
 

@@ -169,6 +169,17 @@ const char *mamba_status_string(int status);
  */
 int mamba_device_status(cudaStream_t stream);
 
+/*
+ * Self-test of the failure path of the bounded device waits.  Launches one
+ * thread that waits on an mbarrier nothing ever completes, for limit_us
+ * microseconds (1 .. 2,000,000), then records the timeout in the device error
+ * word and returns, as the scan kernels do when a copy never lands.  A later
+ * mamba_device_status(stream) returns MAMBA_ERR_TIMEOUT and clears the word.
+ * Nothing hangs and the context stays usable.  Returns MAMBA_ERR_SHAPE for
+ * a limit out of range.
+ */
+int mamba_selftest_wait_timeout(int64_t limit_us, cudaStream_t stream);
+
 /* Library version as major*100 + minor. */
 int mamba_version(void);
 

@@ -21,6 +21,7 @@ from ._lib import (  # noqa: F401
     mamba_scan_fwd,
     mamba_scan_fwd_noalloc,
     mamba_scan_set_tuning,
+    mamba_selftest_wait_timeout,
     mamba_state_update,
     mamba_status_string,
     mamba_version,

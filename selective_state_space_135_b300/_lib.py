@@ -16,7 +16,7 @@ MAMBA_BF16 = 1
 
 # every symbol the header declares
 EXPORTS = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_state_update", "mamba_status_string",
-           "mamba_device_status", "mamba_version", "mamba_scan_set_tuning",
+           "mamba_device_status", "mamba_selftest_wait_timeout", "mamba_version", "mamba_scan_set_tuning",
            "mamba_profile_begin", "mamba_profile_end")
 
 KIND_NAMES = ("scan", "chunk_summary", "chunk_carry", "state_update", "pack_bc")
@@ -55,6 +55,8 @@ def load():
         lib.mamba_status_string.restype = ctypes.c_char_p
         lib.mamba_device_status.argtypes = [vp]
         lib.mamba_device_status.restype = i32
+        lib.mamba_selftest_wait_timeout.argtypes = [i64, vp]
+        lib.mamba_selftest_wait_timeout.restype = i32
         lib.mamba_version.argtypes = []
         lib.mamba_version.restype = i32
         lib.mamba_scan_set_tuning.argtypes = [i32, i32, i32]
@@ -206,6 +208,16 @@ def mamba_device_status(stream=None) -> int:
     lib = load()
     dev = torch.device("cuda", torch.cuda.current_device())
     return lib.mamba_device_status(_stream_handle(stream, dev))
+
+
+def mamba_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Launch the bounded-wait self-test (a wait that can only time out)."""
+    torch = _torch()
+    lib = load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    rc = lib.mamba_selftest_wait_timeout(int(limit_us), _stream_handle(stream, dev))
+    if rc != 0:
+        raise MambaError(rc, "mamba_selftest_wait_timeout")
 
 
 def mamba_scan_set_tuning(tail: int = 0, stages: int = 0, chunks: int = 0) -> None:

@@ -184,13 +184,14 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // Bounded wait: true when the phase completed, false after kWaitLimitNs.
 // The global timer is read only after 4096 unsuccessful polls: reading it is
 // slow, and a wait that ends within a few microseconds never needs it.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     for (int i = 0; i < 4096; ++i)
         if (mbar_test_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (unsigned it = 0;; ++it) {
         if (mbar_test_wait(bar, parity)) return true;
-        if ((it & 255u) == 255u && global_ns() - t0 > kWaitLimitNs) return false;
+        if ((it & 255u) == 255u && global_ns() - t0 > limit_ns) return false;
     }
 }
 __device__ __forceinline__ void bulk_commit() {
@@ -990,6 +991,17 @@ state_update16_kernel(const StepArgs a) {
     }
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier that no
+// copy and no thread ever completes, with a short limit, then records the
+// timeout in the device error word exactly as the scan does, and returns.
+__global__ void wait_timeout_selftest_kernel(unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    if (!mbar_wait_bounded(smem_u32(&bar), 0, limit_ns)) atomicExch(&g_error_word, 1);
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -1392,6 +1404,12 @@ int mamba_profile_end(double* total_ms, int64_t* launches, int nkinds) {
     }
     g_prof_recs.clear();
     return rc;
+}
+
+int mamba_selftest_wait_timeout(int64_t limit_us, cudaStream_t stream) {
+    if (limit_us < 1 || limit_us > 2000000) return MAMBA_ERR_SHAPE;
+    wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>((unsigned long long)limit_us * 1000ull);
+    return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
 
 int mamba_scan_set_tuning(int tail, int stages, int chunks) {
