@@ -11,23 +11,24 @@
 //
 // Design (one GPU, no tensor cores: the work is an elementwise recurrence
 // whose cost is one exp and four fp32 multiply/adds per state entry and step):
-//   * A CTA is four warps (one per SM sub-partition) over 64 channels of
-//     one batch entry.  Two warps share each block of 32 channels, one lane
-//     per channel, each warp holding half of the N state entries in
-//     registers, so a B/C load of a warp is a single-address broadcast and
-//     the SM still gets two warps per sub-partition on the Mamba-2.8B layer.
-//     The CTA walks time in tiles of one 64-byte row per channel (32 bf16 or
-//     16 fp32 steps).
+//   * A CTA is four warps (one per SM sub-partition).  SPLIT warps share a
+//     block of 32 channels, one lane per channel, each warp holding 1/SPLIT
+//     of the N state entries in registers (SPLIT = 4 for dstate > 8: a CTA
+//     covers 32 channels; SPLIT = 2 otherwise: 64 channels).  Every B/C load
+//     of a warp is therefore a single-address broadcast, and the SM gets
+//     several warps per sub-partition even on the Mamba-2.8B layer.  The
+//     CTA walks time in tiles of one 64-byte row per channel (32 bf16 or 16
+//     fp32 steps).
 //   * u, delta, z and y tiles move by tensor-map bulk copies
 //     (cp.async.bulk.tensor, completion on an mbarrier ring), 64-byte swizzled
 //     so that the per-lane 16-byte row accesses are bank-conflict free.
 //   * B and C (shared by all channels of a batch entry) are packed once per
 //     call by a small kernel into fp32 rows of (B pair, C pair) per step and
 //     staged by the same bulk copies.
-//   * Per tile each half computes Delta and Delta*u for half of the steps
-//     into shared memory, both halves run the recurrence over the tile, and
-//     each half finishes half of the outputs (both partial sums C.h, skip
-//     term, gate): no per-token work is done twice.
+//   * Per tile each slice computes Delta and Delta*u for 1/SPLIT of the
+//     steps into shared memory, every slice runs the recurrence over the
+//     tile, and each slice finishes 1/SPLIT of the outputs (all partial sums
+//     C.h in a fixed order, skip term, gate): no per-token work is done twice.
 //   * The expanded (b, d, t, n) tensor is never materialised: Abar and the
 //     input term live only in registers; the state leaves the SM only at the
 //     end of a work unit.
@@ -232,9 +233,11 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
 // scan kernels
 // ---------------------------------------------------------------------------
 
-constexpr int kScanWarps = 4;                    // warps per CTA, one per SM sub-partition
-constexpr int kHalves = 2;                       // warps sharing a channel, half the state each
-constexpr int kCH = 32 * kScanWarps / kHalves;   // channels per CTA
+constexpr int kScanWarps = 4;   // warps per CTA, one per SM sub-partition
+// SPLIT warps share a block of 32 channels, each holding 1/SPLIT of the
+// state; a CTA therefore covers 32 * kScanWarps / SPLIT channels.
+template <int SPLIT>
+constexpr int channels_per_cta() { return 32 * kScanWarps / SPLIT; }
 
 // One 16-byte chunk of a row <-> fp32 values (8 for bf16, 4 for fp32).
 template <typename T> struct Chunk;
@@ -306,11 +309,12 @@ struct ScanArgs {
     int dstate;
     int use_tma;
     int stages;
-    int groups_per_batch;  // ceil(dim / kCH)
+    int ch;                // channels per CTA
+    int groups_per_batch;  // ceil(dim / ch)
     int n_groups;          // batch * groups_per_batch
     int n_full;            // groups [0, n_full) run the whole sequence
     int nchunks;           // time chunks of each remaining ("tail") group
-    int tail_rows;         // (n_groups - n_full) * kCH
+    int tail_rows;         // (n_groups - n_full) * ch
     int unit_offset;       // first unit of this launch (main pass)
 };
 
@@ -342,7 +346,7 @@ __device__ __forceinline__ Unit decode_unit(const ScanArgs& a, int idx) {
         w.k = j % a.nchunks;
     }
     w.b = g / a.groups_per_batch;
-    w.d0 = (g % a.groups_per_batch) * kCH;
+    w.d0 = (g % a.groups_per_batch) * a.ch;
     if (g < a.n_full) {
         w.tail = -1;
         w.t0 = 0;
@@ -361,21 +365,23 @@ __device__ __forceinline__ Unit decode_unit(const ScanArgs& a, int idx) {
 // row r sits at r*64 + ((j ^ ((r >> 1) & 3)) << 4), which makes the
 // per-lane 16-byte row accesses of a warp bank-conflict free.
 //   [0, 1024)       stage mbarriers
-//   stage s         u | delta | z tiles (kCH x 64 B each) | packed B/C (TT x 2*NP fp32)
-//   y tile          kCH x 64 B
+//   stage s         u | delta | z tiles (CH x 64 B each) | packed B/C (TT x 2*NP fp32)
+//   y tile          CH x 64 B
 //   du              (Delta, Delta*u) of every (step, channel) of a tile, float2
-//   part            sum_n C*h of each half of the state, [2][TT][kCH] fp32
-template <typename T, int NT>
+//   part            sum_n C*h of each slice of the state for the steps other
+//                   slices finish, [SPLIT][TT - TT/SPLIT][CH] fp32
+template <typename T, int NT, int SPLIT>
 struct ScanLayout {
-    static constexpr int NP = kHalves * NT;           // padded state size
+    static constexpr int CH = channels_per_cta<SPLIT>();
+    static constexpr int NP = SPLIT * NT;             // padded state size
     static constexpr int kTT = 64 / (int)sizeof(T);   // steps per tile
     static constexpr int kG = 16 / (int)sizeof(T);    // steps per 16-byte chunk
-    static constexpr int kRows = kCH * 64;
+    static constexpr int kRows = CH * 64;
     static constexpr int kBCBytes = kTT * 2 * NP * 4;
     static constexpr int kBC = (kBCBytes + 1023) / 1024 * 1024;
     static constexpr int kStage = 3 * kRows + kBC;
-    static constexpr int kDU = kTT * kCH * 8;
-    static constexpr int kPart = kHalves * kTT * kCH * 4;
+    static constexpr int kDU = kTT * CH * 8;
+    static constexpr int kPart = SPLIT * (kTT - kTT / SPLIT) * CH * 4;
     __host__ __device__ static constexpr int stage(int s) { return 1024 + s * kStage; }
     __host__ __device__ static constexpr int ybuf(int stages) { return stage(stages); }
     __host__ __device__ static constexpr int du(int stages) { return ybuf(stages) + kRows; }
@@ -484,32 +490,33 @@ __device__ __forceinline__ void load_bc(float4 (&bc)[NT / 2], const float4* row)
     for (int i = 0; i < NT / 2; ++i) bc[i] = row[i];
 }
 
-// The scan over one work unit (kCH channels x a time range).  Warp w holds
-// channels [32*(w & 1), 32*(w & 1) + 32) of the tile, one lane per channel,
-// and state entries [NT*(w >> 1), NT*(w >> 1) + NT) of each: the two warps of
+// The scan over one work unit (CH channels x a time range).  With
+// CW = kScanWarps / SPLIT channel blocks per CTA, warp w holds channels
+// [32*(w % CW), 32*(w % CW) + 32) of the tile, one lane per channel, and
+// state entries [NT*(w / CW), NT*(w / CW) + NT) of each: the SPLIT warps of
 // a channel block split the state, so every B/C load of a warp is a
 // single-address broadcast.  Per tile:
-//   (1) each half computes Delta and Delta*u for half of the steps into
+//   (1) each slice computes Delta and Delta*u for 1/SPLIT of the steps into
 //       shared memory (no per-token work is done twice);
-//   (2) both halves run the recurrence over all steps of the tile and store
-//       their partial sums sum_n C*h;
-//   (3) each half finishes half of the outputs: both partial sums, skip
-//       term and gate.
+//   (2) every slice runs the recurrence over all steps of the tile and
+//       stores its partial sums sum_n C*h;
+//   (3) each slice finishes 1/SPLIT of the outputs: all partial sums (in a
+//       fixed order), skip term and gate.
 // STATE_ONLY is the chunk-summary pass: no C, z or y; it returns
 // (exp(A*sum Delta), h_end).
-template <typename T, int NT, bool STATE_ONLY, bool SOFTPLUS, bool HAS_Z>
+template <typename T, int NT, int SPLIT, bool STATE_ONLY, bool SOFTPLUS, bool HAS_Z>
 __global__ void __launch_bounds__(32 * kScanWarps)
 scan_kernel(const __grid_constant__ ScanArgs a) {
-    using Lay = ScanLayout<T, NT>;
+    using Lay = ScanLayout<T, NT, SPLIT>;
     using CK = Chunk<T>;
-    constexpr int NP = Lay::NP;
-    constexpr int TT = Lay::kTT, G = Lay::kG, HT = TT / kHalves;
+    constexpr int NP = Lay::NP, CH = Lay::CH, CW = kScanWarps / SPLIT;
+    constexpr int TT = Lay::kTT, G = Lay::kG, HT = TT / SPLIT, QC = HT / G;
     constexpr int kNThr = 32 * kScanWarps;
     constexpr bool ACC = IO<T>::kAccurate;
     constexpr int kNPair = NT / 2;
     constexpr bool has_z = !STATE_ONLY && HAS_Z;
     static_assert(NT % 2 == 0 && NP <= kMaxN, "bad state size");
-    static_assert(CK::G == G && HT == 2 * G, "a half tile is two 16-byte chunks");
+    static_assert(CK::G == G && QC * G == HT && QC >= 1, "a slice's steps are whole 16-byte chunks");
 
     // Offset the __shared__ array itself (not a pointer rebuilt from an
     // integer) so that every access below stays a shared-memory access.
@@ -517,24 +524,26 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int hh = warp >> 1;                 // which half of the state
-    const int c = (warp & 1) * 32 + lane;     // channel within the tile
+    const int hh = warp / CW;                 // which slice of the state
+    const int c = (warp % CW) * 32 + lane;    // channel within the tile
     const Unit w = decode_unit<STATE_ONLY>(a, (int)blockIdx.x + (STATE_ONLY ? 0 : a.unit_offset));
     const long long dim = a.dim, L_ = a.seqlen;
     const int N = a.dstate;
     const int d = w.d0 + c;
     const bool chan_ok = d < dim;
-    const int rows_valid = (int)min((long long)kCH, dim - w.d0);
+    const int rows_valid = (int)min((long long)CH, dim - w.d0);
     const long long row = (long long)w.b * dim + d;
     const int stages = a.stages;
     const bool tma = a.use_tma != 0;
     const int ntiles = (int)((w.t1 - w.t0 + TT - 1) / TT);
-    const int wrow = (w.tail >= 0) ? w.tail * kCH + c : 0;
+    const int wrow = (w.tail >= 0) ? w.tail * CH + c : 0;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     unsigned char* yt = smem + Lay::ybuf(stages);
-    float2* du_s = reinterpret_cast<float2*>(smem + Lay::du(stages));      // [TT][kCH]
-    float* part_s = reinterpret_cast<float*>(smem + Lay::part(stages));    // [2][TT][kCH]
+    float2* du_s = reinterpret_cast<float2*>(smem + Lay::du(stages));      // [TT][CH]
+    // [SPLIT][TT - HT][CH]: slice q's partial of step t sits at row
+    // (t < q*HT ? t : t - HT), skipping the steps slice q finishes itself
+    float* part_s = reinterpret_cast<float*>(smem + Lay::part(stages));
 
     // ---- per-thread constants and initial state ----
     float2 h2[kNPair], a2[kNPair];
@@ -579,8 +588,8 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
         const long long tt0 = w.t0 + (long long)it * TT;
         const int nv = (int)min((long long)TT, L_ - tt0);
         unsigned char* st = smem + Lay::stage(sidx);
-        for (int e = tid; e < ntens * kCH * TT; e += kNThr) {
-            const int tsr = e / (kCH * TT), rem = e % (kCH * TT);
+        for (int e = tid; e < ntens * CH * TT; e += kNThr) {
+            const int tsr = e / (CH * TT), rem = e % (CH * TT);
             const int cc = rem / TT, t = rem % TT;
             const T* src = static_cast<const T*>(tsr == 0 ? a.u : (tsr == 1 ? a.delta : a.z));
             T v = IO<T>::from_f(0.0f);
@@ -642,12 +651,12 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
         }
     };
 
-    // (1) Delta and Delta*u of this half's steps [hh*HT, hh*HT + HT) of a
+    // (1) Delta and Delta*u of this slice's steps [hh*HT, hh*HT + HT) of a
     //     tile into du_s: independent chains, back to back
     auto phase1 = [&](const unsigned char* st_, int nv_) {
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int ck = hh * 2 + q;
+        for (int q = 0; q < QC; ++q) {
+            const int ck = hh * QC + q;
             const int off = swz(c, ck);
             float uv[G], dv[G];
             CK::load(st_ + Lay::kRows + off, dv);
@@ -657,7 +666,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                 float v = delta_of(dv[j]);
                 const int t = ck * G + j;
                 if (t >= nv_) v = 0.0f;   // past the end of the unit: the state is kept
-                du_s[t * kCH + c] = make_float2(v, v * uv[j]);
+                du_s[t * CH + c] = make_float2(v, v * uv[j]);
             }
         }
     };
@@ -682,11 +691,22 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
         //     three-deep pipeline: at step t the (Delta, Delta*u) of step t+2
         //     and the B/C row of step t+1 are loaded, Abar of step t+1 is
         //     formed, and step t updates the state
-        float own[HT];   // partial sums of the steps this half finishes
+        float own[HT];   // partial sums of the steps this slice finishes
         (void)own;
         {
+            // where this slice's partial of step t goes: registers for its own
+            // steps, row t (steps before them) or row t - HT (steps after)
+            float* pseg[SPLIT];
+            bool mine[SPLIT];
+#pragma unroll
+            for (int k = 0; k < SPLIT; ++k) {
+                mine[k] = k == hh;
+                pseg[k] = part_s + (hh * (TT - HT) - (k < hh ? 0 : HT)) * CH + c;
+            }
+            (void)pseg;
+            (void)mine;
             float2 d0 = du_s[c];
-            float2 d1 = du_s[kCH + c];
+            float2 d1 = du_s[CH + c];
             float2 ab[kNPair];
             float4 bc[kNPair];
             abar_step<NT, ACC>(ab, a2, d0.x);
@@ -696,7 +716,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                 float2 d2 = d1;
                 float2 an[kNPair];
                 float4 bn[kNPair];
-                if (t + 2 < TT) d2 = du_s[(t + 2) * kCH + c];
+                if (t + 2 < TT) d2 = du_s[(t + 2) * CH + c];
                 float pt;
                 if (t + 1 < TT) {
                     load_bc<NT>(bn, bct + (t + 1) * (NP / 2));
@@ -707,13 +727,10 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                 if constexpr (STATE_ONLY) {
                     dsum += d0.x;
                 } else {
-                    part_s[(hh * TT + t) * kCH + c] = pt;
-                    // keep the own partial of the steps this half finishes
-                    if (t < HT) {
-                        if (hh == 0) own[t] = pt;
-                    } else {
-                        if (hh == 1) own[t - HT] = pt;
-                    }
+                    if (mine[t / HT])
+                        own[t % HT] = pt;
+                    else
+                        pseg[t / HT][t * CH] = pt;
                 }
                 if (t + 1 < TT) {
                     d0 = d1;
@@ -741,10 +758,17 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
             phase1(smem + Lay::stage(next_stage), (int)min((long long)TT, w.t1 - tn0));
         }
         if constexpr (!STATE_ONLY) {
-            const float* other = part_s + (1 - hh) * TT * kCH;
+            // the other slices' partials of this slice's steps t = hh*HT + i:
+            // slice r = (hh + k) % SPLIT keeps them at row t (r > hh) or t - HT
+            const float* pk[SPLIT > 1 ? SPLIT - 1 : 1];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int ck = hh * 2 + q;
+            for (int k = 1; k < SPLIT; ++k) {
+                const int r = (hh + k) % SPLIT;
+                pk[k - 1] = part_s + (r * (TT - HT) + hh * HT - (r > hh ? 0 : HT)) * CH + c;
+            }
+#pragma unroll
+            for (int q = 0; q < QC; ++q) {
+                const int ck = hh * QC + q;
                 const int off = swz(c, ck);
                 float uv[G], zv[G], ov[G];
                 (void)zv;
@@ -752,8 +776,10 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                 if constexpr (has_z) CK::load(zt + off, zv);
 #pragma unroll
                 for (int j = 0; j < G; ++j) {
-                    const int t = ck * G + j;
-                    float o = own[q * G + j] + other[t * kCH + c];
+                    // own partial, then the other slices' in a fixed rotation
+                    float o = own[q * G + j];
+#pragma unroll
+                    for (int k = 1; k < SPLIT; ++k) o += pk[k - 1][(q * G + j) * CH];
                     o = fmaf(dsk, uv[j], o);
                     if constexpr (has_z) o *= silu_f<ACC>(zv[j]);
                     ov[j] = o;
@@ -772,7 +798,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                     bulk_commit();
                 }
             } else {
-                for (int e = tid; e < kCH * TT; e += kNThr) {
+                for (int e = tid; e < CH * TT; e += kNThr) {
                     const int cc = e / TT, t = e % TT;
                     if (cc < rows_valid && t < nv) {
                         const int byte = t * (int)sizeof(T);
@@ -1119,9 +1145,9 @@ int sm_count(int dev) {
     return cache[dev];
 }
 
-template <typename T, int NT, bool STATE_ONLY, bool SP, bool HZ>
+template <typename T, int NT, int SPLIT, bool STATE_ONLY, bool SP, bool HZ>
 cudaError_t launch_scan(const ScanArgs& a, int grid, int smem, cudaStream_t st) {
-    auto k = scan_kernel<T, NT, STATE_ONLY, SP, HZ>;
+    auto k = scan_kernel<T, NT, SPLIT, STATE_ONLY, SP, HZ>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     ProfScope prof(STATE_ONLY ? kKindSummary : kKindScan, st);
@@ -1129,22 +1155,30 @@ cudaError_t launch_scan(const ScanArgs& a, int grid, int smem, cudaStream_t st) 
     return cudaGetLastError();
 }
 
-// State entries per lane NT (half of the padded state): 2, 4, 8.
-#define MAMBA_VARIANTS(X) X(2) X(4) X(8)
+// (state entries per lane NT, warps sharing a channel block SPLIT): padded
+// state NT * SPLIT of 4 -> (2, 2), 8 -> (4, 2), 16 -> (4, 4).  Measured on
+// B300 for dstate 16, four slices of 4 beat two of 8: half the channels per
+// CTA (45 KB of shared memory, five CTAs per SM) give each SM sub-partition
+// twice the warps to hide latency with, at about 6% more instructions.
+#if MAMBA_SPLIT16 == 2
+#define MAMBA_VARIANTS(X) X(2, 2) X(4, 2) X(8, 2)
+#else
+#define MAMBA_VARIANTS(X) X(2, 2) X(4, 2) X(4, 4)
+#endif
 
 template <typename T, bool STATE_ONLY>
-cudaError_t dispatch_scan(int nt, bool sp, bool hz, const ScanArgs& a, int grid, int smem,
-                          cudaStream_t st) {
-#define X(NT_)                                                                              \
-    if (nt == NT_) {                                                                         \
+cudaError_t dispatch_scan(int nt, int split, bool sp, bool hz, const ScanArgs& a, int grid,
+                          int smem, cudaStream_t st) {
+#define X(NT_, S_)                                                                          \
+    if (nt == NT_ && split == S_) {                                                          \
         if (STATE_ONLY)                                                                      \
-            return sp ? launch_scan<T, NT_, STATE_ONLY, true, false>(a, grid, smem, st)      \
-                      : launch_scan<T, NT_, STATE_ONLY, false, false>(a, grid, smem, st);    \
+            return sp ? launch_scan<T, NT_, S_, STATE_ONLY, true, false>(a, grid, smem, st)  \
+                      : launch_scan<T, NT_, S_, STATE_ONLY, false, false>(a, grid, smem, st); \
         if (sp)                                                                              \
-            return hz ? launch_scan<T, NT_, STATE_ONLY, true, true>(a, grid, smem, st)       \
-                      : launch_scan<T, NT_, STATE_ONLY, true, false>(a, grid, smem, st);     \
-        return hz ? launch_scan<T, NT_, STATE_ONLY, false, true>(a, grid, smem, st)          \
-                  : launch_scan<T, NT_, STATE_ONLY, false, false>(a, grid, smem, st);        \
+            return hz ? launch_scan<T, NT_, S_, STATE_ONLY, true, true>(a, grid, smem, st)   \
+                      : launch_scan<T, NT_, S_, STATE_ONLY, true, false>(a, grid, smem, st); \
+        return hz ? launch_scan<T, NT_, S_, STATE_ONLY, false, true>(a, grid, smem, st)      \
+                  : launch_scan<T, NT_, S_, STATE_ONLY, false, false>(a, grid, smem, st);    \
     }
     MAMBA_VARIANTS(X)
 #undef X
@@ -1153,22 +1187,27 @@ cudaError_t dispatch_scan(int nt, bool sp, bool hz, const ScanArgs& a, int grid,
 
 struct Plan {
     bool concurrent;   // chunked tail on a side stream beside the whole-sequence units
-    int nt, np, stages, tt;
+    int nt, split, ch, np, stages, tt;
     int groups_per_batch, n_groups, n_full, nchunks;
     long long chunk_len;
     int smem;
 };
 
 template <typename T>
-int smem_bytes_t(int nt, int stages) {
-    if (nt == 2) return ScanLayout<T, 2>::bytes(stages);
-    if (nt == 4) return ScanLayout<T, 4>::bytes(stages);
-    return ScanLayout<T, 8>::bytes(stages);
+int smem_bytes_t(int nt, int split, int stages) {
+    if (split == 4) return ScanLayout<T, 4, 4>::bytes(stages);
+    if (nt == 2) return ScanLayout<T, 2, 2>::bytes(stages);
+    if (nt == 4) return ScanLayout<T, 4, 2>::bytes(stages);
+    return ScanLayout<T, 8, 2>::bytes(stages);
 }
-int smem_bytes(int dt, int nt, int stages) {
-    return dt == MAMBA_BF16 ? smem_bytes_t<__nv_bfloat16>(nt, stages)
-                            : smem_bytes_t<float>(nt, stages);
+int smem_bytes(int dt, int nt, int split, int stages) {
+    return dt == MAMBA_BF16 ? smem_bytes_t<__nv_bfloat16>(nt, split, stages)
+                            : smem_bytes_t<float>(nt, split, stages);
 }
+
+#ifndef MAMBA_SPLIT16
+#define MAMBA_SPLIT16 4
+#endif
 
 int smem_per_sm(int dev) {
     static std::vector<int> cache;
@@ -1182,7 +1221,7 @@ int smem_per_sm(int dev) {
     return cache[dev];
 }
 
-// Work decomposition.  A unit is a tile of kCH channels of one batch entry
+// Work decomposition.  A unit is a tile of `ch` channels of one batch entry
 // (one CTA, one warp per SM sub-partition) over a time range.  The kernel is
 // bound by the ex2 and fp32 issue rates of each sub-partition, so the aim is
 // an equal number of units per SM:
@@ -1207,17 +1246,20 @@ Plan make_plan(int dev, int dt, long long batch, long long dim, int N, long long
     }
     Plan p;
     p.concurrent = false;
-    p.nt = N <= 4 ? 2 : (N <= 8 ? 4 : 8);
-    p.np = kHalves * p.nt;
+    // padded state 4, 8 or 16; dstate > 8 splits it MAMBA_SPLIT16 ways
+    p.split = N > 8 ? MAMBA_SPLIT16 : 2;
+    p.np = N <= 4 ? 4 : (N <= 8 ? 8 : 16);
+    p.nt = p.np / p.split;
+    p.ch = 32 * kScanWarps / p.split;
     p.tt = 64 / esize(dt);
     const int sms = sm_count(dev);
     // at least two stages: the next tile is filled while this one finishes
     int stages = tma ? (tn.stages > 1 ? std::min(tn.stages, kMaxStages) : 2) : 2;
-    int per_sm = smem_per_sm(dev) / (smem_bytes(dt, p.nt, stages) + 1024);
+    int per_sm = smem_per_sm(dev) / (smem_bytes(dt, p.nt, p.split, stages) + 1024);
     per_sm = std::max(1, std::min(per_sm, 16));
     p.stages = stages;
-    p.smem = smem_bytes(dt, p.nt, stages);
-    p.groups_per_batch = (int)((dim + kCH - 1) / kCH);
+    p.smem = smem_bytes(dt, p.nt, p.split, stages);
+    p.groups_per_batch = (int)((dim + p.ch - 1) / p.ch);
     p.n_groups = (int)(batch * p.groups_per_batch);
     const long long tiles = (L + p.tt - 1) / p.tt;
     const long long min_chunk_tiles = 4;
@@ -1234,7 +1276,9 @@ Plan make_plan(int dev, int dt, long long batch, long long dim, int N, long long
         // imbalance it removes, so without the side stream (the
         // no-allocation entry point) the tail scans whole sequences.
         const int tail = p.n_groups % sms;
-        const int mode = tn.tail != 0 ? tn.tail : (side_ok ? 3 : 1);
+        // automatic: chunk the tail only when it is at most a third of a
+        // wave; a larger tail costs more in summary work than it saves
+        const int mode = tn.tail != 0 ? tn.tail : (side_ok && 3 * tail <= sms ? 3 : 1);
         if (tail > 0 && (mode == 2 || mode == 3)) {
             n_chunked = tail;
             K = (int)std::max<long long>(2, std::min<long long>(sms / tail, max_k));
@@ -1329,8 +1373,7 @@ int noalloc_scratch(int dev, void** out) {
 
 // Bytes of packed B/C rows per (batch entry, step): 2 * padded state * fp32.
 long long packed_row_bytes(int64_t dstate) {
-    const int nt = dstate <= 4 ? 2 : (dstate <= 8 ? 4 : 8);
-    return 2LL * kHalves * nt * (long long)sizeof(float);
+    return 2LL * (dstate <= 4 ? 4 : (dstate <= 8 ? 8 : 16)) * (long long)sizeof(float);
 }
 
 }  // namespace mamba
@@ -1480,7 +1523,7 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
 
     // scratch: packed B/C rows, then the chunk summaries
     const size_t bc_bytes = (size_t)batch * (size_t)seqlen * (size_t)pl.np * 2 * sizeof(float);
-    const size_t tail_rows = (size_t)(pl.n_groups - pl.n_full) * kCH;
+    const size_t tail_rows = (size_t)(pl.n_groups - pl.n_full) * pl.ch;
     const size_t entries = tail_rows * (size_t)dstate;
     const size_t ws_bytes = chunked ? 2 * entries * (size_t)(pl.nchunks - 1) * sizeof(float) : 0;
     void* scratch = nullptr;
@@ -1508,10 +1551,10 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     if (tma) {
         const bool bf = io_dtype == MAMBA_BF16;
         const int tt = pl.tt;
-        tma = encode_map(&a.m_u, u, es, bf, seqlen, dim, batch, tt, kCH, true) &&
-              encode_map(&a.m_dl, delta, es, bf, seqlen, dim, batch, tt, kCH, true) &&
-              (!z || encode_map(&a.m_z, z, es, bf, seqlen, dim, batch, tt, kCH, true)) &&
-              encode_map(&a.m_y, y, es, bf, seqlen, dim, batch, tt, kCH, true) &&
+        tma = encode_map(&a.m_u, u, es, bf, seqlen, dim, batch, tt, pl.ch, true) &&
+              encode_map(&a.m_dl, delta, es, bf, seqlen, dim, batch, tt, pl.ch, true) &&
+              (!z || encode_map(&a.m_z, z, es, bf, seqlen, dim, batch, tt, pl.ch, true)) &&
+              encode_map(&a.m_y, y, es, bf, seqlen, dim, batch, tt, pl.ch, true) &&
               encode_map(&a.m_bc, scratch, 4, false, 2 * pl.np, seqlen, batch, 2 * pl.np, tt,
                          false);
         if (!tma) pl = make_plan(dev, io_dtype, batch, dim, (int)dstate, seqlen, false, !no_alloc);
@@ -1521,6 +1564,7 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     a.dim = dim; a.seqlen = seqlen; a.chunk_len = pl.chunk_len;
     a.batch = (int)batch; a.dstate = (int)dstate;
     a.use_tma = tma ? 1 : 0; a.stages = pl.stages;
+    a.ch = pl.ch;
     a.groups_per_batch = pl.groups_per_batch; a.n_groups = pl.n_groups;
     a.n_full = pl.n_full; a.nchunks = pl.nchunks;
     a.tail_rows = (int)tail_rows;
@@ -1546,9 +1590,9 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     const bool hz = z != nullptr;
     auto summary_and_carry = [&](cudaStream_t st) -> cudaError_t {
         const int grid1 = (pl.n_groups - pl.n_full) * (pl.nchunks - 1);
-        cudaError_t r = bf ? dispatch_scan<__nv_bfloat16, true>(pl.nt, softplus, false, a, grid1,
+        cudaError_t r = bf ? dispatch_scan<__nv_bfloat16, true>(pl.nt, pl.split, softplus, false, a, grid1,
                                                                pl.smem, st)
-                           : dispatch_scan<float, true>(pl.nt, softplus, false, a, grid1,
+                           : dispatch_scan<float, true>(pl.nt, pl.split, softplus, false, a, grid1,
                                                         pl.smem, st);
         if (r != cudaSuccess) return r;
         const long long n_ent = (long long)entries;
@@ -1562,8 +1606,8 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     auto main_pass = [&](int first, int count, cudaStream_t st) -> cudaError_t {
         ScanArgs m = a;
         m.unit_offset = first;
-        return bf ? dispatch_scan<__nv_bfloat16, false>(pl.nt, softplus, hz, m, count, pl.smem, st)
-                  : dispatch_scan<float, false>(pl.nt, softplus, hz, m, count, pl.smem, st);
+        return bf ? dispatch_scan<__nv_bfloat16, false>(pl.nt, pl.split, softplus, hz, m, count, pl.smem, st)
+                  : dispatch_scan<float, false>(pl.nt, pl.split, softplus, hz, m, count, pl.smem, st);
     };
     const int n_chunk_units = chunked ? (pl.n_groups - pl.n_full) * pl.nchunks : 0;
     if (e == cudaSuccess && pl.concurrent && chunked && !no_alloc) {
