@@ -55,12 +55,15 @@ def _load():
             P = ctypes.POINTER(ctypes.c_double)
             i64 = ctypes.c_int64
             lib.oracle_scan_f64.argtypes = [i64, i64, i64, i64, P, P, P, P, P, P, P, P,
-                                            ctypes.c_int, P, P, P, ctypes.c_int]
+                                            ctypes.c_int, ctypes.c_int, P, P, P, ctypes.c_int]
             lib.oracle_scan_f64.restype = ctypes.c_int
-            lib.oracle_state_update_f64.argtypes = [i64, i64, i64, P, P, P, P, P, P, P, P, P, P]
+            lib.oracle_state_update_f64.argtypes = [i64, i64, i64, P, P, P, P, P, P, P, P, P,
+                                                    ctypes.c_int, ctypes.c_int, P]
             lib.oracle_state_update_f64.restype = ctypes.c_int
             lib.oracle_softplus_f64.argtypes = [ctypes.c_double]
             lib.oracle_softplus_f64.restype = ctypes.c_double
+            lib.oracle_zoh_weight_f64.argtypes = [ctypes.c_double, ctypes.c_double]
+            lib.oracle_zoh_weight_f64.restype = ctypes.c_double
             lib.oracle_silu_f64.argtypes = [ctypes.c_double]
             lib.oracle_silu_f64.restype = ctypes.c_double
             _lib = lib
@@ -87,12 +90,18 @@ def silu(z: float) -> float:
     return _load().oracle_silu_f64(float(z))
 
 
+def zoh_weight(dt: float, a: float) -> float:
+    return _load().oracle_zoh_weight_f64(float(dt), float(a))
+
+
 def scan(u, delta, A, B, C, dt_bias=None, D_skip=None, z=None, softplus: bool = True,
-         h0=None, threads: Optional[int] = None) -> Tuple[np.ndarray, np.ndarray, int]:
+         h0=None, threads: Optional[int] = None, zoh: bool = False
+         ) -> Tuple[np.ndarray, np.ndarray, int]:
     """Selective scan in fp64.
 
     u, delta, z: (batch, D, L); B, C: (batch, N, L); A: (D, N);
-    dt_bias, D_skip: (D,); h0: optional (batch, D, N) initial state.
+    dt_bias, D_skip: (D,); h0: optional (batch, D, N) initial state; zoh
+    selects the zero-order-hold input term instead of Euler's.
     Returns (y (batch, D, L), final state (batch, D, N), threads used).
     """
     u, delta, A, B, C = map(_f64, (u, delta, A, B, C))
@@ -109,13 +118,14 @@ def scan(u, delta, A, B, C, dt_bias=None, D_skip=None, z=None, softplus: bool = 
     hT = np.empty((bt, d, n), dtype=np.float64)
     rc = _load().oracle_scan_f64(bt, d, n, l, _ptr(u), _ptr(delta), _ptr(dt_bias), _ptr(A),
                                  _ptr(B), _ptr(C), _ptr(D_skip), _ptr(z), int(bool(softplus)),
-                                 _ptr(h0), _ptr(y), _ptr(hT), int(threads or 0))
+                                 int(bool(zoh)), _ptr(h0), _ptr(y), _ptr(hT), int(threads or 0))
     if rc <= 0:
         raise RuntimeError(f"oracle_scan_f64 failed: {rc}")
     return y, hT, rc
 
 
-def state_update(state, x, delta, A, B, C, dt_bias=None, D_skip=None, z=None):
+def state_update(state, x, delta, A, B, C, dt_bias=None, D_skip=None, z=None,
+                 softplus: bool = True, zoh: bool = False):
     """One decode step in fp64, in place on ``state`` (batch, D, N) float64.
 
     x, delta, z: (batch, D); B, C: (batch, N).  Returns y (batch, D).
@@ -127,7 +137,8 @@ def state_update(state, x, delta, A, B, C, dt_bias=None, D_skip=None, z=None):
     y = np.empty((bt, d), dtype=np.float64)
     rc = _load().oracle_state_update_f64(bt, d, n, _ptr(state), _ptr(x), _ptr(delta),
                                          _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C),
-                                         _ptr(D_skip), _ptr(z), _ptr(y))
+                                         _ptr(D_skip), _ptr(z), int(bool(softplus)),
+                                         int(bool(zoh)), _ptr(y))
     if rc != 0:
         raise RuntimeError(f"oracle_state_update_f64 failed: {rc}")
     return y

@@ -18,7 +18,17 @@
  *
  * with h = h0[b,d,:] (zero when h0 is absent) before the first step, the gate
  * skipped when z is absent, and the state after the last step returned in
- * final_state.  The single-token update is one step of the same recurrence
+ * final_state.
+ *
+ * With the zoh flag the input term Delta_t * B * u becomes the zero-order
+ * hold one, w * B * u with w = (exp(Delta_t * A[d,n]) - 1) / A[d,n]: the
+ * textbook exact discretisation of h' = A h + B x over a step of length
+ * Delta_t with x held constant (for diagonal A the matrix formula
+ * (Delta A)^-1 (exp(Delta A) - I) Delta B reduces to this per entry).  The
+ * pages print only Abar = exp(Delta*A); this is the reading under which
+ * Theorem 1 (page "Mamba: linear-time sequence modeling with selective
+ * state spaces", "Main results") is exact.  w tends to Delta_t as A -> 0,
+ * and A[d,n] == 0 takes that limit.  The single-token update is one step of the same recurrence
  * applied in place to a caller-held state, with softplus always applied (the
  * generation mode of page "Mamba: Linear-Time Sequence Modeling with
  * Selective State Spaces", section "Architecture": one state update per
@@ -45,6 +55,15 @@ double oracle_softplus_f64(double s)
     return log1p(exp(s));
 }
 
+/* Zero-order-hold input weight (exp(dt*a) - 1) / a, and its limit dt at
+ * a == 0.  expm1 keeps full relative precision when dt*a is small. */
+double oracle_zoh_weight_f64(double dt, double a)
+{
+    if (a == 0.0)
+        return dt;
+    return expm1(dt * a) / a;
+}
+
 /* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
 double oracle_silu_f64(double z)
 {
@@ -54,7 +73,7 @@ double oracle_silu_f64(double z)
 typedef struct {
     int64_t batch, dim, dstate, seqlen;
     const double *u, *delta, *dt_bias, *A, *B, *C, *D_skip, *z, *h0;
-    int softplus;
+    int softplus, zoh;
     double *y, *final_state;
     int64_t row_begin, row_end;
     int status;
@@ -89,7 +108,8 @@ static void scan_rows(scan_job *j)
             double acc = 0.0;
             for (int64_t n = 0; n < N; ++n) {
                 const double abar = exp(dt * Ad[n]);
-                h[n] = abar * h[n] + dt * Bb[n * L + t] * u[t];
+                const double w = j->zoh ? oracle_zoh_weight_f64(dt, Ad[n]) : dt;
+                h[n] = abar * h[n] + w * Bb[n * L + t] * u[t];
                 acc += Cb[n * L + t] * h[n];
             }
             double out = acc + dsk * u[t];
@@ -127,7 +147,7 @@ static int pick_threads(int requested, int64_t rows)
 int oracle_scan_f64(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
                     const double *u, const double *delta, const double *dt_bias,
                     const double *A, const double *B, const double *C,
-                    const double *D_skip, const double *z, int softplus,
+                    const double *D_skip, const double *z, int softplus, int zoh,
                     const double *h0, double *y, double *final_state,
                     int nthreads)
 {
@@ -160,6 +180,7 @@ int oracle_scan_f64(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
         j->z = z;
         j->h0 = h0;
         j->softplus = softplus;
+        j->zoh = zoh;
         j->y = y;
         j->final_state = final_state;
         j->row_begin = rows * i / nt;
@@ -191,16 +212,18 @@ int oracle_scan_f64(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
 
 /*
  * One generation step on a (batch, dim, N) state, in place:
- *   Delta = softplus(delta[b,d] + dt_bias[d])
- *   h[n]  = exp(Delta*A[d,n]) * h[n] + Delta*B[b,n]*x[b,d]
+ *   Delta = softplus(delta[b,d] + dt_bias[d])   (delta + dt_bias without softplus)
+ *   h[n]  = exp(Delta*A[d,n]) * h[n] + w*B[b,n]*x[b,d]
  *   y     = (sum_n C[b,n]*h[n] + D_skip[d]*x[b,d]) * silu(z[b,d])
+ * with w = Delta (Euler), or the zero-order-hold weight with the zoh flag.
  * x, delta, z, y are (batch, dim); B, C are (batch, N).
  */
 int oracle_state_update_f64(int64_t batch, int64_t dim, int64_t dstate,
                             double *state, const double *x, const double *delta,
                             const double *dt_bias, const double *A,
                             const double *B, const double *C,
-                            const double *D_skip, const double *z, double *y)
+                            const double *D_skip, const double *z, int softplus, int zoh,
+                            double *y)
 {
     if (batch < 0 || dim < 0 || dstate < 0)
         return -2;
@@ -210,11 +233,14 @@ int oracle_state_update_f64(int64_t batch, int64_t dim, int64_t dstate,
     for (int64_t b = 0; b < batch; ++b) {
         for (int64_t d = 0; d < dim; ++d) {
             const int64_t row = b * dim + d;
-            const double dt = oracle_softplus_f64(delta[row] + (dt_bias ? dt_bias[d] : 0.0));
+            const double s = delta[row] + (dt_bias ? dt_bias[d] : 0.0);
+            const double dt = softplus ? oracle_softplus_f64(s) : s;
             double *h = state + row * N;
             double acc = 0.0;
             for (int64_t n = 0; n < N; ++n) {
-                h[n] = exp(dt * A[d * N + n]) * h[n] + dt * B[b * N + n] * x[row];
+                const double a = A[d * N + n];
+                const double w = zoh ? oracle_zoh_weight_f64(dt, a) : dt;
+                h[n] = exp(dt * a) * h[n] + w * B[b * N + n] * x[row];
                 acc += C[b * N + n] * h[n];
             }
             double out = acc + (D_skip ? D_skip[d] : 0.0) * x[row];

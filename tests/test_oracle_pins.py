@@ -20,7 +20,14 @@ formulation or a closed form, chosen so that a plausible slip in the oracle
   state spaces": earlier SSMs use one fixed rule; with it the model is a
   convolution), checked with numpy.convolve;
 * linearity in u, causality, chunk associativity through the initial-state
-  argument, decode == scan, thread-count independence.
+  argument, decode == scan, thread-count independence;
+* the zero-order-hold input term (the textbook exact discretisation of
+  h' = A h + B x with x held over the step; the pages print only
+  Abar = exp(Delta A)): its weight against a 50-digit evaluation, Theorem 1
+  holding exactly with the unscaled input, the continuous-time steady state
+  -B u / A reached exactly under constant input, the unrolled sum and the
+  time-invariant convolution with the ZOH weight, and the Euler limit at
+  A = 0.
 """
 
 import math
@@ -203,7 +210,7 @@ def test_large_delta_resets_state():
 # --------------------------------------------------------------------------
 # explicit unrolled sum (brute force, long double)
 
-def _unrolled(p, softplus=True):
+def _unrolled(p, softplus=True, zoh=False):
     ld = np.longdouble
     u, delta, B, C, A = (np.asarray(p[k], dtype=ld) for k in ("u", "delta", "B", "C", "A"))
     bt, d, l = u.shape
@@ -219,7 +226,12 @@ def _unrolled(p, softplus=True):
         # decay from step t to T: exp(A_n * sum_{s=t+1..T} Delta_s) = exp(A_n (S_T - S_t))
         gap = S[:, :, T:T + 1] - S[:, :, :T + 1]                          # (bt,d,T+1)
         w = np.exp(A[None, :, :, None] * gap[:, :, None, :])              # (bt,d,n,T+1)
-        drive = dt[:, :, None, :T + 1] * B[:, None, :, :T + 1] * u[:, :, None, :T + 1]
+        if zoh:
+            # (exp(Delta A) - 1) / A per entry, written with expm1 in long double
+            wt = np.expm1(A[None, :, :, None] * dt[:, :, None, :T + 1]) / A[None, :, :, None]
+        else:
+            wt = dt[:, :, None, :T + 1]
+        drive = wt * B[:, None, :, :T + 1] * u[:, :, None, :T + 1]
         h = np.sum(w * drive, axis=3)                                     # (bt,d,n)
         y[:, :, T] = np.einsum("bdn,bn->bd", h, C[:, :, T])
         if T == l - 1:
@@ -232,13 +244,15 @@ def _unrolled(p, softplus=True):
     return y.astype(np.float64), hT.astype(np.float64)
 
 
-@pytest.mark.parametrize("seed,gate,dskip,bias", [(0, True, True, True), (1, False, True, True),
-                                                  (2, True, False, False), (3, False, False, True)])
-def test_unrolled_sum_matches(seed, gate, dskip, bias):
+@pytest.mark.parametrize("seed,gate,dskip,bias,zoh", [
+    (0, True, True, True, False), (1, False, True, True, False),
+    (2, True, False, False, False), (3, False, False, True, False),
+    (4, True, True, True, True), (5, False, False, True, True)])
+def test_unrolled_sum_matches(seed, gate, dskip, bias, zoh):
     p = _rand_problem(seed, bt=2, d=3, n=5, l=64, gate=gate, dskip=dskip, bias=bias)
     y, hT, _ = oracle.scan(p["u"], p["delta"], p["A"], p["B"], p["C"], dt_bias=p["dt_bias"],
-                           D_skip=p["D_skip"], z=p["z"])
-    yr, hr = _unrolled(p)
+                           D_skip=p["D_skip"], z=p["z"], zoh=zoh)
+    yr, hr = _unrolled(p, zoh=zoh)
     scale = max(1.0, np.max(np.abs(yr)))
     np.testing.assert_allclose(y, yr, rtol=0, atol=1e-12 * scale)
     np.testing.assert_allclose(hT, hr, rtol=0, atol=1e-12 * max(1.0, np.max(np.abs(hr))))
@@ -284,6 +298,89 @@ def test_lti_case_is_convolution():
     K = np.sum(Cn[:, None] * np.exp(np.outer(A[0], k) * dt) * dt * Bn[:, None], axis=0)
     ref = np.convolve(u[0, 0], K)[:l] + dsk[0] * u[0, 0]
     np.testing.assert_allclose(y[0, 0], ref, rtol=0, atol=1e-12 * max(1, np.abs(ref).max()))
+
+
+def test_lti_case_is_convolution_zoh():
+    # same system, zero-order hold: K_k = sum_n C_n e^{k dt A_n} (e^{dt A_n} - 1) / A_n B_n
+    g = np.random.default_rng(22)
+    n, l = 5, 70
+    dt = 0.29
+    A = -g.uniform(0.2, 3.0, (1, n))
+    Bn = g.standard_normal(n)
+    Cn = g.standard_normal(n)
+    u = g.standard_normal((1, 1, l))
+    B = np.repeat(Bn[None, :, None], l, axis=2)
+    C = np.repeat(Cn[None, :, None], l, axis=2)
+    y, _, _ = oracle.scan(u, np.full((1, 1, l), dt), A, B, C, softplus=False, zoh=True)
+    k = np.arange(l)
+    wz = (np.exp(dt * A[0]) - 1.0) / A[0]
+    K = np.sum(Cn[:, None] * np.exp(np.outer(A[0], k) * dt) * (wz * Bn)[:, None], axis=0)
+    ref = np.convolve(u[0, 0], K)[:l]
+    np.testing.assert_allclose(y[0, 0], ref, rtol=0, atol=1e-12 * max(1, np.abs(ref).max()))
+
+
+# --------------------------------------------------------------------------
+# zero-order hold
+
+def test_zoh_weight_against_high_precision():
+    import mpmath
+    mpmath.mp.dps = 50
+    for dt in (1e-9, 1e-4, 0.0025, 0.049, 0.7, 3.0, 40.0):
+        for a in (-16.0, -1.0, -1e-3, -1e-12, 0.5, 2.0):
+            exact = (mpmath.exp(mpmath.mpf(dt) * a) - 1) / a
+            got = oracle.zoh_weight(dt, a)
+            assert abs(got - float(exact)) <= 4e-16 * abs(float(exact)), (dt, a, got)
+    # A == 0 is the limit dt; the weight never exceeds dt for A < 0
+    assert oracle.zoh_weight(0.37, 0.0) == 0.37
+    assert oracle.zoh_weight(0.37, -2.0) < 0.37
+
+
+def test_theorem1_exact_under_zoh():
+    # N = 1, A = -1, B = 1: Abar = 1 - g and the ZOH input weight is
+    # (1 - e^{-Delta}) = g, so the scan is the gated RNN on the raw input.
+    s_pre, bias, x = _theorem1_inputs(13)
+    rows, _, l = x.shape
+    gate = expit(s_pre + bias[0])
+    ones = np.ones((rows, 1, l))
+    y, hT, _ = oracle.scan(x, s_pre, -np.ones((1, 1)), ones, ones, dt_bias=bias,
+                           softplus=True, zoh=True)
+    h = np.zeros(rows)
+    ref = np.empty((rows, l))
+    for t in range(l):
+        h = (1.0 - gate[:, 0, t]) * h + gate[:, 0, t] * x[:, 0, t]
+        ref[:, t] = h
+    np.testing.assert_allclose(y[:, 0, :], ref, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(hT[:, 0, 0], ref[:, -1], rtol=1e-12, atol=1e-13)
+
+
+def test_zoh_reaches_continuous_steady_state():
+    # Under constant input the ZOH recurrence has the fixed point of the
+    # continuous system, h = -B u / A (Euler's is Delta B u / (1 - e^{Delta A})).
+    # (the residual after L steps is prod Abar = e^{-Delta |A| L} <= e^{-50} here)
+    g = np.random.default_rng(17)
+    n, l = 4, 2000
+    A = -g.uniform(0.5, 4.0, (1, n))
+    Bn = g.standard_normal(n)
+    uval = 1.3
+    for dt in (0.05, 0.6):
+        delta = np.full((1, 1, l), dt)
+        B = np.repeat(Bn[None, :, None], l, axis=2)
+        C = np.zeros((1, n, l))
+        _, hT, _ = oracle.scan(np.full((1, 1, l), uval), delta, A, B, C, softplus=False,
+                               zoh=True)
+        np.testing.assert_allclose(hT[0, 0], -Bn * uval / A[0], rtol=1e-12)
+        _, hE, _ = oracle.scan(np.full((1, 1, l), uval), delta, A, B, C, softplus=False)
+        assert np.max(np.abs(hE[0, 0] + Bn * uval / A[0])) > 1e-3   # Euler's differs
+
+
+def test_zoh_at_zero_A_is_euler():
+    p = _rand_problem(23)
+    A = np.zeros_like(p["A"])
+    kw = dict(dt_bias=p["dt_bias"], D_skip=p["D_skip"], z=p["z"])
+    y1, h1, _ = oracle.scan(p["u"], p["delta"], A, p["B"], p["C"], zoh=True, **kw)
+    y0, h0, _ = oracle.scan(p["u"], p["delta"], A, p["B"], p["C"], **kw)
+    np.testing.assert_array_equal(y1, y0)
+    np.testing.assert_array_equal(h1, h0)
 
 
 # --------------------------------------------------------------------------
@@ -332,16 +429,20 @@ def test_chunk_associativity():
     np.testing.assert_array_equal(hb, hT)
 
 
-def test_decode_steps_equal_scan():
+@pytest.mark.parametrize("softplus,zoh", [(True, False), (True, True), (False, True)])
+def test_decode_steps_equal_scan(softplus, zoh):
     p = _rand_problem(61, l=30)
+    if not softplus:
+        p["delta"] = np.abs(p["delta"]) + 0.01
     y, hT, _ = oracle.scan(p["u"], p["delta"], p["A"], p["B"], p["C"], dt_bias=p["dt_bias"],
-                           D_skip=p["D_skip"], z=p["z"])
+                           D_skip=p["D_skip"], z=p["z"], softplus=softplus, zoh=zoh)
     bt, d, l = p["u"].shape
     state = np.zeros((bt, d, p["A"].shape[1]))
     for t in range(l):
         yt = oracle.state_update(state, p["u"][:, :, t], p["delta"][:, :, t], p["A"],
                                  p["B"][:, :, t], p["C"][:, :, t], dt_bias=p["dt_bias"],
-                                 D_skip=p["D_skip"], z=p["z"][:, :, t])
+                                 D_skip=p["D_skip"], z=p["z"][:, :, t], softplus=softplus,
+                                 zoh=zoh)
         np.testing.assert_array_equal(yt, y[:, :, t])
     np.testing.assert_array_equal(state, hT)
 
