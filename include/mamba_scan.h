@@ -73,8 +73,14 @@ typedef enum {
     MAMBA_ERR_ALLOC = -6,    /* scratch memory could not be obtained */
     MAMBA_ERR_DTYPE = -7,    /* io_dtype is not one of mamba_dtype_t */
     MAMBA_ERR_ALIAS = -8,    /* an output overlaps an input */
-    MAMBA_ERR_TOO_BIG = -9   /* needs more than MAMBA_NOALLOC_SCRATCH_BYTES of scratch */
+    MAMBA_ERR_TOO_BIG = -9,  /* needs more than MAMBA_NOALLOC_SCRATCH_BYTES of scratch */
+    MAMBA_ERR_FLAGS = -10    /* a flags argument has a bit the call does not know */
 } mamba_status_t;
+
+/* Bits of the `flags` argument of the extended entry points. */
+#define MAMBA_FLAG_SOFTPLUS 1  /* Delta = softplus(delta + dt_bias), else delta + dt_bias */
+#define MAMBA_FLAG_ZOH 2       /* zero-order-hold input term, else Euler (Delta * B * u) */
+#define MAMBA_FLAG_NOALLOC 4   /* scan: fixed scratch, no allocation (as mamba_scan_fwd_noalloc) */
 
 /* Size of the fixed scratch array used by mamba_scan_fwd_noalloc (16 MiB). */
 #define MAMBA_NOALLOC_SCRATCH_BYTES (16ll << 20)
@@ -140,6 +146,46 @@ int mamba_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t dstate, int64_t s
                            void *y, float *final_state, cudaStream_t stream);
 
 /*
+ * mamba_scan_fwd with an initial state, per-entry lengths and a choice of
+ * discretisation: the scan side of chunked prefill (a long sequence handed
+ * over in pieces, each starting from the previous piece's final_state) and
+ * of a padded batch of sequences with different lengths.  Arguments as in
+ * mamba_scan_fwd, plus:
+ *
+ *   flags         : MAMBA_FLAG_* bits; other bits -> MAMBA_ERR_FLAGS
+ *   initial_state : (batch, dim, dstate) fp32, nullable (zero state); h
+ *                   before the first step.  Must not overlap y or
+ *                   final_state (MAMBA_ERR_ALIAS): ping-pong two buffers to
+ *                   chain pieces.
+ *   seqlens       : (batch) int32 on the device, nullable (all entries use
+ *                   seqlen steps).  Entry b uses steps [0, seqlens[b]);
+ *                   values are clamped to [0, seqlen].  For t >= seqlens[b]
+ *                   the state is kept, y[b, :, t] is written as 0, and
+ *                   final_state[b] is h after step seqlens[b] - 1 (the
+ *                   initial state when seqlens[b] == 0).
+ *
+ * Discretisation.  Euler (the default, as mamba_scan_fwd): h <- Abar h +
+ * Delta B u.  MAMBA_FLAG_ZOH: h <- Abar h + ((Abar - 1) / A) B u per state
+ * entry (zero-order hold of the continuous system; the weight tends to
+ * Delta where A == 0, and that entry takes Delta).  With N = 1, A = -1,
+ * B = 1 it makes the scan exactly the gated RNN of Theorem 1 (paper "Mamba:
+ * linear-time sequence modeling with selective state spaces", "Main
+ * results").  Abar = exp(Delta A) in both.
+ *
+ * With MAMBA_FLAG_NOALLOC the call takes its scratch from the fixed array
+ * of mamba_scan_fwd_noalloc, with the same limits and the same rule on
+ * overlapping calls; otherwise from the stream-ordered pool.  When seqlen
+ * is 0, final_state (if given) receives initial_state (or zeros).
+ */
+int mamba_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                      int io_dtype,
+                      const void *u, const void *delta, const float *dt_bias,
+                      const float *A, const void *B, const void *C,
+                      const float *D_skip, const void *z, int flags,
+                      const float *initial_state, const int32_t *seqlens,
+                      void *y, float *final_state, cudaStream_t stream);
+
+/*
  * One generation step, updating `state` in place:
  *
  *   state       : (batch, dim, dstate)    fp32         read and written
@@ -158,6 +204,20 @@ int mamba_state_update(int64_t batch, int64_t dim, int64_t dstate, int io_dtype,
                        const float *dt_bias, const float *A,
                        const void *B, const void *C, const float *D_skip,
                        const void *z, void *y, cudaStream_t stream);
+
+/*
+ * mamba_state_update with flags: MAMBA_FLAG_SOFTPLUS (Delta = softplus(delta
+ * + dt_bias), else delta + dt_bias) and MAMBA_FLAG_ZOH (the input term of
+ * mamba_scan_fwd_ex's zero-order hold).  Any other bit, MAMBA_FLAG_NOALLOC
+ * included, returns MAMBA_ERR_FLAGS (the step allocates nothing anyway).
+ * With flags = MAMBA_FLAG_SOFTPLUS it is mamba_state_update.  The step that
+ * follows a mamba_scan_fwd_ex prefill takes the same SOFTPLUS and ZOH bits.
+ */
+int mamba_state_update_ex(int64_t batch, int64_t dim, int64_t dstate, int io_dtype,
+                          float *state, const void *x, const void *delta,
+                          const float *dt_bias, const float *A,
+                          const void *B, const void *C, const float *D_skip,
+                          const void *z, int flags, void *y, cudaStream_t stream);
 
 /* Static, human-readable name of a mamba_status_t value. */
 const char *mamba_status_string(int status);

@@ -12,6 +12,9 @@ from ._lib import (  # noqa: F401
     KIND_NAMES,
     MAMBA_BF16,
     MAMBA_F32,
+    MAMBA_FLAG_NOALLOC,
+    MAMBA_FLAG_SOFTPLUS,
+    MAMBA_FLAG_ZOH,
     MambaError,
     lib_path,
     load,
@@ -19,10 +22,12 @@ from ._lib import (  # noqa: F401
     mamba_profile_begin,
     mamba_profile_end,
     mamba_scan_fwd,
+    mamba_scan_fwd_ex,
     mamba_scan_fwd_noalloc,
     mamba_scan_set_tuning,
     mamba_selftest_wait_timeout,
     mamba_state_update,
+    mamba_state_update_ex,
     mamba_status_string,
     mamba_version,
 )

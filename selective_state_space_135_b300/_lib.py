@@ -15,9 +15,15 @@ MAMBA_F32 = 0
 MAMBA_BF16 = 1
 
 # every symbol the header declares
-EXPORTS = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_state_update", "mamba_status_string",
-           "mamba_device_status", "mamba_selftest_wait_timeout", "mamba_version", "mamba_scan_set_tuning",
+EXPORTS = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_ex", "mamba_state_update",
+           "mamba_state_update_ex", "mamba_status_string", "mamba_device_status",
+           "mamba_selftest_wait_timeout", "mamba_version", "mamba_scan_set_tuning",
            "mamba_profile_begin", "mamba_profile_end")
+
+# flags of the extended entry points
+MAMBA_FLAG_SOFTPLUS = 1
+MAMBA_FLAG_ZOH = 2
+MAMBA_FLAG_NOALLOC = 4
 
 KIND_NAMES = ("scan", "chunk_summary", "chunk_carry", "state_update", "pack_bc")
 
@@ -51,6 +57,12 @@ def load():
         lib.mamba_state_update.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                            vp, vp, vp]
         lib.mamba_state_update.restype = i32
+        lib.mamba_scan_fwd_ex.argtypes = [i64, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                          i32, vp, vp, vp, vp, vp]
+        lib.mamba_scan_fwd_ex.restype = i32
+        lib.mamba_state_update_ex.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              vp, i32, vp, vp]
+        lib.mamba_state_update_ex.restype = i32
         lib.mamba_status_string.argtypes = [i32]
         lib.mamba_status_string.restype = ctypes.c_char_p
         lib.mamba_device_status.argtypes = [vp]
@@ -171,6 +183,50 @@ def mamba_scan_fwd_noalloc(u, delta, dt_bias, A, B, C, D_skip, z, softplus: bool
                       y, final_state, stream)
 
 
+def scan_flags(softplus: bool = True, zoh: bool = False, no_alloc: bool = False) -> int:
+    return ((MAMBA_FLAG_SOFTPLUS if softplus else 0) | (MAMBA_FLAG_ZOH if zoh else 0)
+            | (MAMBA_FLAG_NOALLOC if no_alloc else 0))
+
+
+def mamba_scan_fwd_ex(u, delta, dt_bias, A, B, C, D_skip, z, softplus: bool = True,
+                      zoh: bool = False, initial_state=None, seqlens=None, y=None,
+                      final_state=None, no_alloc: bool = False, stream=None):
+    """mamba_scan_fwd plus an initial state (batch, dim, N) fp32, per-entry
+    lengths seqlens (batch,) int32 on the device, the zero-order-hold input
+    term (zoh=True) and the no-allocation scratch (no_alloc=True).  Returns y;
+    y[b, :, t] is 0 for t >= seqlens[b]."""
+    torch = _torch()
+    lib = load()
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    dev = u.device
+    io = _io_dtype(u)
+    if y is None:
+        y = torch.empty_like(u)
+    args = (
+        _ptr(u, "u", u.dtype, (batch, dim, L), dev),
+        _ptr(delta, "delta", u.dtype, (batch, dim, L), dev),
+        _ptr(dt_bias, "dt_bias", torch.float32, (dim,), dev),
+        _ptr(A, "A", torch.float32, (dim, N), dev),
+        _ptr(B, "B", u.dtype, (batch, N, L), dev),
+        _ptr(C, "C", u.dtype, (batch, N, L), dev),
+        _ptr(D_skip, "D_skip", torch.float32, (dim,), dev),
+        _ptr(z, "z", u.dtype, (batch, dim, L), dev),
+    )
+    hp = _ptr(initial_state, "initial_state", torch.float32, (batch, dim, N), dev)
+    lp = _ptr(seqlens, "seqlens", torch.int32, (batch,), dev)
+    yp = _ptr(y, "y", u.dtype, (batch, dim, L), dev)
+    fp = _ptr(final_state, "final_state", torch.float32, (batch, dim, N), dev)
+    with torch.cuda.device(dev):
+        st = _stream_handle(stream, dev)
+        rc = lib.mamba_scan_fwd_ex(batch, dim, N, L, io, args[0], args[1], args[2], args[3],
+                                   args[4], args[5], args[6], args[7],
+                                   scan_flags(softplus, zoh, no_alloc), hp, lp, yp, fp, st)
+    if rc != 0:
+        raise MambaError(rc, "mamba_scan_fwd_ex")
+    return y
+
+
 def mamba_state_update(state, x, delta, dt_bias, A, B, C, D_skip, z, y=None, stream=None):
     """One decode step in place on state (batch, dim, N) fp32.  x, delta, z:
     (batch, dim); B, C: (batch, N).  Returns y (batch, dim)."""
@@ -199,6 +255,38 @@ def mamba_state_update(state, x, delta, dt_bias, A, B, C, D_skip, z, y=None, str
                                     args[4], args[5], args[6], args[7], yp, st)
     if rc != 0:
         raise MambaError(rc, "mamba_state_update")
+    return y
+
+
+def mamba_state_update_ex(state, x, delta, dt_bias, A, B, C, D_skip, z, softplus: bool = True,
+                          zoh: bool = False, y=None, stream=None):
+    """mamba_state_update with the softplus and zero-order-hold switches."""
+    torch = _torch()
+    lib = load()
+    batch, dim, N = state.shape
+    dev = state.device
+    io = _io_dtype(x)
+    if y is None:
+        y = torch.empty_like(x)
+    sp = _ptr(state, "state", torch.float32, (batch, dim, N), dev)
+    args = (
+        _ptr(x, "x", x.dtype, (batch, dim), dev),
+        _ptr(delta, "delta", x.dtype, (batch, dim), dev),
+        _ptr(dt_bias, "dt_bias", torch.float32, (dim,), dev),
+        _ptr(A, "A", torch.float32, (dim, N), dev),
+        _ptr(B, "B", x.dtype, (batch, N), dev),
+        _ptr(C, "C", x.dtype, (batch, N), dev),
+        _ptr(D_skip, "D_skip", torch.float32, (dim,), dev),
+        _ptr(z, "z", x.dtype, (batch, dim), dev),
+    )
+    yp = _ptr(y, "y", x.dtype, (batch, dim), dev)
+    with torch.cuda.device(dev):
+        st = _stream_handle(stream, dev)
+        rc = lib.mamba_state_update_ex(batch, dim, N, io, sp, args[0], args[1], args[2], args[3],
+                                       args[4], args[5], args[6], args[7],
+                                       scan_flags(softplus, zoh), yp, st)
+    if rc != 0:
+        raise MambaError(rc, "mamba_state_update_ex")
     return y
 
 

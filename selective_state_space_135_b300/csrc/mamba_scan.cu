@@ -307,6 +307,8 @@ struct ScanArgs {
     float* final_state;
     float* ws_P;  // chunk decay products  [(k * tail_rows + wrow) * N + n]
     float* ws_h;  // chunk end states, then carried-in states (same layout)
+    const float* h0;       // initial state (batch, dim, N), or null for zero
+    const int* seqlens;    // per batch entry: steps in use, or null for all
     long long dim;
     long long seqlen;
     long long chunk_len;  // multiple of the time tile
@@ -417,19 +419,54 @@ __device__ __forceinline__ void abar_step(float2 (&ab)[NT / 2], const float2 (&a
     }
 }
 
+// Per-lane constants of the zero-order-hold input term (see zoh_term).
+template <int NT>
+struct ZohK {
+    float2 ia[NT / 2];   // fast path: 1 / (ln2 * A), 0 where A == 0
+    float2 e[NT / 2];    // fast path: 1 where A == 0 (Euler limit), else 0
+};
+
+// Input term of one state pair.  Euler (the default): (Delta*u) * B, with
+// du = Delta*u.  Zero-order hold, the textbook exact discretisation of
+// h' = A h + B x over a step Delta with x held constant (the pages print
+// only Abar = exp(Delta*A); with this input term the gated-RNN identity of
+// Theorem 1, page "Mamba: linear-time sequence modeling with selective state
+// spaces", "Main results", holds exactly): for diagonal A the input weight
+// is (exp(Delta*A) - 1) / A per state entry, which tends to Delta as A -> 0;
+// here du = u and dt is Delta (log2 units on the fast path, where B carries
+// the factor ln 2).  The fast path forms the weight from the step's Abar:
+// Abar * ia - ia, plus dt where A == 0.
+template <int NT, bool ACC, bool ZOH>
+__device__ __forceinline__ float2 input_term(int i, const float2& ab, const float2& a2,
+                                             const ZohK<NT>& zk, float dt, float du,
+                                             const float4& bc) {
+    const float2 b2 = make_float2(bc.x, bc.y);
+    if constexpr (!ZOH) {
+        return __fmul2_rn(make_float2(du, du), b2);
+    } else if constexpr (ACC) {
+        const float w0 = a2.x != 0.0f ? expm1f(dt * a2.x) / a2.x : dt;
+        const float w1 = a2.y != 0.0f ? expm1f(dt * a2.y) / a2.y : dt;
+        return make_float2(w0 * du * b2.x, w1 * du * b2.y);
+    } else {
+        float2 w = __ffma2_rn(ab, zk.ia[i], make_float2(-zk.ia[i].x, -zk.ia[i].y));
+        w = __ffma2_rn(zk.e[i], make_float2(dt, dt), w);
+        return __fmul2_rn(w, __fmul2_rn(make_float2(du, du), b2));
+    }
+}
+
 // One time step of the NT state entries of one channel given Abar:
-//   h <- Abar * h + (Delta*u) * B ;  returns sum_n C*h.
+//   h <- Abar * h + (input term) ;  returns sum_n C*h.
 // bc holds the step's NT/2 float4 (B pair, C pair), the same for every lane
 // of the warp (on the fast path B carries the factor ln 2 that turns the
-// log2-unit du back into Delta*u).  All input terms are formed before the
-// state updates, and two accumulators halve the dependent chain.
-template <int NT, bool STATE_ONLY>
+// log2-unit Delta back into natural units).  All input terms are formed
+// before the state updates, and two accumulators halve the dependent chain.
+template <int NT, bool ACC, bool ZOH, bool STATE_ONLY>
 __device__ __forceinline__ float state_step(float2 (&h2)[NT / 2], const float2 (&ab)[NT / 2],
-                                            float du, const float4 (&bc)[NT / 2]) {
-    const float2 du2 = make_float2(du, du);
+                                            const float2 (&a2)[NT / 2], const ZohK<NT>& zk,
+                                            float dt, float du, const float4 (&bc)[NT / 2]) {
     float2 bx[NT / 2];
 #pragma unroll
-    for (int i = 0; i < NT / 2; ++i) bx[i] = __fmul2_rn(du2, make_float2(bc[i].x, bc[i].y));
+    for (int i = 0; i < NT / 2; ++i) bx[i] = input_term<NT, ACC, ZOH>(i, ab[i], a2[i], zk, dt, du, bc[i]);
 #pragma unroll
     for (int i = 0; i < NT / 2; ++i) h2[i] = __ffma2_rn(ab[i], h2[i], bx[i]);
     if constexpr (STATE_ONLY) {
@@ -455,12 +492,11 @@ __device__ __forceinline__ float state_step(float2 (&h2)[NT / 2], const float2 (
 // step (as abar_step), pair by pair, so that the ex2 work of step t+1 sits
 // between the multiply/adds of step t in the instruction stream instead of
 // stalling the warp in one burst.
-template <int NT, bool ACC, bool STATE_ONLY>
+template <int NT, bool ACC, bool ZOH, bool STATE_ONLY>
 __device__ __forceinline__ float fused_step(float2 (&h2)[NT / 2], const float2 (&ab)[NT / 2],
                                             float2 (&an)[NT / 2], const float2 (&a2)[NT / 2],
-                                            float dt_next, float du,
-                                            const float4 (&bc)[NT / 2]) {
-    const float2 du2 = make_float2(du, du);
+                                            const ZohK<NT>& zk, float dt_next, float dt,
+                                            float du, const float4 (&bc)[NT / 2]) {
     const float2 dt2 = make_float2(dt_next, dt_next);
     float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
 #pragma unroll
@@ -471,7 +507,7 @@ __device__ __forceinline__ float fused_step(float2 (&h2)[NT / 2], const float2 (
             const float2 arg = __fmul2_rn(dt2, a2[i]);
             an[i] = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
         }
-        const float2 bx = __fmul2_rn(du2, make_float2(bc[i].x, bc[i].y));
+        const float2 bx = input_term<NT, ACC, ZOH>(i, ab[i], a2[i], zk, dt, du, bc[i]);
         h2[i] = __ffma2_rn(ab[i], h2[i], bx);
         if constexpr (!STATE_ONLY) {
             const float2 cp = make_float2(bc[i].z, bc[i].w);
@@ -508,8 +544,8 @@ __device__ __forceinline__ void load_bc(float4 (&bc)[NT / 2], const float4* row)
 //   (3) each slice finishes 1/SPLIT of the outputs: all partial sums (in a
 //       fixed order), skip term and gate.
 // STATE_ONLY is the chunk-summary pass: no C, z or y; it returns
-// (exp(A*sum Delta), h_end).
-template <typename T, int NT, int SPLIT, bool STATE_ONLY, bool SOFTPLUS, bool HAS_Z>
+// (exp(A*sum Delta), h_end).  ZOH selects the zero-order-hold input term.
+template <typename T, int NT, int SPLIT, bool STATE_ONLY, bool SOFTPLUS, bool HAS_Z, bool ZOH>
 __global__ void __launch_bounds__(32 * kScanWarps, kScanMinBlocks)
 scan_kernel(const __grid_constant__ ScanArgs a) {
     using Lay = ScanLayout<T, NT, SPLIT>;
@@ -542,6 +578,11 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     const bool tma = a.use_tma != 0;
     const int ntiles = (int)((w.t1 - w.t0 + TT - 1) / TT);
     const int wrow = (w.tail >= 0) ? w.tail * CH + c : 0;
+    // steps in use for this batch entry: past them Delta is 0 (the state is
+    // kept) and y is 0
+    long long len = L_;
+    if (a.seqlens) len = min(L_, max(0LL, (long long)a.seqlens[w.b]));
+    const long long t_end = min(w.t1, len);   // end of the live steps of this unit
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     unsigned char* yt = smem + Lay::ybuf(stages);
@@ -551,22 +592,36 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     float* part_s = reinterpret_cast<float*>(smem + Lay::part(stages));
 
     // ---- per-thread constants and initial state ----
+    // A unit that starts at t = 0 starts from the caller's initial state
+    // (zero without one); a later chunk of the main pass from the carried
+    // state; a later chunk of the summary pass from zero.
     float2 h2[kNPair], a2[kNPair];
+    ZohK<NT> zk;
+    (void)zk;
 #pragma unroll
     for (int i = 0; i < kNPair; ++i) {
-        float av[2], hv[2];
+        float av[2], hv[2], iv[2], ev[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int n = hh * NT + 2 * i + j;
             const bool ok = chan_ok && n < N;
             av[j] = ok ? a.A[(long long)d * N + n] : 0.0f;
             float h0 = 0.0f;
-            if (ok && w.tail >= 0 && w.k > 0 && !STATE_ONLY)
-                h0 = a.ws_h[((long long)(w.k - 1) * a.tail_rows + wrow) * N + n];
+            if (ok) {
+                if (w.tail >= 0 && w.k > 0) {
+                    if (!STATE_ONLY) h0 = a.ws_h[((long long)(w.k - 1) * a.tail_rows + wrow) * N + n];
+                } else if (a.h0) {
+                    h0 = a.h0[row * N + n];
+                }
+            }
             hv[j] = h0;
+            iv[j] = av[j] != 0.0f ? 1.0f / (kLn2 * av[j]) : 0.0f;
+            ev[j] = av[j] != 0.0f ? 0.0f : 1.0f;
         }
         a2[i] = make_float2(av[0], av[1]);
         h2[i] = make_float2(hv[0], hv[1]);
+        zk.ia[i] = make_float2(iv[0], iv[1]);
+        zk.e[i] = make_float2(ev[0], ev[1]);
     }
     const float bias0 = (chan_ok && a.dt_bias) ? a.dt_bias[d] : 0.0f;
     const float bias = ACC ? bias0 : bias0 * kLog2e;
@@ -656,8 +711,9 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
         }
     };
 
-    // (1) Delta and Delta*u of this slice's steps [hh*HT, hh*HT + HT) of a
-    //     tile into du_s: independent chains, back to back
+    // (1) Delta and Delta*u (Euler) or u (zero-order hold) of this slice's
+    //     steps [hh*HT, hh*HT + HT) of a tile into du_s: independent chains,
+    //     back to back
     auto phase1 = [&](const unsigned char* st_, int nv_) {
 #pragma unroll
         for (int q = 0; q < QC; ++q) {
@@ -668,10 +724,10 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
             CK::load(st_ + off, uv);
 #pragma unroll
             for (int j = 0; j < G; ++j) {
-                float v = delta_of(dv[j]);
+                float v = delta_of(dv[j]), uu = uv[j];
                 const int t = ck * G + j;
-                if (t >= nv_) v = 0.0f;   // past the end of the unit: the state is kept
-                du_s[t * CH + c] = make_float2(v, v * uv[j]);
+                if (t >= nv_) v = uu = 0.0f;   // past the live steps: the state is kept
+                du_s[t * CH + c] = make_float2(v, ZOH ? uu : v * uu);
             }
         }
     };
@@ -680,13 +736,14 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     uint32_t parity = 0;    // mbarrier phase parity of tile `it`
     if (ntiles > 0) {
         const bool to = acquire(0, 0, 0);
-        phase1(smem + Lay::stage(0), (int)min((long long)TT, w.t1 - w.t0));
+        phase1(smem + Lay::stage(0), (int)max(-1LL, min((long long)TT, t_end - w.t0)));
         aborted = __syncthreads_or(to);
     }
 
     for (int it = 0; it < ntiles && !aborted; ++it) {
         const long long tt0 = w.t0 + (long long)it * TT;
         const int nv = (int)min((long long)TT, w.t1 - tt0);   // steps of this unit in the tile
+        const long long ny = t_end - tt0;                       // live steps in the tile (may be <= 0)
         const unsigned char* st = smem + Lay::stage(stage);
         const unsigned char* ut = st;
         const unsigned char* zt = st + 2 * Lay::kRows;
@@ -725,9 +782,9 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                 float pt;
                 if (t + 1 < TT) {
                     load_bc<NT>(bn, bct + (t + 1) * (NP / 2));
-                    pt = fused_step<NT, ACC, STATE_ONLY>(h2, ab, an, a2, d1.x, d0.y, bc);
+                    pt = fused_step<NT, ACC, ZOH, STATE_ONLY>(h2, ab, an, a2, zk, d1.x, d0.x, d0.y, bc);
                 } else {
-                    pt = state_step<NT, STATE_ONLY>(h2, ab, d0.y, bc);
+                    pt = state_step<NT, ACC, ZOH, STATE_ONLY>(h2, ab, a2, zk, d0.x, d0.y, bc);
                 }
                 if constexpr (STATE_ONLY) {
                     dsum += d0.x;
@@ -760,7 +817,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
         if (has_next) {
             to = acquire(it + 1, next_stage, next_parity);
             const long long tn0 = tt0 + TT;
-            phase1(smem + Lay::stage(next_stage), (int)min((long long)TT, w.t1 - tn0));
+            phase1(smem + Lay::stage(next_stage), (int)max(-1LL, min((long long)TT, t_end - tn0)));
         }
         if constexpr (!STATE_ONLY) {
             // the other slices' partials of this slice's steps t = hh*HT + i:
@@ -787,7 +844,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                     for (int k = 1; k < SPLIT; ++k) o += pk[k - 1][(q * G + j) * CH];
                     o = fmaf(dsk, uv[j], o);
                     if constexpr (has_z) o *= silu_f<ACC>(zv[j]);
-                    ov[j] = o;
+                    ov[j] = (q * G + j + hh * HT < ny) ? o : 0.0f;
                 }
                 CK::store(yt + off, ov);
             }
@@ -889,7 +946,19 @@ struct StepArgs {
     long long dim;
     int dstate;
     int vec_state;  // state rows 16-byte aligned and N % 4 == 0
+    int softplus;   // Delta = softplus(delta + dt_bias), else delta + dt_bias
+    int zoh;        // zero-order-hold input term, else Euler
 };
+
+// Zero-order-hold input weight of one state entry (as the scan's
+// input_term): (Abar - 1) / A, Delta where A == 0.  dt is Delta in natural
+// units and dA the step's Abar.  The generation step is bound by memory, so
+// the division costs nothing here.
+template <bool ACC>
+__device__ __forceinline__ float zoh_weight(float dA, float dt, float A) {
+    if (A == 0.0f) return dt;
+    return (ACC ? expm1f(dt * A) : dA - 1.0f) / A;
+}
 
 // Four lanes per (b, d) row; lane q owns state entries [4q, 4q + 4).
 template <typename T>
@@ -907,7 +976,7 @@ state_update_kernel(const StepArgs a) {
         xv = IO<T>::to_f(static_cast<const T*>(a.x)[row]);
         const float s = IO<T>::to_f(static_cast<const T*>(a.delta)[row]) +
                         (a.dt_bias ? a.dt_bias[d] : 0.0f);
-        const float dt = softplus_f<ACC>(s);
+        const float dt = a.softplus ? softplus_f<ACC>(s) : s;
         const float du = dt * xv;
         if (a.z) zv = IO<T>::to_f(static_cast<const T*>(a.z)[row]);
         dsk = a.D_skip ? a.D_skip[d] : 0.0f;
@@ -923,14 +992,16 @@ state_update_kernel(const StepArgs a) {
             for (int j = 0; j < 4; ++j) {
                 const int n = n0 + j;
                 const float dA = ACC ? expf(dt * Ad[n]) : ex2_approx(dt * (Ad[n] * kLog2e));
-                hs[j] = fmaf(dA, hs[j], du * IO<T>::to_f(Bb[n]));
+                const float bin = a.zoh ? zoh_weight<ACC>(dA, dt, Ad[n]) * xv : du;
+                hs[j] = fmaf(dA, hs[j], bin * IO<T>::to_f(Bb[n]));
                 acc = fmaf(IO<T>::to_f(Cb[n]), hs[j], acc);
             }
             *reinterpret_cast<float4*>(h + n0) = make_float4(hs[0], hs[1], hs[2], hs[3]);
         } else {
             for (int n = n0; n < n0 + 4 && n < N; ++n) {
                 const float dA = ACC ? expf(dt * Ad[n]) : ex2_approx(dt * (Ad[n] * kLog2e));
-                const float hn = fmaf(dA, h[n], du * IO<T>::to_f(Bb[n]));
+                const float bin = a.zoh ? zoh_weight<ACC>(dA, dt, Ad[n]) * xv : du;
+                const float hn = fmaf(dA, h[n], bin * IO<T>::to_f(Bb[n]));
                 h[n] = hn;
                 acc = fmaf(IO<T>::to_f(Cb[n]), hn, acc);
             }
@@ -973,15 +1044,18 @@ state_update16_kernel(const StepArgs a) {
         const float bias = a.dt_bias ? a.dt_bias[d] : 0.0f;
         if (a.z) zv = IO<T>::to_f(static_cast<const T*>(a.z)[row]);
         dsk = a.D_skip ? a.D_skip[d] : 0.0f;
-        float dt, du;   // Delta (log2 units on the fast path) and Delta*u (natural units)
+        // Delta (log2 units on the fast path), Delta (natural units), Delta*u
+        float dt, dtn, du;
         if constexpr (ACC) {
-            dt = softplus_f<true>(dv + bias);
-            du = dt * xv;
+            const float sarg = dv + bias;
+            dt = a.softplus ? softplus_f<true>(sarg) : sarg;
+            dtn = dt;
         } else {
             const float tl = fmaf(dv, kLog2e, bias * kLog2e);
-            dt = tl > 30.0f ? tl : lg2_approx(1.0f + ex2_approx(tl));
-            du = dt * kLn2 * xv;
+            dt = !a.softplus ? tl : (tl > 30.0f ? tl : lg2_approx(1.0f + ex2_approx(tl)));
+            dtn = dt * kLn2;
         }
+        du = dtn * xv;
         float Bv[H], Cv[H], Av[H];
         const T* Bb = static_cast<const T*>(a.B) + b * N + H * q;
         const T* Cb = static_cast<const T*>(a.C) + b * N + H * q;
@@ -1006,7 +1080,8 @@ state_update16_kernel(const StepArgs a) {
 #pragma unroll
         for (int k = 0; k < H; ++k) {
             const float dA = ACC ? expf(dt * Av[k]) : ex2_approx(dt * Av[k]);
-            hs[k] = fmaf(dA, hs[k], du * Bv[k]);
+            const float bin = a.zoh ? zoh_weight<ACC>(dA, dtn, Av[k]) * xv : du;
+            hs[k] = fmaf(dA, hs[k], bin * Bv[k]);
             if (k & 1) acc1 = fmaf(Cv[k], hs[k], acc1);
             else acc = fmaf(Cv[k], hs[k], acc);
         }
@@ -1150,9 +1225,9 @@ int sm_count(int dev) {
     return cache[dev];
 }
 
-template <typename T, int NT, int SPLIT, bool STATE_ONLY, bool SP, bool HZ>
+template <typename T, int NT, int SPLIT, bool STATE_ONLY, bool SP, bool HZ, bool ZOH>
 cudaError_t launch_scan(const ScanArgs& a, int grid, int smem, cudaStream_t st) {
-    auto k = scan_kernel<T, NT, SPLIT, STATE_ONLY, SP, HZ>;
+    auto k = scan_kernel<T, NT, SPLIT, STATE_ONLY, SP, HZ, ZOH>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     ProfScope prof(STATE_ONLY ? kKindSummary : kKindScan, st);
@@ -1171,20 +1246,29 @@ cudaError_t launch_scan(const ScanArgs& a, int grid, int smem, cudaStream_t st) 
 #define MAMBA_VARIANTS(X) X(2, 2) X(4, 2) X(4, 4)
 #endif
 
-template <typename T, bool STATE_ONLY>
-cudaError_t dispatch_scan(int nt, int split, bool sp, bool hz, const ScanArgs& a, int grid,
-                          int smem, cudaStream_t st) {
-#define X(NT_, S_)                                                                          \
-    if (nt == NT_ && split == S_) {                                                          \
-        if (STATE_ONLY)                                                                      \
-            return sp ? launch_scan<T, NT_, S_, STATE_ONLY, true, false>(a, grid, smem, st)  \
-                      : launch_scan<T, NT_, S_, STATE_ONLY, false, false>(a, grid, smem, st); \
-        if (sp)                                                                              \
-            return hz ? launch_scan<T, NT_, S_, STATE_ONLY, true, true>(a, grid, smem, st)   \
-                      : launch_scan<T, NT_, S_, STATE_ONLY, true, false>(a, grid, smem, st); \
-        return hz ? launch_scan<T, NT_, S_, STATE_ONLY, false, true>(a, grid, smem, st)      \
-                  : launch_scan<T, NT_, S_, STATE_ONLY, false, false>(a, grid, smem, st);    \
+// The summary pass reads no z, so it has no HAS_Z instances.
+template <typename T, bool STATE_ONLY, int NT, int S, bool ZOH>
+cudaError_t dispatch_flags(bool sp, bool hz, const ScanArgs& a, int grid, int smem,
+                           cudaStream_t st) {
+    if constexpr (STATE_ONLY) {
+        return sp ? launch_scan<T, NT, S, true, true, false, ZOH>(a, grid, smem, st)
+                  : launch_scan<T, NT, S, true, false, false, ZOH>(a, grid, smem, st);
+    } else {
+        if (sp)
+            return hz ? launch_scan<T, NT, S, false, true, true, ZOH>(a, grid, smem, st)
+                      : launch_scan<T, NT, S, false, true, false, ZOH>(a, grid, smem, st);
+        return hz ? launch_scan<T, NT, S, false, false, true, ZOH>(a, grid, smem, st)
+                  : launch_scan<T, NT, S, false, false, false, ZOH>(a, grid, smem, st);
     }
+}
+
+template <typename T, bool STATE_ONLY>
+cudaError_t dispatch_scan(int nt, int split, bool sp, bool hz, bool zoh, const ScanArgs& a,
+                          int grid, int smem, cudaStream_t st) {
+#define X(NT_, S_)                                                                  \
+    if (nt == NT_ && split == S_)                                                    \
+        return zoh ? dispatch_flags<T, STATE_ONLY, NT_, S_, true>(sp, hz, a, grid, smem, st) \
+                   : dispatch_flags<T, STATE_ONLY, NT_, S_, false>(sp, hz, a, grid, smem, st);
     MAMBA_VARIANTS(X)
 #undef X
     return cudaErrorInvalidValue;
@@ -1402,6 +1486,7 @@ const char* mamba_status_string(int status) {
         case MAMBA_ERR_ALIAS: return "an output overlaps an input";
         case MAMBA_ERR_TOO_BIG:
             return "the call needs more scratch than the fixed MAMBA_NOALLOC_SCRATCH_BYTES";
+        case MAMBA_ERR_FLAGS: return "a flags argument has an unknown bit";
         default: return "unknown status";
     }
 }
@@ -1470,12 +1555,14 @@ int mamba_scan_set_tuning(int tail, int stages, int chunks) {
     return MAMBA_OK;
 }
 
-// Shared body of mamba_scan_fwd (scratch from the stream-ordered pool) and
-// mamba_scan_fwd_noalloc (the fixed scratch array, no allocation).
+// Shared body of mamba_scan_fwd (scratch from the stream-ordered pool),
+// mamba_scan_fwd_noalloc (the fixed scratch array, no allocation) and
+// mamba_scan_fwd_ex (either, plus initial state, lengths and ZOH).
 static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
                            int io_dtype, const void* u, const void* delta,
                            const float* dt_bias, const float* A, const void* B, const void* C,
-                           const float* D_skip, const void* z, int softplus, void* y,
+                           const float* D_skip, const void* z, int softplus, bool zoh,
+                           const float* h0, const int32_t* seqlens, void* y,
                            float* final_state, cudaStream_t stream, bool no_alloc) {
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
     if (batch < 1 || dim < 1 || dstate < 1 || dstate > kMaxN || seqlen < 0) return MAMBA_ERR_SHAPE;
@@ -1490,21 +1577,26 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     for (const void* q : {u, delta, z, B, C, (const void*)y})
         if (q && !aligned(q, es)) return MAMBA_ERR_ALIGN;
     for (const void* q : {(const void*)dt_bias, (const void*)A, (const void*)D_skip,
-                          (const void*)final_state})
+                          (const void*)final_state, (const void*)h0, (const void*)seqlens})
         if (q && !aligned(q, 4)) return MAMBA_ERR_ALIGN;
     {
-        const void* ins[] = {u, delta, z, B, C, dt_bias, A, D_skip};
+        const void* ins[] = {u, delta, z, B, C, dt_bias, A, D_skip, h0, seqlens};
         const size_t insz[] = {big, big, big, bcb, bcb, (size_t)dim * 4,
-                               (size_t)(dim * dstate) * 4, (size_t)dim * 4};
-        for (int i = 0; i < 8; ++i) {
+                               (size_t)(dim * dstate) * 4, (size_t)dim * 4, fsb,
+                               (size_t)batch * 4};
+        for (int i = 0; i < 10; ++i) {
             if (overlaps(y, big, ins[i], insz[i])) return MAMBA_ERR_ALIAS;
             if (overlaps(final_state, fsb, ins[i], insz[i])) return MAMBA_ERR_ALIAS;
         }
         if (overlaps(y, big, final_state, fsb)) return MAMBA_ERR_ALIAS;
     }
     if (seqlen == 0) {
-        if (final_state && cudaMemsetAsync(final_state, 0, fsb, stream) != cudaSuccess)
-            return MAMBA_ERR_CUDA;
+        if (final_state) {
+            const cudaError_t r =
+                h0 ? cudaMemcpyAsync(final_state, h0, fsb, cudaMemcpyDeviceToDevice, stream)
+                   : cudaMemsetAsync(final_state, 0, fsb, stream);
+            if (r != cudaSuccess) return MAMBA_ERR_CUDA;
+        }
         return MAMBA_OK;
     }
 
@@ -1566,6 +1658,7 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     }
     a.u = u; a.delta = delta; a.z = z;
     a.dt_bias = dt_bias; a.A = A; a.D_skip = D_skip; a.y = y; a.final_state = final_state;
+    a.h0 = h0; a.seqlens = seqlens;
     a.dim = dim; a.seqlen = seqlen; a.chunk_len = pl.chunk_len;
     a.batch = (int)batch; a.dstate = (int)dstate;
     a.use_tma = tma ? 1 : 0; a.stages = pl.stages;
@@ -1595,10 +1688,11 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     const bool hz = z != nullptr;
     auto summary_and_carry = [&](cudaStream_t st) -> cudaError_t {
         const int grid1 = (pl.n_groups - pl.n_full) * (pl.nchunks - 1);
-        cudaError_t r = bf ? dispatch_scan<__nv_bfloat16, true>(pl.nt, pl.split, softplus, false, a, grid1,
-                                                               pl.smem, st)
-                           : dispatch_scan<float, true>(pl.nt, pl.split, softplus, false, a, grid1,
-                                                        pl.smem, st);
+        cudaError_t r =
+            bf ? dispatch_scan<__nv_bfloat16, true>(pl.nt, pl.split, softplus, false, zoh, a,
+                                                    grid1, pl.smem, st)
+               : dispatch_scan<float, true>(pl.nt, pl.split, softplus, false, zoh, a, grid1,
+                                            pl.smem, st);
         if (r != cudaSuccess) return r;
         const long long n_ent = (long long)entries;
         {
@@ -1611,8 +1705,10 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     auto main_pass = [&](int first, int count, cudaStream_t st) -> cudaError_t {
         ScanArgs m = a;
         m.unit_offset = first;
-        return bf ? dispatch_scan<__nv_bfloat16, false>(pl.nt, pl.split, softplus, hz, m, count, pl.smem, st)
-                  : dispatch_scan<float, false>(pl.nt, pl.split, softplus, hz, m, count, pl.smem, st);
+        return bf ? dispatch_scan<__nv_bfloat16, false>(pl.nt, pl.split, softplus, hz, zoh, m,
+                                                        count, pl.smem, st)
+                  : dispatch_scan<float, false>(pl.nt, pl.split, softplus, hz, zoh, m, count,
+                                                pl.smem, st);
     };
     const int n_chunk_units = chunked ? (pl.n_groups - pl.n_full) * pl.nchunks : 0;
     if (e == cudaSuccess && pl.concurrent && chunked && !no_alloc) {
@@ -1647,7 +1743,8 @@ int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, i
                    const void* B, const void* C, const float* D_skip, const void* z,
                    int softplus, void* y, float* final_state, cudaStream_t stream) {
     return scan_fwd_common(batch, dim, dstate, seqlen, io_dtype, u, delta, dt_bias, A, B, C,
-                           D_skip, z, softplus, y, final_state, stream, false);
+                           D_skip, z, softplus, false, nullptr, nullptr, y, final_state, stream,
+                           false);
 }
 
 int mamba_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
@@ -1656,13 +1753,28 @@ int mamba_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t dstate, int64_t s
                            const float* D_skip, const void* z, int softplus, void* y,
                            float* final_state, cudaStream_t stream) {
     return scan_fwd_common(batch, dim, dstate, seqlen, io_dtype, u, delta, dt_bias, A, B, C,
-                           D_skip, z, softplus, y, final_state, stream, true);
+                           D_skip, z, softplus, false, nullptr, nullptr, y, final_state, stream,
+                           true);
 }
 
-int mamba_state_update(int64_t batch, int64_t dim, int64_t dstate, int io_dtype, float* state,
-                       const void* x, const void* delta, const float* dt_bias, const float* A,
-                       const void* B, const void* C, const float* D_skip, const void* z, void* y,
-                       cudaStream_t stream) {
+int mamba_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io_dtype,
+                      const void* u, const void* delta, const float* dt_bias, const float* A,
+                      const void* B, const void* C, const float* D_skip, const void* z,
+                      int flags, const float* initial_state, const int32_t* seqlens, void* y,
+                      float* final_state, cudaStream_t stream) {
+    if (flags & ~(MAMBA_FLAG_SOFTPLUS | MAMBA_FLAG_ZOH | MAMBA_FLAG_NOALLOC))
+        return MAMBA_ERR_FLAGS;
+    return scan_fwd_common(batch, dim, dstate, seqlen, io_dtype, u, delta, dt_bias, A, B, C,
+                           D_skip, z, (flags & MAMBA_FLAG_SOFTPLUS) ? 1 : 0,
+                           (flags & MAMBA_FLAG_ZOH) != 0, initial_state, seqlens, y,
+                           final_state, stream, (flags & MAMBA_FLAG_NOALLOC) != 0);
+}
+
+static int state_update_common(int64_t batch, int64_t dim, int64_t dstate, int io_dtype,
+                               float* state, const void* x, const void* delta,
+                               const float* dt_bias, const float* A, const void* B,
+                               const void* C, const float* D_skip, const void* z, int flags,
+                               void* y, cudaStream_t stream) {
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
     if (batch < 1 || dim < 1 || dstate < 1 || dstate > kMaxN) return MAMBA_ERR_SHAPE;
     if ((double)batch * dim > 1.0e15) return MAMBA_ERR_SHAPE;
@@ -1691,6 +1803,8 @@ int mamba_state_update(int64_t batch, int64_t dim, int64_t dstate, int io_dtype,
     a.dt_bias = dt_bias; a.A = A; a.D_skip = D_skip; a.y = y;
     a.rows = rows; a.dim = dim; a.dstate = (int)dstate;
     a.vec_state = (dstate % 4 == 0) && aligned(state, 16);
+    a.softplus = (flags & MAMBA_FLAG_SOFTPLUS) ? 1 : 0;
+    a.zoh = (flags & MAMBA_FLAG_ZOH) ? 1 : 0;
     // dstate 16 with 16-byte aligned rows: the vectorised two-lane kernel
     const bool vec16 = dstate == 16 && aligned(state, 16) && aligned(A, 16) && aligned(B, 16) &&
                        aligned(C, 16) && batch <= 65535LL * kStepBatches;
@@ -1714,6 +1828,23 @@ int mamba_state_update(int64_t batch, int64_t dim, int64_t dstate, int io_dtype,
             state_update_kernel<float><<<grid, kThreads, 0, stream>>>(a);
     }
     return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
+}
+
+int mamba_state_update(int64_t batch, int64_t dim, int64_t dstate, int io_dtype, float* state,
+                       const void* x, const void* delta, const float* dt_bias, const float* A,
+                       const void* B, const void* C, const float* D_skip, const void* z, void* y,
+                       cudaStream_t stream) {
+    return state_update_common(batch, dim, dstate, io_dtype, state, x, delta, dt_bias, A, B, C,
+                               D_skip, z, MAMBA_FLAG_SOFTPLUS, y, stream);
+}
+
+int mamba_state_update_ex(int64_t batch, int64_t dim, int64_t dstate, int io_dtype,
+                          float* state, const void* x, const void* delta, const float* dt_bias,
+                          const float* A, const void* B, const void* C, const float* D_skip,
+                          const void* z, int flags, void* y, cudaStream_t stream) {
+    if (flags & ~(MAMBA_FLAG_SOFTPLUS | MAMBA_FLAG_ZOH)) return MAMBA_ERR_FLAGS;
+    return state_update_common(batch, dim, dstate, io_dtype, state, x, delta, dt_bias, A, B, C,
+                               D_skip, z, flags, y, stream);
 }
 
 }  // extern "C"

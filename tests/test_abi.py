@@ -15,6 +15,8 @@ HEADER = os.path.join(ROOT, "include", "mamba_scan.h")
 
 OK, ENULL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EALLOC, EDTYPE, EALIAS = 0, -1, -2, -3, -4, -5, -6, -7, -8
 ETOOBIG = -9
+EFLAGS = -10
+SOFTPLUS, ZOH, NOALLOC = 1, 2, 4
 
 
 def declared_functions():
@@ -41,7 +43,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in (OK, ENULL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EALLOC, EDTYPE, EALIAS, ETOOBIG):
+    for code in (OK, ENULL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EALLOC, EDTYPE, EALIAS, ETOOBIG,
+                 EFLAGS):
         s = mm.mamba_status_string(code)
         assert s and s != "unknown status"
     assert mm.mamba_status_string(12345) == "unknown status"
@@ -120,6 +123,34 @@ def test_noalloc_rejects_oversize_before_any_cuda_call(lib):
     assert "MAMBA_NOALLOC_SCRATCH_BYTES" in mm.mamba_status_string(ETOOBIG)
 
 
+def ex_call(lib, batch=2, dim=16, dstate=4, seqlen=64, io=1, flags=SOFTPLUS, h0=11, lens=12,
+            fin=10, y=9, extra=None):
+    ptrs = dict(u=1, delta=2, dtb=3, A=4, B=5, C=6, Dk=7, z=8, y=y, fin=fin, h0=h0, lens=lens)
+    v = {k: (None if q is None else addr(q, (extra or {}).get(k, 0))) for k, q in ptrs.items()}
+    return lib.mamba_scan_fwd_ex(batch, dim, dstate, seqlen, io, v["u"], v["delta"], v["dtb"],
+                                 v["A"], v["B"], v["C"], v["Dk"], v["z"], flags, v["h0"],
+                                 v["lens"], v["y"], v["fin"], None)
+
+
+def test_scan_ex_validation(lib):
+    assert ex_call(lib, flags=8) == EFLAGS
+    assert ex_call(lib, flags=-1) == EFLAGS
+    assert ex_call(lib, dstate=17) == ESHAPE
+    assert ex_call(lib, extra={"h0": 2}) == EALIGN
+    assert ex_call(lib, extra={"lens": 2}) == EALIGN
+    assert ex_call(lib, h0=9) == EALIAS           # initial state on top of y
+    assert ex_call(lib, h0=10) == EALIAS          # initial state on top of final_state
+    assert ex_call(lib, lens=9) == EALIAS         # lengths on top of y
+    assert ex_call(lib, flags=NOALLOC, dstate=16, seqlen=70000) == ETOOBIG
+
+
+def test_scan_ex_passes_validation_without_launching(lib):
+    # seqlen 0 with no final_state is complete without any CUDA call, so the
+    # fake addresses are never dereferenced
+    for flags in (0, SOFTPLUS, ZOH, SOFTPLUS | ZOH | NOALLOC):
+        assert ex_call(lib, seqlen=0, flags=flags, fin=None) == OK
+
+
 def step_call(lib, batch=2, dim=8, dstate=16, io=1, state=1, x=2, delta=3, dtb=4, A=5, B=6, C=7,
               Dk=8, z=9, y=10, extra=None):
     ptrs = dict(state=state, x=x, delta=delta, dtb=dtb, A=A, B=B, C=C, Dk=Dk, z=z, y=y)
@@ -139,6 +170,20 @@ def test_state_update_validation(lib):
     assert step_call(lib, extra={"x": 1}) == EALIGN
     assert step_call(lib, y=1) == EALIAS
     assert step_call(lib, x=1) == EALIAS       # state overlaps x
+
+
+def test_state_update_ex_flags(lib):
+    def call(flags, **kw):
+        v = {k: addr(i) for i, k in enumerate(("state", "x", "delta", "dtb", "A", "B", "C",
+                                               "Dk", "z", "y"), 1)}
+        v.update(kw)
+        return lib.mamba_state_update_ex(2, 8, 16, 1, v["state"], v["x"], v["delta"], v["dtb"],
+                                         v["A"], v["B"], v["C"], v["Dk"], v["z"], flags, v["y"],
+                                         None)
+    assert call(NOALLOC) == EFLAGS
+    assert call(16) == EFLAGS
+    assert call(SOFTPLUS | ZOH, state=None) == ENULL
+    assert call(ZOH, y=addr(1)) == EALIAS
 
 
 def test_tuning_validation(lib):
