@@ -355,6 +355,8 @@ def run_ours(args, shape):
         line["e2e"] = e2e_leg(args, shape, inp, dev, stream, mm, ws, pg)
     if not args.no_decode and rank == 0:
         line["decode"] = decode_leg(dev, mm)
+    if not args.no_ext and rank == 0:
+        line["ext"] = ext_leg(shape, (u, delta, dtb, A, B, C, dsk, z), y, fin, dev, stream, mm)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, thr, nrows, secs = oracle_rate(inp, shape, args.cpu_seconds)
         line["cpu_baseline"] = {
@@ -443,6 +445,33 @@ def e2e_leg(args, shape, inp, dev, stream, mm, ws, pg):
             "ms_per_step": ms / k, "overlap": "h2d / scan / d2h of neighbouring steps"}
 
 
+def ext_leg(shape, ins, y, fin, dev, stream, mm, steps=200, warmup=5):
+    """The extended entry point on the same workload: Euler and zero-order
+    hold, each starting from a (random) initial state, every entry using all
+    steps.  Device-resident inputs, CUDA events on the launching stream."""
+    import torch
+    g = torch.Generator(device=dev).manual_seed(7)
+    h0 = 0.3 * torch.randn((shape.batch, shape.dim, shape.dstate), device=dev, generator=g)
+    out = {}
+    for name, zoh in (("euler_initial_state", False), ("zoh_initial_state", True)):
+        def step():
+            mm.mamba_scan_fwd_ex(*ins, softplus=True, zoh=zoh, initial_state=h0, y=y,
+                                 final_state=fin, stream=stream)
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        out[name] = {"ms_per_step": ms, "value": shape.elems / (ms * 1e-3), "unit": UNIT,
+                     "steps": steps}
+    return out
+
+
 def decode_leg(dev, mm):
     """Batched generation: (128, 5120, 16) fp32 state, single-token steps,
     1024 steps replayed from one CUDA graph; 16 distinct input sets cycled."""
@@ -507,6 +536,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-ext", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -498,6 +498,7 @@ __device__ __forceinline__ float fused_step(float2 (&h2)[NT / 2], const float2 (
                                             const ZohK<NT>& zk, float dt_next, float dt,
                                             float du, const float4 (&bc)[NT / 2]) {
     const float2 dt2 = make_float2(dt_next, dt_next);
+    const float2 du2 = make_float2(du, du);
     float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int i = 0; i < NT / 2; ++i) {
@@ -507,7 +508,9 @@ __device__ __forceinline__ float fused_step(float2 (&h2)[NT / 2], const float2 (
             const float2 arg = __fmul2_rn(dt2, a2[i]);
             an[i] = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
         }
-        const float2 bx = input_term<NT, ACC, ZOH>(i, ab[i], a2[i], zk, dt, du, bc[i]);
+        float2 bx;
+        if constexpr (!ZOH) bx = __fmul2_rn(du2, make_float2(bc[i].x, bc[i].y));
+        else bx = input_term<NT, ACC, ZOH>(i, ab[i], a2[i], zk, dt, du, bc[i]);
         h2[i] = __ffma2_rn(ab[i], h2[i], bx);
         if constexpr (!STATE_ONLY) {
             const float2 cp = make_float2(bc[i].z, bc[i].w);
@@ -544,8 +547,13 @@ __device__ __forceinline__ void load_bc(float4 (&bc)[NT / 2], const float4* row)
 //   (3) each slice finishes 1/SPLIT of the outputs: all partial sums (in a
 //       fixed order), skip term and gate.
 // STATE_ONLY is the chunk-summary pass: no C, z or y; it returns
-// (exp(A*sum Delta), h_end).  ZOH selects the zero-order-hold input term.
-template <typename T, int NT, int SPLIT, bool STATE_ONLY, bool SOFTPLUS, bool HAS_Z, bool ZOH>
+// (exp(A*sum Delta), h_end).  MODE: kModePlain (Euler, zero initial state,
+// every entry uses all steps), kModeExt (Euler with an initial state and
+// per-entry lengths) or kModeExtZoh (the same with the zero-order-hold input
+// term).  The plain mode is compiled without the extensions: their per-tile
+// bookkeeping costs about 2% on B300.
+enum { kModePlain = 0, kModeExt = 1, kModeExtZoh = 2 };
+template <typename T, int NT, int SPLIT, bool STATE_ONLY, bool SOFTPLUS, bool HAS_Z, int MODE>
 __global__ void __launch_bounds__(32 * kScanWarps, kScanMinBlocks)
 scan_kernel(const __grid_constant__ ScanArgs a) {
     using Lay = ScanLayout<T, NT, SPLIT>;
@@ -556,6 +564,8 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     constexpr bool ACC = IO<T>::kAccurate;
     constexpr int kNPair = NT / 2;
     constexpr bool has_z = !STATE_ONLY && HAS_Z;
+    constexpr bool EXT = MODE != kModePlain;
+    constexpr bool ZOH = MODE == kModeExtZoh;
     static_assert(NT % 2 == 0 && NP <= kMaxN, "bad state size");
     static_assert(CK::G == G && QC * G == HT && QC >= 1, "a slice's steps are whole 16-byte chunks");
 
@@ -580,9 +590,10 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     const int wrow = (w.tail >= 0) ? w.tail * CH + c : 0;
     // steps in use for this batch entry: past them Delta is 0 (the state is
     // kept) and y is 0
-    long long len = L_;
-    if (a.seqlens) len = min(L_, max(0LL, (long long)a.seqlens[w.b]));
-    const long long t_end = min(w.t1, len);   // end of the live steps of this unit
+    long long t_end = w.t1;   // end of the live steps of this unit
+    if constexpr (EXT) {
+        if (a.seqlens) t_end = min(t_end, max(0LL, (long long)a.seqlens[w.b]));
+    }
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     unsigned char* yt = smem + Lay::ybuf(stages);
@@ -610,7 +621,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
             if (ok) {
                 if (w.tail >= 0 && w.k > 0) {
                     if (!STATE_ONLY) h0 = a.ws_h[((long long)(w.k - 1) * a.tail_rows + wrow) * N + n];
-                } else if (a.h0) {
+                } else if (EXT && a.h0) {
                     h0 = a.h0[row * N + n];
                 }
             }
@@ -724,10 +735,10 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
             CK::load(st_ + off, uv);
 #pragma unroll
             for (int j = 0; j < G; ++j) {
-                float v = delta_of(dv[j]), uu = uv[j];
+                float v = delta_of(dv[j]);
                 const int t = ck * G + j;
-                if (t >= nv_) v = uu = 0.0f;   // past the live steps: the state is kept
-                du_s[t * CH + c] = make_float2(v, ZOH ? uu : v * uu);
+                if (t >= nv_) v = 0.0f;   // past the live steps: the state is kept
+                du_s[t * CH + c] = make_float2(v, ZOH ? (t >= nv_ ? 0.0f : uv[j]) : v * uv[j]);
             }
         }
     };
@@ -743,7 +754,10 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     for (int it = 0; it < ntiles && !aborted; ++it) {
         const long long tt0 = w.t0 + (long long)it * TT;
         const int nv = (int)min((long long)TT, w.t1 - tt0);   // steps of this unit in the tile
-        const long long ny = t_end - tt0;                       // live steps in the tile (may be <= 0)
+        // with per-entry lengths, the steps of the tile past them get y = 0
+        // (without, steps past the sequence are not stored at all)
+        const int ylim =
+            (EXT && a.seqlens && t_end - tt0 < TT) ? (int)max(0LL, t_end - tt0) : TT;
         const unsigned char* st = smem + Lay::stage(stage);
         const unsigned char* ut = st;
         const unsigned char* zt = st + 2 * Lay::kRows;
@@ -844,7 +858,12 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                     for (int k = 1; k < SPLIT; ++k) o += pk[k - 1][(q * G + j) * CH];
                     o = fmaf(dsk, uv[j], o);
                     if constexpr (has_z) o *= silu_f<ACC>(zv[j]);
-                    ov[j] = (q * G + j + hh * HT < ny) ? o : 0.0f;
+                    ov[j] = o;
+                }
+                if (EXT && ylim < TT) {   // uniform over the CTA
+#pragma unroll
+                    for (int j = 0; j < G; ++j)
+                        if (q * G + j + hh * HT >= ylim) ov[j] = 0.0f;
                 }
                 CK::store(yt + off, ov);
             }
@@ -946,8 +965,6 @@ struct StepArgs {
     long long dim;
     int dstate;
     int vec_state;  // state rows 16-byte aligned and N % 4 == 0
-    int softplus;   // Delta = softplus(delta + dt_bias), else delta + dt_bias
-    int zoh;        // zero-order-hold input term, else Euler
 };
 
 // Zero-order-hold input weight of one state entry (as the scan's
@@ -961,7 +978,9 @@ __device__ __forceinline__ float zoh_weight(float dA, float dt, float A) {
 }
 
 // Four lanes per (b, d) row; lane q owns state entries [4q, 4q + 4).
-template <typename T>
+// SP: softplus on Delta; ZOH: zero-order-hold input term (compile-time, so
+// that the common step carries no per-entry branch).
+template <typename T, bool SP, bool ZOH>
 __global__ void __launch_bounds__(kThreads)
 state_update_kernel(const StepArgs a) {
     constexpr bool ACC = IO<T>::kAccurate;
@@ -976,7 +995,7 @@ state_update_kernel(const StepArgs a) {
         xv = IO<T>::to_f(static_cast<const T*>(a.x)[row]);
         const float s = IO<T>::to_f(static_cast<const T*>(a.delta)[row]) +
                         (a.dt_bias ? a.dt_bias[d] : 0.0f);
-        const float dt = a.softplus ? softplus_f<ACC>(s) : s;
+        const float dt = SP ? softplus_f<ACC>(s) : s;
         const float du = dt * xv;
         if (a.z) zv = IO<T>::to_f(static_cast<const T*>(a.z)[row]);
         dsk = a.D_skip ? a.D_skip[d] : 0.0f;
@@ -992,7 +1011,7 @@ state_update_kernel(const StepArgs a) {
             for (int j = 0; j < 4; ++j) {
                 const int n = n0 + j;
                 const float dA = ACC ? expf(dt * Ad[n]) : ex2_approx(dt * (Ad[n] * kLog2e));
-                const float bin = a.zoh ? zoh_weight<ACC>(dA, dt, Ad[n]) * xv : du;
+                const float bin = ZOH ? zoh_weight<ACC>(dA, dt, Ad[n]) * xv : du;
                 hs[j] = fmaf(dA, hs[j], bin * IO<T>::to_f(Bb[n]));
                 acc = fmaf(IO<T>::to_f(Cb[n]), hs[j], acc);
             }
@@ -1000,7 +1019,7 @@ state_update_kernel(const StepArgs a) {
         } else {
             for (int n = n0; n < n0 + 4 && n < N; ++n) {
                 const float dA = ACC ? expf(dt * Ad[n]) : ex2_approx(dt * (Ad[n] * kLog2e));
-                const float bin = a.zoh ? zoh_weight<ACC>(dA, dt, Ad[n]) * xv : du;
+                const float bin = ZOH ? zoh_weight<ACC>(dA, dt, Ad[n]) * xv : du;
                 const float hn = fmaf(dA, h[n], bin * IO<T>::to_f(Bb[n]));
                 h[n] = hn;
                 acc = fmaf(IO<T>::to_f(Cb[n]), hn, acc);
@@ -1024,7 +1043,7 @@ state_update_kernel(const StepArgs a) {
 // (bf16) or two 16-byte (fp32) loads.  Fast path as in the scan: Delta is
 // kept in log2 units and Abar = ex2(Delta' * A).
 constexpr int kStepDims = 32, kStepBatches = 4;   // block = 32 x 4 rows x 2 lanes
-template <typename T>
+template <typename T, bool SP, bool ZOH>
 __global__ void __launch_bounds__(2 * kStepDims * kStepBatches)
 state_update16_kernel(const StepArgs a) {
     constexpr bool ACC = IO<T>::kAccurate;
@@ -1048,11 +1067,11 @@ state_update16_kernel(const StepArgs a) {
         float dt, dtn, du;
         if constexpr (ACC) {
             const float sarg = dv + bias;
-            dt = a.softplus ? softplus_f<true>(sarg) : sarg;
+            dt = SP ? softplus_f<true>(sarg) : sarg;
             dtn = dt;
         } else {
             const float tl = fmaf(dv, kLog2e, bias * kLog2e);
-            dt = !a.softplus ? tl : (tl > 30.0f ? tl : lg2_approx(1.0f + ex2_approx(tl)));
+            dt = !SP ? tl : (tl > 30.0f ? tl : lg2_approx(1.0f + ex2_approx(tl)));
             dtn = dt * kLn2;
         }
         du = dtn * xv;
@@ -1080,7 +1099,7 @@ state_update16_kernel(const StepArgs a) {
 #pragma unroll
         for (int k = 0; k < H; ++k) {
             const float dA = ACC ? expf(dt * Av[k]) : ex2_approx(dt * Av[k]);
-            const float bin = a.zoh ? zoh_weight<ACC>(dA, dtn, Av[k]) * xv : du;
+            const float bin = ZOH ? zoh_weight<ACC>(dA, dtn, Av[k]) * xv : du;
             hs[k] = fmaf(dA, hs[k], bin * Bv[k]);
             if (k & 1) acc1 = fmaf(Cv[k], hs[k], acc1);
             else acc = fmaf(Cv[k], hs[k], acc);
@@ -1225,9 +1244,9 @@ int sm_count(int dev) {
     return cache[dev];
 }
 
-template <typename T, int NT, int SPLIT, bool STATE_ONLY, bool SP, bool HZ, bool ZOH>
+template <typename T, int NT, int SPLIT, bool STATE_ONLY, bool SP, bool HZ, int MODE>
 cudaError_t launch_scan(const ScanArgs& a, int grid, int smem, cudaStream_t st) {
-    auto k = scan_kernel<T, NT, SPLIT, STATE_ONLY, SP, HZ, ZOH>;
+    auto k = scan_kernel<T, NT, SPLIT, STATE_ONLY, SP, HZ, MODE>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     ProfScope prof(STATE_ONLY ? kKindSummary : kKindScan, st);
@@ -1247,28 +1266,36 @@ cudaError_t launch_scan(const ScanArgs& a, int grid, int smem, cudaStream_t st) 
 #endif
 
 // The summary pass reads no z, so it has no HAS_Z instances.
-template <typename T, bool STATE_ONLY, int NT, int S, bool ZOH>
+template <typename T, bool STATE_ONLY, int NT, int S, int MODE>
 cudaError_t dispatch_flags(bool sp, bool hz, const ScanArgs& a, int grid, int smem,
                            cudaStream_t st) {
     if constexpr (STATE_ONLY) {
-        return sp ? launch_scan<T, NT, S, true, true, false, ZOH>(a, grid, smem, st)
-                  : launch_scan<T, NT, S, true, false, false, ZOH>(a, grid, smem, st);
+        return sp ? launch_scan<T, NT, S, true, true, false, MODE>(a, grid, smem, st)
+                  : launch_scan<T, NT, S, true, false, false, MODE>(a, grid, smem, st);
     } else {
         if (sp)
-            return hz ? launch_scan<T, NT, S, false, true, true, ZOH>(a, grid, smem, st)
-                      : launch_scan<T, NT, S, false, true, false, ZOH>(a, grid, smem, st);
-        return hz ? launch_scan<T, NT, S, false, false, true, ZOH>(a, grid, smem, st)
-                  : launch_scan<T, NT, S, false, false, false, ZOH>(a, grid, smem, st);
+            return hz ? launch_scan<T, NT, S, false, true, true, MODE>(a, grid, smem, st)
+                      : launch_scan<T, NT, S, false, true, false, MODE>(a, grid, smem, st);
+        return hz ? launch_scan<T, NT, S, false, false, true, MODE>(a, grid, smem, st)
+                  : launch_scan<T, NT, S, false, false, false, MODE>(a, grid, smem, st);
     }
 }
 
+template <typename T, bool STATE_ONLY, int NT, int S>
+cudaError_t dispatch_mode(int mode, bool sp, bool hz, const ScanArgs& a, int grid, int smem,
+                          cudaStream_t st) {
+    if (mode == kModeExtZoh)
+        return dispatch_flags<T, STATE_ONLY, NT, S, kModeExtZoh>(sp, hz, a, grid, smem, st);
+    if (mode == kModeExt)
+        return dispatch_flags<T, STATE_ONLY, NT, S, kModeExt>(sp, hz, a, grid, smem, st);
+    return dispatch_flags<T, STATE_ONLY, NT, S, kModePlain>(sp, hz, a, grid, smem, st);
+}
+
 template <typename T, bool STATE_ONLY>
-cudaError_t dispatch_scan(int nt, int split, bool sp, bool hz, bool zoh, const ScanArgs& a,
+cudaError_t dispatch_scan(int nt, int split, bool sp, bool hz, int mode, const ScanArgs& a,
                           int grid, int smem, cudaStream_t st) {
-#define X(NT_, S_)                                                                  \
-    if (nt == NT_ && split == S_)                                                    \
-        return zoh ? dispatch_flags<T, STATE_ONLY, NT_, S_, true>(sp, hz, a, grid, smem, st) \
-                   : dispatch_flags<T, STATE_ONLY, NT_, S_, false>(sp, hz, a, grid, smem, st);
+#define X(NT_, S_) \
+    if (nt == NT_ && split == S_) return dispatch_mode<T, STATE_ONLY, NT_, S_>(mode, sp, hz, a, grid, smem, st);
     MAMBA_VARIANTS(X)
 #undef X
     return cudaErrorInvalidValue;
@@ -1468,6 +1495,27 @@ long long packed_row_bytes(int64_t dstate) {
 }  // namespace mamba
 
 using namespace mamba;
+
+// Launch the generation-step kernel (vectorised dstate-16 or generic) with
+// its (softplus, ZOH) instance.
+#define MAMBA_STEP_LAUNCH(KERNEL)                                                        \
+    if (sp) {                                                                            \
+        if (zoh) KERNEL<T, true, true><<<grid, threads, 0, st>>>(a);                     \
+        else KERNEL<T, true, false><<<grid, threads, 0, st>>>(a);                        \
+    } else {                                                                             \
+        if (zoh) KERNEL<T, false, true><<<grid, threads, 0, st>>>(a);                    \
+        else KERNEL<T, false, false><<<grid, threads, 0, st>>>(a);                       \
+    }
+template <typename T>
+void launch_step16(bool sp, bool zoh, dim3 grid, int threads, const StepArgs& a, cudaStream_t st) {
+    MAMBA_STEP_LAUNCH(state_update16_kernel)
+}
+template <typename T>
+void launch_step_generic(bool sp, bool zoh, dim3 grid, int threads, const StepArgs& a,
+                         cudaStream_t st) {
+    MAMBA_STEP_LAUNCH(state_update_kernel)
+}
+#undef MAMBA_STEP_LAUNCH
 
 extern "C" {
 
@@ -1686,12 +1734,13 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     }
     const bool bf = io_dtype == MAMBA_BF16;
     const bool hz = z != nullptr;
+    const int mode = zoh ? kModeExtZoh : ((h0 || seqlens) ? kModeExt : kModePlain);
     auto summary_and_carry = [&](cudaStream_t st) -> cudaError_t {
         const int grid1 = (pl.n_groups - pl.n_full) * (pl.nchunks - 1);
         cudaError_t r =
-            bf ? dispatch_scan<__nv_bfloat16, true>(pl.nt, pl.split, softplus, false, zoh, a,
+            bf ? dispatch_scan<__nv_bfloat16, true>(pl.nt, pl.split, softplus, false, mode, a,
                                                     grid1, pl.smem, st)
-               : dispatch_scan<float, true>(pl.nt, pl.split, softplus, false, zoh, a, grid1,
+               : dispatch_scan<float, true>(pl.nt, pl.split, softplus, false, mode, a, grid1,
                                             pl.smem, st);
         if (r != cudaSuccess) return r;
         const long long n_ent = (long long)entries;
@@ -1705,9 +1754,9 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     auto main_pass = [&](int first, int count, cudaStream_t st) -> cudaError_t {
         ScanArgs m = a;
         m.unit_offset = first;
-        return bf ? dispatch_scan<__nv_bfloat16, false>(pl.nt, pl.split, softplus, hz, zoh, m,
+        return bf ? dispatch_scan<__nv_bfloat16, false>(pl.nt, pl.split, softplus, hz, mode, m,
                                                         count, pl.smem, st)
-                  : dispatch_scan<float, false>(pl.nt, pl.split, softplus, hz, zoh, m, count,
+                  : dispatch_scan<float, false>(pl.nt, pl.split, softplus, hz, mode, m, count,
                                                 pl.smem, st);
     };
     const int n_chunk_units = chunked ? (pl.n_groups - pl.n_full) * pl.nchunks : 0;
@@ -1770,6 +1819,7 @@ int mamba_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen
                            final_state, stream, (flags & MAMBA_FLAG_NOALLOC) != 0);
 }
 
+
 static int state_update_common(int64_t batch, int64_t dim, int64_t dstate, int io_dtype,
                                float* state, const void* x, const void* delta,
                                const float* dt_bias, const float* A, const void* B,
@@ -1803,8 +1853,7 @@ static int state_update_common(int64_t batch, int64_t dim, int64_t dstate, int i
     a.dt_bias = dt_bias; a.A = A; a.D_skip = D_skip; a.y = y;
     a.rows = rows; a.dim = dim; a.dstate = (int)dstate;
     a.vec_state = (dstate % 4 == 0) && aligned(state, 16);
-    a.softplus = (flags & MAMBA_FLAG_SOFTPLUS) ? 1 : 0;
-    a.zoh = (flags & MAMBA_FLAG_ZOH) ? 1 : 0;
+    const bool sp = (flags & MAMBA_FLAG_SOFTPLUS) != 0, zoh = (flags & MAMBA_FLAG_ZOH) != 0;
     // dstate 16 with 16-byte aligned rows: the vectorised two-lane kernel
     const bool vec16 = dstate == 16 && aligned(state, 16) && aligned(A, 16) && aligned(B, 16) &&
                        aligned(C, 16) && batch <= 65535LL * kStepBatches;
@@ -1813,9 +1862,9 @@ static int state_update_common(int64_t batch, int64_t dim, int64_t dstate, int i
                         (unsigned)((batch + kStepBatches - 1) / kStepBatches));
         ProfScope prof(kKindStep, stream);
         if (io_dtype == MAMBA_BF16)
-            state_update16_kernel<__nv_bfloat16><<<grid, 2 * kStepDims * kStepBatches, 0, stream>>>(a);
+            launch_step16<__nv_bfloat16>(sp, zoh, grid, 2 * kStepDims * kStepBatches, a, stream);
         else
-            state_update16_kernel<float><<<grid, 2 * kStepDims * kStepBatches, 0, stream>>>(a);
+            launch_step16<float>(sp, zoh, grid, 2 * kStepDims * kStepBatches, a, stream);
         return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
     }
     const long long threads = rows * 4;
@@ -1823,9 +1872,9 @@ static int state_update_common(int64_t batch, int64_t dim, int64_t dstate, int i
     {
         ProfScope prof(kKindStep, stream);
         if (io_dtype == MAMBA_BF16)
-            state_update_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(a);
+            launch_step_generic<__nv_bfloat16>(sp, zoh, dim3(grid), kThreads, a, stream);
         else
-            state_update_kernel<float><<<grid, kThreads, 0, stream>>>(a);
+            launch_step_generic<float>(sp, zoh, dim3(grid), kThreads, a, stream);
     }
     return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
