@@ -13,7 +13,9 @@ and the page it follows.
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
 closed forms and independent formulations (Theorem 1's gated RNN, the
 keep/reset limits, the explicitly unrolled sum, the time-invariant
-convolution, linearity, causality).
+convolution, linearity, causality); the backward pass ``scan_bwd`` by
+``tests/test_oracle_bwd_pins.py`` (central finite differences of the
+forward for every input, and exact adjoint identities).
 """
 
 from __future__ import annotations
@@ -60,6 +62,9 @@ def _load():
             lib.oracle_state_update_f64.argtypes = [i64, i64, i64, P, P, P, P, P, P, P, P, P,
                                                     ctypes.c_int, ctypes.c_int, P]
             lib.oracle_state_update_f64.restype = ctypes.c_int
+            lib.oracle_scan_bwd_f64.argtypes = [i64, i64, i64, i64] + [P] * 8 + [ctypes.c_int] \
+                + [P] * 12
+            lib.oracle_scan_bwd_f64.restype = ctypes.c_int
             lib.oracle_softplus_f64.argtypes = [ctypes.c_double]
             lib.oracle_softplus_f64.restype = ctypes.c_double
             lib.oracle_zoh_weight_f64.argtypes = [ctypes.c_double, ctypes.c_double]
@@ -122,6 +127,30 @@ def scan(u, delta, A, B, C, dt_bias=None, D_skip=None, z=None, softplus: bool = 
     if rc <= 0:
         raise RuntimeError(f"oracle_scan_f64 failed: {rc}")
     return y, hT, rc
+
+
+def scan_bwd(u, delta, A, B, C, dy, dt_bias=None, D_skip=None, z=None, softplus: bool = True,
+             h0=None, dfinal=None) -> dict:
+    """Gradients of J = sum(dy * y) + sum(dfinal * final_state) with respect
+    to every input of ``scan`` (Euler input term), in fp64.  Returns a dict
+    with du, ddelta, dz (or None), dA, dB, dC, dD, ddt_bias and dh0."""
+    u, delta, A, B, C, dy = map(_f64, (u, delta, A, B, C, dy))
+    dt_bias, D_skip, z, h0, dfinal = map(_f64, (dt_bias, D_skip, z, h0, dfinal))
+    bt, d, l = u.shape
+    n = A.shape[1]
+    assert dy.shape == u.shape and B.shape == (bt, n, l) and C.shape == (bt, n, l)
+    out = dict(du=np.empty((bt, d, l)), ddelta=np.empty((bt, d, l)),
+               dz=None if z is None else np.empty((bt, d, l)), dA=np.empty((d, n)),
+               dB=np.empty((bt, n, l)), dC=np.empty((bt, n, l)), dD=np.empty(d),
+               ddt_bias=np.empty(d), dh0=np.empty((bt, d, n)))
+    rc = _load().oracle_scan_bwd_f64(
+        bt, d, n, l, _ptr(u), _ptr(delta), _ptr(dt_bias), _ptr(A), _ptr(B), _ptr(C),
+        _ptr(D_skip), _ptr(z), int(bool(softplus)), _ptr(h0), _ptr(dy), _ptr(dfinal),
+        _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]),
+        _ptr(out["dD"]), _ptr(out["dz"]), _ptr(out["ddt_bias"]), _ptr(out["dh0"]))
+    if rc != 0:
+        raise RuntimeError(f"oracle_scan_bwd_f64 failed: {rc}")
+    return out
 
 
 def state_update(state, x, delta, A, B, C, dt_bias=None, D_skip=None, z=None,

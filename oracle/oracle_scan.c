@@ -251,3 +251,109 @@ int oracle_state_update_f64(int64_t batch, int64_t dim, int64_t dstate,
     }
     return 0;
 }
+
+/*
+ * Reverse-mode gradient of oracle_scan_f64 (Euler input term), for the
+ * backward pass that recomputes the state instead of storing it (page
+ * "Mamba: linear-time sequence modeling with selective state spaces", "What
+ * they did": the fused scan keeps the expanded state on chip and recomputes
+ * it in the backward pass).  Given dy = dJ/dy and, optionally, dfinal =
+ * dJ/d final_state, it returns the gradients of J with respect to every
+ * input.  Written out from the chain rule on the forward loop:
+ *
+ *   pre_t   = sum_n C[n,t] h_t[n] + D u_t,       y_t = pre_t * silu(z_t)
+ *   g_t     = dy_t * silu(z_t)                   (dy_t without z)
+ *   dz_t    = dy_t * pre_t * silu'(z_t),         silu'(z) = s(z) (1 + z (1 - s(z)))
+ *   dh      accumulates g_t C[:,t] at step t, then flows to step t-1 times Abar_t
+ *   dB[n,t] = dh[n] Delta_t u_t   (summed over d)    dC[n,t] = g_t h_t[n]  (over d)
+ *   du_t    = g_t D + sum_n dh[n] Delta_t B[n,t]
+ *   dDelta  = sum_n dh[n] (A[n] Abar_t[n] h_{t-1}[n] + B[n,t] u_t)
+ *   dA[n]   = sum_t dh[n] Delta_t Abar_t[n] h_{t-1}[n]   (summed over b)
+ *   ddelta  = dDelta * sigmoid(s_t) with softplus (dDelta without); ddt_bias = sum of ddelta
+ *   dD      = sum_t g_t u_t;   dh0 = dh after step 0
+ *
+ * Single-threaded; dz may be NULL when z is; dh0, dfinal, h0 nullable.
+ * Accumulated outputs (dA, dB, dC, dD, ddt_bias) are zeroed first.
+ */
+int oracle_scan_bwd_f64(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                        const double *u, const double *delta, const double *dt_bias,
+                        const double *A, const double *B, const double *C,
+                        const double *D_skip, const double *z, int softplus,
+                        const double *h0, const double *dy, const double *dfinal,
+                        double *du, double *ddelta, double *dA, double *dB, double *dC,
+                        double *dD, double *dz, double *ddt_bias, double *dh0)
+{
+    if (batch < 0 || dim < 0 || dstate < 0 || seqlen < 0)
+        return -2;
+    if (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC || !dD ||
+        !ddt_bias || (z && !dz))
+        return -1;
+    const int64_t N = dstate, L = seqlen, D = dim;
+    memset(dA, 0, sizeof(double) * (size_t)(D * N));
+    memset(dB, 0, sizeof(double) * (size_t)(batch * N * L));
+    memset(dC, 0, sizeof(double) * (size_t)(batch * N * L));
+    memset(dD, 0, sizeof(double) * (size_t)D);
+    memset(ddt_bias, 0, sizeof(double) * (size_t)D);
+    double *hs = (double *)malloc(sizeof(double) * (size_t)((L + 1) * (N > 0 ? N : 1)));
+    double *dh = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    if (!hs || !dh) {
+        free(hs);
+        free(dh);
+        return -3;
+    }
+    for (int64_t row = 0; row < batch * D; ++row) {
+        const int64_t b = row / D, d = row % D;
+        const double *ur = u + row * L, *dl = delta + row * L, *dyr = dy + row * L;
+        const double *zr = z ? z + row * L : NULL;
+        const double *Bb = B + b * N * L, *Cb = C + b * N * L, *Ad = A + d * N;
+        const double bias = dt_bias ? dt_bias[d] : 0.0;
+        const double dsk = D_skip ? D_skip[d] : 0.0;
+        /* forward, keeping every state: hs[t*N + n] is the state before step t */
+        for (int64_t n = 0; n < N; ++n)
+            hs[n] = h0 ? h0[row * N + n] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            const double s = dl[t] + bias;
+            const double dt = softplus ? oracle_softplus_f64(s) : s;
+            for (int64_t n = 0; n < N; ++n)
+                hs[(t + 1) * N + n] = exp(dt * Ad[n]) * hs[t * N + n] + dt * Bb[n * L + t] * ur[t];
+        }
+        for (int64_t n = 0; n < N; ++n)
+            dh[n] = dfinal ? dfinal[row * N + n] : 0.0;
+        for (int64_t t = L - 1; t >= 0; --t) {
+            const double s = dl[t] + bias;
+            const double dt = softplus ? oracle_softplus_f64(s) : s;
+            const double sig = softplus ? 1.0 / (1.0 + exp(-s)) : 1.0;
+            const double *ht = hs + (t + 1) * N, *hp = hs + t * N;
+            double pre = dsk * ur[t];
+            for (int64_t n = 0; n < N; ++n)
+                pre += Cb[n * L + t] * ht[n];
+            double g = dyr[t];
+            if (zr) {
+                const double sz = 1.0 / (1.0 + exp(-zr[t]));
+                g = dyr[t] * zr[t] * sz;
+                dz[row * L + t] = dyr[t] * pre * sz * (1.0 + zr[t] * (1.0 - sz));
+            }
+            dD[d] += g * ur[t];
+            double dut = g * dsk, ddt = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                const double abar = exp(dt * Ad[n]);
+                dh[n] += g * Cb[n * L + t];
+                dC[b * N * L + n * L + t] += g * ht[n];
+                dB[b * N * L + n * L + t] += dh[n] * dt * ur[t];
+                dut += dh[n] * dt * Bb[n * L + t];
+                ddt += dh[n] * (Ad[n] * abar * hp[n] + Bb[n * L + t] * ur[t]);
+                dA[d * N + n] += dh[n] * dt * abar * hp[n];
+                dh[n] *= abar;
+            }
+            du[row * L + t] = dut;
+            ddelta[row * L + t] = ddt * sig;
+            ddt_bias[d] += ddt * sig;
+        }
+        if (dh0)
+            for (int64_t n = 0; n < N; ++n)
+                dh0[row * N + n] = dh[n];
+    }
+    free(hs);
+    free(dh);
+    return 0;
+}
