@@ -357,6 +357,8 @@ def run_ours(args, shape):
         line["decode"] = decode_leg(dev, mm)
     if not args.no_ext and rank == 0:
         line["ext"] = ext_leg(shape, (u, delta, dtb, A, B, C, dsk, z), y, fin, dev, stream, mm)
+    if not args.no_bwd and rank == 0:
+        line["bwd"] = bwd_leg(shape, (u, delta, dtb, A, B, C, dsk, z), dev, stream, mm)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, thr, nrows, secs = oracle_rate(inp, shape, args.cpu_seconds)
         line["cpu_baseline"] = {
@@ -472,6 +474,34 @@ def ext_leg(shape, ins, y, fin, dev, stream, mm, steps=200, warmup=5):
     return out
 
 
+def bwd_leg(shape, ins, dev, stream, mm, steps=10, warmup=3):
+    """The backward pass on the same workload: gradients of every input from
+    a random dy, with the final-state gradient off.  Device-resident inputs
+    and outputs, CUDA events on the launching stream; per-kind device times
+    from the library's launch timing."""
+    import torch
+    g = torch.Generator(device=dev).manual_seed(11)
+    dy = torch.randn(ins[0].shape, device=dev, generator=g).to(ins[0].dtype)
+    out = mm.mamba_scan_bwd(*ins, dy, stream=stream)
+    for _ in range(warmup):
+        mm.mamba_scan_bwd(*ins, dy, out=out, stream=stream)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    mm.mamba_profile_begin()
+    e0.record(stream)
+    for _ in range(steps):
+        mm.mamba_scan_bwd(*ins, dy, out=out, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    prof = mm.mamba_profile_end()
+    ms = e0.elapsed_time(e1) / steps
+    updates = shape.batch * shape.dim * shape.seqlen * shape.dstate
+    return {"ms_per_step": ms, "value": shape.elems / (ms * 1e-3), "unit": UNIT, "steps": steps,
+            "state_updates_per_s": updates / (ms * 1e-3),
+            "launch_ms_by_kind": {k: v[0] / v[1] for k, v in prof.items() if v[1]},
+            "note": "checkpoint pass + reverse pass (recomputes each 12-step tile) + reductions"}
+
+
 def decode_leg(dev, mm):
     """Batched generation: (128, 5120, 16) fp32 state, single-token steps,
     1024 steps replayed from one CUDA graph; 16 distinct input sets cycled."""
@@ -537,6 +567,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-ext", action="store_true")
+    ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -219,6 +219,48 @@ int mamba_state_update_ex(int64_t batch, int64_t dim, int64_t dstate, int io_dty
                           const void *B, const void *C, const float *D_skip,
                           const void *z, int flags, void *y, cudaStream_t stream);
 
+/*
+ * Backward pass of the scan (Euler input term): gradients of a loss J with
+ * respect to every input, given dy = dJ/dy and optionally dJ/d final_state.
+ * The states are recomputed, not stored by the forward call (paper "Mamba:
+ * linear-time sequence modeling with selective state spaces", "What they
+ * did": the fused scan recomputes the expanded state in the backward pass):
+ * a checkpoint pass keeps the state every 12 steps in scratch memory, and a
+ * reverse pass recomputes each 12-step tile from its checkpoint.
+ *
+ *   inputs as in mamba_scan_fwd_ex (u, delta, dt_bias, A, B, C, D_skip, z,
+ *   initial_state), plus
+ *   flags          : MAMBA_FLAG_SOFTPLUS only (other bits -> MAMBA_ERR_FLAGS)
+ *   dy             : (batch, dim, seqlen)    io_dtype
+ *   d_final_state  : (batch, dim, dstate)    fp32   nullable (taken as 0)
+ * outputs (written, never accumulated into):
+ *   du, ddelta     : (batch, dim, seqlen)    io_dtype
+ *   dz             : (batch, dim, seqlen)    io_dtype  required when z is given
+ *   dA             : (dim, dstate)           fp32
+ *   dB, dC         : (batch, dstate, seqlen) fp32   (sums over the channels)
+ *   dD_skip        : (dim)                   fp32   nullable
+ *   ddt_bias       : (dim)                   fp32   nullable
+ *   d_initial_state: (batch, dim, dstate)    fp32   nullable
+ *
+ * ddelta is dJ/d(delta) (through the softplus when the flag is set), and
+ * ddt_bias its sum over batch and time.  Sums over channels, batch and time
+ * are formed from per-warp partials added in a fixed order, so results are
+ * deterministic.  Scratch (about batch * dim * seqlen * dstate / 3 bytes of
+ * checkpoints plus 2 * batch * dstate * seqlen * ceil(dim / 32) * 4 bytes of
+ * partials, padded dstate) comes from the stream-ordered pool.  Outputs must
+ * not overlap inputs or each other.
+ */
+int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                   int io_dtype,
+                   const void *u, const void *delta, const float *dt_bias,
+                   const float *A, const void *B, const void *C,
+                   const float *D_skip, const void *z, int flags,
+                   const float *initial_state, const void *dy,
+                   const float *d_final_state,
+                   void *du, void *ddelta, float *dA, float *dB, float *dC,
+                   float *dD_skip, void *dz, float *ddt_bias,
+                   float *d_initial_state, cudaStream_t stream);
+
 /* Static, human-readable name of a mamba_status_t value. */
 const char *mamba_status_string(int status);
 
@@ -264,7 +306,9 @@ int mamba_scan_set_tuning(int tail, int stages, int chunks);
  * each kernel kind k < nkinds, the summed device time in milliseconds
  * (total_ms[k]) and the number of launches (launches[k]).  Kinds:
  * 0 = scan, 1 = chunk summary, 2 = chunk carry, 3 = state update,
- * 4 = B/C packing (one per scan call).
+ * 4 = B/C packing (one per scan or backward call), 5 = backward checkpoint
+ * pass, 6 = backward reverse pass, 7 = backward reductions (one timing for
+ * the three reduction launches of a call).
  * Either output may be NULL.  Not meant for use during stream capture.
  */
 int mamba_profile_begin(void);

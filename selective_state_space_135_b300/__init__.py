@@ -21,6 +21,7 @@ from ._lib import (  # noqa: F401
     mamba_device_status,
     mamba_profile_begin,
     mamba_profile_end,
+    mamba_scan_bwd,
     mamba_scan_fwd,
     mamba_scan_fwd_ex,
     mamba_scan_fwd_noalloc,

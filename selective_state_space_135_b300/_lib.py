@@ -15,7 +15,8 @@ MAMBA_F32 = 0
 MAMBA_BF16 = 1
 
 # every symbol the header declares
-EXPORTS = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_ex", "mamba_state_update",
+EXPORTS = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_ex", "mamba_scan_bwd",
+           "mamba_state_update",
            "mamba_state_update_ex", "mamba_status_string", "mamba_device_status",
            "mamba_selftest_wait_timeout", "mamba_version", "mamba_scan_set_tuning",
            "mamba_profile_begin", "mamba_profile_end")
@@ -25,7 +26,8 @@ MAMBA_FLAG_SOFTPLUS = 1
 MAMBA_FLAG_ZOH = 2
 MAMBA_FLAG_NOALLOC = 4
 
-KIND_NAMES = ("scan", "chunk_summary", "chunk_carry", "state_update", "pack_bc")
+KIND_NAMES = ("scan", "chunk_summary", "chunk_carry", "state_update", "pack_bc",
+              "bwd_checkpoint", "bwd", "bwd_reduce")
 
 
 class MambaError(RuntimeError):
@@ -63,6 +65,11 @@ def load():
         lib.mamba_state_update_ex.argtypes = [i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                               vp, i32, vp, vp]
         lib.mamba_state_update_ex.restype = i32
+        # sizes, dtype; 8 inputs; flags; initial state, dy, d_final_state;
+        # 9 outputs; stream
+        lib.mamba_scan_bwd.argtypes = [i64, i64, i64, i64, i32] + [vp] * 8 + [i32] + [vp] * 3 \
+            + [vp] * 9 + [vp]
+        lib.mamba_scan_bwd.restype = i32
         lib.mamba_status_string.argtypes = [i32]
         lib.mamba_status_string.restype = ctypes.c_char_p
         lib.mamba_device_status.argtypes = [vp]
@@ -225,6 +232,60 @@ def mamba_scan_fwd_ex(u, delta, dt_bias, A, B, C, D_skip, z, softplus: bool = Tr
     if rc != 0:
         raise MambaError(rc, "mamba_scan_fwd_ex")
     return y
+
+
+def mamba_scan_bwd(u, delta, dt_bias, A, B, C, D_skip, z, dy, softplus: bool = True,
+                   initial_state=None, d_final_state=None, want_initial_state_grad: bool = False,
+                   out=None, stream=None) -> dict:
+    """Backward pass of the scan: returns a dict of gradients du, ddelta, dz
+    (None without z), dA, dB, dC, dD_skip, ddt_bias and, when asked,
+    d_initial_state.  dy has u's shape and dtype; d_final_state (batch, dim,
+    N) fp32 is optional.  `out` may supply any of the output tensors."""
+    torch = _torch()
+    lib = load()
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    dev = u.device
+    io = _io_dtype(u)
+    f32 = torch.float32
+    o = dict(out or {})
+    o.setdefault("du", torch.empty_like(u))
+    o.setdefault("ddelta", torch.empty_like(u))
+    o.setdefault("dz", None if z is None else torch.empty_like(u))
+    o.setdefault("dA", torch.empty((dim, N), dtype=f32, device=dev))
+    o.setdefault("dB", torch.empty((batch, N, L), dtype=f32, device=dev))
+    o.setdefault("dC", torch.empty((batch, N, L), dtype=f32, device=dev))
+    o.setdefault("dD_skip", torch.empty((dim,), dtype=f32, device=dev))
+    o.setdefault("ddt_bias", torch.empty((dim,), dtype=f32, device=dev))
+    o.setdefault("d_initial_state", torch.empty((batch, dim, N), dtype=f32, device=dev)
+                 if want_initial_state_grad else None)
+    ins = (
+        _ptr(u, "u", u.dtype, (batch, dim, L), dev),
+        _ptr(delta, "delta", u.dtype, (batch, dim, L), dev),
+        _ptr(dt_bias, "dt_bias", f32, (dim,), dev),
+        _ptr(A, "A", f32, (dim, N), dev),
+        _ptr(B, "B", u.dtype, (batch, N, L), dev),
+        _ptr(C, "C", u.dtype, (batch, N, L), dev),
+        _ptr(D_skip, "D_skip", f32, (dim,), dev),
+        _ptr(z, "z", u.dtype, (batch, dim, L), dev),
+    )
+    h0 = _ptr(initial_state, "initial_state", f32, (batch, dim, N), dev)
+    dyp = _ptr(dy, "dy", u.dtype, (batch, dim, L), dev)
+    dfp = _ptr(d_final_state, "d_final_state", f32, (batch, dim, N), dev)
+    shapes = dict(du=((batch, dim, L), u.dtype), ddelta=((batch, dim, L), u.dtype),
+                  dz=((batch, dim, L), u.dtype), dA=((dim, N), f32), dB=((batch, N, L), f32),
+                  dC=((batch, N, L), f32), dD_skip=((dim,), f32), ddt_bias=((dim,), f32),
+                  d_initial_state=((batch, dim, N), f32))
+    op = {k: _ptr(o[k], k, shapes[k][1], shapes[k][0], dev) for k in shapes}
+    with torch.cuda.device(dev):
+        st = _stream_handle(stream, dev)
+        rc = lib.mamba_scan_bwd(batch, dim, N, L, io, *ins, int(bool(softplus)), h0, dyp, dfp,
+                                op["du"], op["ddelta"], op["dA"], op["dB"], op["dC"],
+                                op["dD_skip"], op["dz"], op["ddt_bias"], op["d_initial_state"],
+                                st)
+    if rc != 0:
+        raise MambaError(rc, "mamba_scan_bwd")
+    return o
 
 
 def mamba_state_update(state, x, delta, dt_bias, A, B, C, D_skip, z, y=None, stream=None):

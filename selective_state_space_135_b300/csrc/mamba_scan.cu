@@ -44,16 +44,12 @@
 //     accumulation are fp32 in both.  Packed fp32x2 multiply/FMA (sm_100+)
 //     halves the instruction count of the state update.
 
-#include "mamba_scan.h"
+#include "scan_common.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
 
 #include <algorithm>
-#include <cmath>
-#include <cstdint>
 #include <cstring>
 #include <mutex>
 #include <type_traits>
@@ -69,86 +65,7 @@ __device__ int g_error_word;  // nonzero once a bounded device wait gave up
 
 constexpr int kThreads = 128;        // threads per CTA of the state-update kernel
 constexpr int kMaxStages = 4;
-constexpr int kMaxN = 16;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
-
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.69314718055994531f;
-
-template <typename T> struct IO;
-template <> struct IO<float> {
-    static constexpr bool kAccurate = true;
-    __device__ static void unpack(const uint4& r, float* v) {
-        v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
-        v[2] = __uint_as_float(r.z); v[3] = __uint_as_float(r.w);
-    }
-    __device__ static uint4 pack(const float* v) {
-        return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
-                          __float_as_uint(v[2]), __float_as_uint(v[3]));
-    }
-    __device__ static float to_f(float x) { return x; }
-    __device__ static float from_f(float x) { return x; }
-};
-template <> struct IO<__nv_bfloat16> {
-    static constexpr bool kAccurate = false;
-    __device__ static void unpack(const uint4& r, float* v) {
-        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[2 * i] = __uint_as_float(w[i] << 16);
-            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
-    }
-    __device__ static uint4 pack(const float* v) {
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-            w[i] = *reinterpret_cast<uint32_t*>(&p);
-        }
-        return make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    __device__ static float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
-    __device__ static __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
-};
-
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float lg2_approx(float x) {
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// softplus(s) = log(1 + e^s); for s > 20 it equals s to within e^-20.
-template <bool ACC>
-__device__ __forceinline__ float softplus_f(float s) {
-    float r;
-    if (ACC) {
-        r = log1pf(expf(s));
-    } else {
-        r = lg2_approx(1.0f + ex2_approx(s * kLog2e)) * kLn2;
-    }
-    return s > 20.0f ? s : r;
-}
-
-// silu(z) = z * sigmoid(z).  Accurate path: z / (1 + e^-z).  Fast path:
-// sigmoid(z) = (1 + tanh(z/2)) / 2, so silu(z) = h + h * tanh(h) with h = z/2,
-// one hardware tanh (max relative error about 2^-11).
-__device__ __forceinline__ float tanh_approx(float x) {
-    float y;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-template <bool ACC>
-__device__ __forceinline__ float silu_f(float z) {
-    if (ACC) return z / (1.0f + expf(-z));
-    const float h = 0.5f * z;
-    return fmaf(h, tanh_approx(h), h);
-}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -1142,9 +1059,6 @@ std::vector<cudaMemPool_t> g_pools;
 
 // Optional per-launch timing: while enabled, every kernel launch is bracketed
 // by two CUDA events recorded on its own stream.
-enum LaunchKind {
-    kKindScan = 0, kKindSummary = 1, kKindCarry = 2, kKindStep = 3, kKindPack = 4, kKinds = 5
-};
 struct ProfRec {
     int kind;
     cudaEvent_t start, stop;
@@ -1153,39 +1067,24 @@ std::mutex g_prof_mu;
 bool g_prof_on = false;
 std::vector<ProfRec> g_prof_recs;
 
-struct ProfScope {
-    cudaEvent_t stop = nullptr;
-    cudaStream_t st;
-    ProfScope(int kind, cudaStream_t s) : st(s) {
-        std::lock_guard<std::mutex> lk(g_prof_mu);
-        if (!g_prof_on) return;
-        ProfRec r;
-        r.kind = kind;
-        if (cudaEventCreate(&r.start) != cudaSuccess) return;
-        if (cudaEventCreate(&r.stop) != cudaSuccess) {
-            cudaEventDestroy(r.start);
-            return;
-        }
-        cudaEventRecord(r.start, st);
-        stop = r.stop;
-        g_prof_recs.push_back(r);
+ProfScope::ProfScope(int kind, cudaStream_t s) : st(s) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on) return;
+    ProfRec r;
+    r.kind = kind;
+    if (cudaEventCreate(&r.start) != cudaSuccess) return;
+    if (cudaEventCreate(&r.stop) != cudaSuccess) {
+        cudaEventDestroy(r.start);
+        return;
     }
-    ~ProfScope() {
-        if (stop) cudaEventRecord(stop, st);
-    }
-};
-
-int esize(int dt) { return dt == MAMBA_BF16 ? 2 : 4; }
-
-bool aligned(const void* p, size_t a) {
-    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+    cudaEventRecord(r.start, st);
+    stop = r.stop;
+    g_prof_recs.push_back(r);
+}
+ProfScope::~ProfScope() {
+    if (stop) cudaEventRecord(stop, st);
 }
 
-bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
-    if (!a || !b || na == 0 || nb == 0) return false;
-    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-    return x < y + nb && y < x + na;
-}
 
 int get_pool(int dev, cudaMemPool_t* out) {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -1242,6 +1141,26 @@ int sm_count(int dev) {
         cache[dev] = v > 0 ? v : 148;
     }
     return cache[dev];
+}
+
+cudaError_t launch_pack_bc(int io_dtype, const void* B, const void* C, float4* out,
+                           long long batch, long long L, int N, int NP, float scale,
+                           cudaStream_t stream) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const long long items = batch * L * (NP / 2);
+    const int blocks = (int)std::max<long long>(
+        1, std::min<long long>((items + 255) / 256, 16LL * sm_count(dev)));
+    ProfScope prof(kKindPack, stream);
+    if (io_dtype == MAMBA_BF16)
+        pack_bc_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), out,
+            batch, L, N, NP, scale);
+    else
+        pack_bc_kernel<float><<<blocks, 256, 0, stream>>>(
+            static_cast<const float*>(B), static_cast<const float*>(C), out, batch, L, N, NP,
+            scale);
+    return cudaGetLastError();
 }
 
 template <typename T, int NT, int SPLIT, bool STATE_ONLY, bool SP, bool HZ, int MODE>
@@ -1716,22 +1635,8 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     a.tail_rows = (int)tail_rows;
 
     cudaError_t e;
-    {
-        const long long items = batch * seqlen * (pl.np / 2);
-        const int blocks = (int)std::min<long long>((items + 255) / 256, 16LL * sm_count(dev));
-        ProfScope prof(kKindPack, stream);
-        const float scale = acc ? 1.0f : kLn2;
-        float4* out = static_cast<float4*>(scratch);
-        if (io_dtype == MAMBA_BF16)
-            pack_bc_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
-                static_cast<const __nv_bfloat16*>(B), static_cast<const __nv_bfloat16*>(C), out,
-                batch, seqlen, (int)dstate, pl.np, scale);
-        else
-            pack_bc_kernel<float><<<blocks, 256, 0, stream>>>(
-                static_cast<const float*>(B), static_cast<const float*>(C), out, batch, seqlen,
-                (int)dstate, pl.np, scale);
-        e = cudaGetLastError();
-    }
+    e = launch_pack_bc(io_dtype, B, C, static_cast<float4*>(scratch), batch, seqlen,
+                       (int)dstate, pl.np, acc ? 1.0f : kLn2, stream);
     const bool bf = io_dtype == MAMBA_BF16;
     const bool hz = z != nullptr;
     const int mode = zoh ? kModeExtZoh : ((h0 || seqlens) ? kModeExt : kModePlain);

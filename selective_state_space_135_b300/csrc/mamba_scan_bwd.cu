@@ -1,0 +1,658 @@
+// Backward pass of the selective scan (Euler input term) for B300 (sm_103a).
+//
+// The fused forward keeps the expanded state on chip and the backward pass
+// recomputes it instead of reading it back (page "Mamba: linear-time
+// sequence modeling with selective state spaces", "What they did").  Here:
+//
+//   1. checkpoint pass: one lane per channel holding all N state entries
+//      runs the forward recurrence and stores the state before every tile of
+//      kBwdTile steps (B x D x ceil(L / kBwdTile) x N fp32);
+//   2. reverse pass: per tile, last to first, the lane recomputes the tile's
+//      states from its checkpoint into shared memory, then walks the tile
+//      backwards carrying dh = dJ/dh:
+//        g_t   = dy_t * silu(z_t)             dz_t = dy_t * pre_t * silu'(z_t)
+//        dh   += g_t C_t                       dC_t += g_t h_t,  dB_t += dh Delta_t u_t
+//        du_t  = g_t D + sum_n dh Delta_t B_t  dDelta_t = sum_n dh (A Abar h_{t-1} + B_t u_t)
+//        dA   += dh Delta_t Abar h_{t-1}       dh   *= Abar_t
+//      with ddelta = dDelta * sigmoid(s) under softplus.  B and C are shared
+//      by all channels of a batch entry, so dB and dC are sums over d: the
+//      warp sums its 32 channels with a transposing butterfly of shuffles
+//      (one shuffle per value) and writes one partial per 32 channels;
+//   3. reduction passes add the partials in a fixed order (deterministic
+//      results, no atomics): dB, dC over channel groups, dA, D_skip and
+//      dt_bias gradients over the batch.
+
+#include "scan_common.cuh"
+
+#include <algorithm>
+#include <cstring>
+
+namespace mamba {
+namespace {
+
+constexpr int kBwdTile = 12;        // steps between checkpoints = reverse tile (35 KB of
+                                    // shared memory per warp at dstate 16: six per SM)
+constexpr int kCkptThreads = 128;   // checkpoint pass: four independent warps per CTA
+constexpr int kReduceThreads = 256;
+
+struct BwdArgs {
+    const void* u;
+    const void* delta;
+    const void* z;
+    const void* dy;
+    const float4* bc;   // packed rows (B pair, C pair), natural units: [batch][L][NP / 2]
+    const float* dt_bias;
+    const float* A;
+    const float* D_skip;
+    const float* h0;      // initial state or null
+    const float* dfinal;  // dJ / d final state or null
+    float* ckpt;          // [row][ntiles][NP]: state before each tile
+    void* du;
+    void* ddelta;
+    void* dz;
+    float* pB;            // [group][batch][L][NP]: dB summed over the group's 32 channels
+    float* pC;
+    float* pA;            // [row][NP]
+    float* pD;            // [row]
+    float* pbias;         // [row]
+    float* dh0;           // [row][N] or null
+    long long dim, L;
+    int batch, N, groups, ntiles;
+    int vec8;   // every (batch, d) row of u, delta, z, dy, du, ddelta, dz is 8-byte aligned
+};
+
+// One lane's kBwdTile consecutive elements of its row, starting at a tile
+// boundary: 8-byte accesses for a full tile of an aligned row (the tile
+// start is 8-byte aligned: kBwdTile elements are 24 or 48 bytes), scalar
+// accesses otherwise.
+template <typename T>
+__device__ __forceinline__ void load_tile_row(const T* row, long long t0, int nv, bool vec,
+                                              bool on, float (&v)[kBwdTile]) {
+    if (on && vec && nv == kBwdTile) {
+        const uint2* p = reinterpret_cast<const uint2*>(row + t0);
+        constexpr int kPer = 8 / (int)sizeof(T);
+#pragma unroll
+        for (int k = 0; k < kBwdTile / kPer; ++k) {
+            const uint2 r = p[k];
+            if constexpr (sizeof(T) == 2) {
+                v[4 * k] = __uint_as_float(r.x << 16);
+                v[4 * k + 1] = __uint_as_float(r.x & 0xffff0000u);
+                v[4 * k + 2] = __uint_as_float(r.y << 16);
+                v[4 * k + 3] = __uint_as_float(r.y & 0xffff0000u);
+            } else {
+                v[2 * k] = __uint_as_float(r.x);
+                v[2 * k + 1] = __uint_as_float(r.y);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kBwdTile; ++i) v[i] = (on && i < nv) ? IO<T>::to_f(row[t0 + i]) : 0.0f;
+    }
+}
+template <typename T>
+__device__ __forceinline__ void store_tile_row(T* row, long long t0, int nv, bool vec,
+                                               const float (&v)[kBwdTile]) {
+    if (vec && nv == kBwdTile) {
+        uint2* p = reinterpret_cast<uint2*>(row + t0);
+        constexpr int kPer = 8 / (int)sizeof(T);
+#pragma unroll
+        for (int k = 0; k < kBwdTile / kPer; ++k) {
+            uint2 r;
+            if constexpr (sizeof(T) == 2) {
+                __nv_bfloat162 lo = __floats2bfloat162_rn(v[4 * k], v[4 * k + 1]);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(v[4 * k + 2], v[4 * k + 3]);
+                r.x = *reinterpret_cast<uint32_t*>(&lo);
+                r.y = *reinterpret_cast<uint32_t*>(&hi);
+            } else {
+                r.x = __float_as_uint(v[2 * k]);
+                r.y = __float_as_uint(v[2 * k + 1]);
+            }
+            p[k] = r;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kBwdTile; ++i)
+            if (i < nv) row[t0 + i] = IO<T>::from_f(v[i]);
+    }
+}
+
+// Delta (natural units) and, with softplus, its derivative sigmoid(s).
+template <bool ACC, bool SP>
+__device__ __forceinline__ float delta_nat(float s) {
+    if constexpr (!SP) return s;
+    else return softplus_f<ACC>(s);
+}
+template <bool ACC>
+__device__ __forceinline__ float sigmoid_f(float s) {
+    if constexpr (ACC) return 1.0f / (1.0f + expf(-s));
+    else return __fdividef(1.0f, 1.0f + ex2_approx(-s * kLog2e));
+}
+template <bool ACC>
+__device__ __forceinline__ float exp_f(float x) {
+    if constexpr (ACC) return expf(x);
+    else return ex2_approx(x * kLog2e);
+}
+
+// Warp unit of both passes: 32 consecutive channels of one batch entry.
+struct WarpUnit {
+    int b, grp, lane;
+    long long d, row;
+    bool ok;
+};
+__device__ __forceinline__ WarpUnit warp_unit(const BwdArgs& a, long long w) {
+    WarpUnit u;
+    u.lane = threadIdx.x & 31;
+    u.b = (int)(w / a.groups);
+    u.grp = (int)(w % a.groups);
+    u.d = (long long)u.grp * 32 + u.lane;
+    u.ok = u.d < a.dim;
+    u.row = (long long)u.b * a.dim + (u.ok ? u.d : 0);
+    return u;
+}
+
+template <typename T, int NP, bool SP>
+__global__ void __launch_bounds__(kCkptThreads)
+bwd_checkpoint_kernel(const BwdArgs a) {
+    constexpr bool ACC = IO<T>::kAccurate;
+    // the tile's B/C rows of each warp of the CTA
+    __shared__ float4 ck_bc[kCkptThreads / 32][kBwdTile * (kMaxN / 2)];
+    const long long w = ((long long)blockIdx.x * kCkptThreads + threadIdx.x) >> 5;
+    if (w >= (long long)a.batch * a.groups) return;   // whole warps leave together
+    float4* sb = ck_bc[threadIdx.x >> 5];
+    const WarpUnit q = warp_unit(a, w);
+    const int N = a.N;
+    const long long L = a.L;
+    float h[NP], Ar[NP];
+#pragma unroll
+    for (int n = 0; n < NP; ++n) {
+        const bool on = q.ok && n < N;
+        Ar[n] = on ? a.A[q.d * N + n] : 0.0f;
+        h[n] = (on && a.h0) ? a.h0[q.row * N + n] : 0.0f;
+    }
+    const float bias = (q.ok && a.dt_bias) ? a.dt_bias[q.d] : 0.0f;
+    const T* ur = static_cast<const T*>(a.u) + q.row * L;
+    const T* dl = static_cast<const T*>(a.delta) + q.row * L;
+    const float4* bcb = a.bc + (long long)q.b * L * (NP / 2);
+    float4* ck = reinterpret_cast<float4*>(a.ckpt + q.row * a.ntiles * NP);
+    for (int k = 0; k < a.ntiles; ++k) {
+        if (q.ok) {
+#pragma unroll
+            for (int j = 0; j < NP / 4; ++j)
+                ck[k * (NP / 4) + j] = make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+        }
+        // every load of the tile issued before the recurrence uses any
+        const long long t0 = (long long)k * kBwdTile;
+        const int nv = (int)min((long long)kBwdTile, L - t0);
+        float uvs[kBwdTile], dvs[kBwdTile];
+        load_tile_row<T>(ur, t0, nv, a.vec8 != 0, q.ok, uvs);
+        load_tile_row<T>(dl, t0, nv, a.vec8 != 0, q.ok, dvs);
+#pragma unroll
+        for (int r = 0; r < (kBwdTile * (NP / 2) + 31) / 32; ++r) {
+            const int e = r * 32 + q.lane;
+            if (e < kBwdTile * (NP / 2)) {
+                const int i = e / (NP / 2);
+                sb[e] = i < nv ? bcb[(t0 + i) * (NP / 2) + (e % (NP / 2))]
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < kBwdTile; ++i) {
+            if (i < nv) {
+                const float dt = delta_nat<ACC, SP>(dvs[i] + bias);
+                const float du = dt * uvs[i];
+#pragma unroll
+                for (int j = 0; j < NP / 2; ++j) {
+                    const float4 p = sb[i * (NP / 2) + j];
+                    h[2 * j] = fmaf(exp_f<ACC>(dt * Ar[2 * j]), h[2 * j], du * p.x);
+                    h[2 * j + 1] = fmaf(exp_f<ACC>(dt * Ar[2 * j + 1]), h[2 * j + 1], du * p.y);
+                }
+            }
+        }
+        __syncwarp();   // the rows are rewritten for the next tile
+    }
+}
+
+// Sum v over the 32 lanes of the warp, NP values at once: at each of the
+// first log2(NP) levels a lane keeps half of its values and sends the other
+// half to its partner, so every value costs one shuffle in all.  On return
+// every lane holds the full sum of v[n] for n = bwd_lane_entry<NP>(lane).
+template <int NP>
+__device__ __forceinline__ int bwd_levels() {
+    return NP == 16 ? 4 : (NP == 8 ? 3 : 2);
+}
+template <int NP>
+__device__ __forceinline__ int bwd_lane_entry(int lane) {
+    constexpr int LV = NP == 16 ? 4 : (NP == 8 ? 3 : 2);
+    int n = 0;
+#pragma unroll
+    for (int lev = 0; lev < LV; ++lev) n += ((lane >> (4 - lev)) & 1) * (NP >> (lev + 1));
+    return n;
+}
+template <int NP>
+__device__ __forceinline__ float warp_sum_transpose(float (&v)[NP], int lane) {
+    constexpr int LV = NP == 16 ? 4 : (NP == 8 ? 3 : 2);
+#pragma unroll
+    for (int lev = 0; lev < LV; ++lev) {
+        const int m = 16 >> lev;
+        const bool upper = (lane & m) != 0;
+        constexpr int kMax = NP / 2;
+#pragma unroll
+        for (int i = 0; i < kMax; ++i) {
+            const int half = NP >> (lev + 1);
+            if (i < half) {
+                const float send = upper ? v[i] : v[i + half];
+                const float keep = upper ? v[i + half] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+            }
+        }
+    }
+    float s = v[0];
+#pragma unroll
+    for (int m = 16 >> LV; m >= 1; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+    return s;
+}
+
+// Shared memory of one warp, per tile: the states h_t (after step t) as
+// [kBwdTile][NP][32]; per step and lane g = dy * silu(z), u, Delta,
+// sigmoid(s) (softplus derivative), dy * silu'(z), dy and the outputs du,
+// ddelta, dz as [9][kBwdTile][32];
+// the packed B/C rows of the tile as [kBwdTile][NP / 2] float4.
+enum { kSG = 0, kSU = 1, kSDT = 2, kSSIG = 3, kSZF = 4, kSDY = 5, kSDU = 6, kSDD = 7, kSDZ = 8,
+       kSRows = 9 };
+template <int NP>
+constexpr int bwd_smem_floats() {
+    return kBwdTile * NP * 32 + kSRows * kBwdTile * 32 + kBwdTile * (NP / 2) * 4;
+}
+
+template <typename T, int NP, bool SP, bool HZ>
+__global__ void __launch_bounds__(32)
+bwd_kernel(const BwdArgs a) {
+    constexpr bool ACC = IO<T>::kAccurate;
+    extern __shared__ __align__(16) float bwd_smem[];
+    float* hist = bwd_smem;
+    float* sv = bwd_smem + kBwdTile * NP * 32;   // [kSRows][kBwdTile][32]
+    float4* sbc = reinterpret_cast<float4*>(sv + kSRows * kBwdTile * 32);   // [kBwdTile][NP/2]
+    auto S = [&](int r, int i) -> float& { return sv[(r * kBwdTile + i) * 32 + threadIdx.x]; };
+    const long long w = blockIdx.x;
+    const WarpUnit q = warp_unit(a, w);
+    const int lane = q.lane, N = a.N;
+    const long long L = a.L;
+
+    float Ar[NP], dh[NP], dA[NP], hs[NP];
+#pragma unroll
+    for (int n = 0; n < NP; ++n) {
+        const bool on = q.ok && n < N;
+        Ar[n] = on ? a.A[q.d * N + n] : 0.0f;
+        dh[n] = (on && a.dfinal) ? a.dfinal[q.row * N + n] : 0.0f;
+        dA[n] = 0.0f;
+    }
+    const float bias = (q.ok && a.dt_bias) ? a.dt_bias[q.d] : 0.0f;
+    const float dsk = (q.ok && a.D_skip) ? a.D_skip[q.d] : 0.0f;
+    float dD = 0.0f, dbias = 0.0f;
+    const T* ur = static_cast<const T*>(a.u) + q.row * L;
+    const T* dl = static_cast<const T*>(a.delta) + q.row * L;
+    const T* zr = HZ ? static_cast<const T*>(a.z) + q.row * L : nullptr;
+    const T* dyr = static_cast<const T*>(a.dy) + q.row * L;
+    T* dur = static_cast<T*>(a.du) + q.row * L;
+    T* ddr = static_cast<T*>(a.ddelta) + q.row * L;
+    T* dzr = HZ ? static_cast<T*>(a.dz) + q.row * L : nullptr;
+    const float4* bcb = a.bc + (long long)q.b * L * (NP / 2);
+    const float4* ck = reinterpret_cast<const float4*>(a.ckpt + q.row * a.ntiles * NP);
+    const int my_n = bwd_lane_entry<NP>(lane);
+    const bool writer = (lane & ((16 >> bwd_levels<NP>()) * 2 - 1)) == 0;
+    float* pBg = a.pB + ((long long)q.grp * a.batch + q.b) * L * NP;
+    float* pCg = a.pC + ((long long)q.grp * a.batch + q.b) * L * NP;
+
+    for (int k = a.ntiles - 1; k >= 0; --k) {
+        const long long t0 = (long long)k * kBwdTile;
+        const int nv = (int)min((long long)kBwdTile, L - t0);
+        // (a) the tile's inputs into shared memory, every load of the tile
+        //     issued before any is used
+        {
+            const bool vec = a.vec8 != 0;
+            float uvs[kBwdTile], dvs[kBwdTile], dys[kBwdTile], zvs[kBwdTile];
+            load_tile_row<T>(ur, t0, nv, vec, q.ok, uvs);
+            load_tile_row<T>(dl, t0, nv, vec, q.ok, dvs);
+            load_tile_row<T>(dyr, t0, nv, vec, q.ok, dys);
+            if constexpr (HZ) load_tile_row<T>(zr, t0, nv, vec, q.ok, zvs);
+#pragma unroll
+            for (int i = 0; i < kBwdTile; ++i) {
+                const bool on = q.ok && i < nv;
+                const float sarg = dvs[i] + bias;
+                S(kSU, i) = uvs[i];
+                S(kSDT, i) = on ? delta_nat<ACC, SP>(sarg) : 0.0f;
+                S(kSSIG, i) = SP ? sigmoid_f<ACC>(sarg) : 1.0f;
+                // the gate's factors do not depend on the state
+                if constexpr (HZ) {
+                    const float zv = zvs[i], sz = sigmoid_f<ACC>(zv);
+                    S(kSG, i) = dys[i] * zv * sz;
+                    S(kSZF, i) = dys[i] * sz * fmaf(zv, 1.0f - sz, 1.0f);
+                } else {
+                    S(kSG, i) = dys[i];
+                }
+                S(kSDY, i) = dys[i];
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < (kBwdTile * (NP / 2) + 31) / 32; ++r) {
+            const int e = r * 32 + lane;        // (step, pair) of the tile
+            if (e < kBwdTile * (NP / 2)) {
+                const int i = e / (NP / 2);
+                sbc[e] = i < nv ? bcb[(t0 + i) * (NP / 2) + (e % (NP / 2))]
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        // the tile's states from its checkpoint (inactive lanes: zeros)
+#pragma unroll
+        for (int j = 0; j < NP / 4; ++j) {
+            const float4 c4 = q.ok ? ck[k * (NP / 4) + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+            hs[4 * j] = c4.x; hs[4 * j + 1] = c4.y; hs[4 * j + 2] = c4.z; hs[4 * j + 3] = c4.w;
+        }
+        __syncwarp();
+        // (b) recompute the tile's states and pre-gate outputs
+        {
+            float h[NP];
+#pragma unroll
+            for (int n = 0; n < NP; ++n) h[n] = hs[n];
+#pragma unroll
+            for (int i = 0; i < kBwdTile; ++i) {
+                if (i >= nv) continue;
+                const float uv = S(kSU, i), dt = S(kSDT, i);
+                const float du = dt * uv;
+                float acc = dsk * uv;
+#pragma unroll
+                for (int j = 0; j < NP / 2; ++j) {
+                    const float4 p = sbc[i * (NP / 2) + j];
+                    h[2 * j] = fmaf(exp_f<ACC>(dt * Ar[2 * j]), h[2 * j], du * p.x);
+                    h[2 * j + 1] = fmaf(exp_f<ACC>(dt * Ar[2 * j + 1]), h[2 * j + 1], du * p.y);
+                    acc = fmaf(p.z, h[2 * j], acc);
+                    acc = fmaf(p.w, h[2 * j + 1], acc);
+                    hist[(i * NP + 2 * j) * 32 + lane] = h[2 * j];
+                    hist[(i * NP + 2 * j + 1) * 32 + lane] = h[2 * j + 1];
+                }
+                if constexpr (HZ) S(kSDZ, i) = S(kSZF, i) * acc;   // dz = dy pre silu'(z)
+                else (void)acc;
+            }
+        }
+        __syncwarp();
+        // (c) backwards through the tile; h_t of step i is h_{t-1} of step
+        //     i + 1, so each state is read from shared memory once
+        float hn[NP];
+#pragma unroll
+        for (int n = 0; n < NP; ++n) hn[n] = nv > 0 ? hist[((nv - 1) * NP + n) * 32 + lane] : 0.0f;
+#pragma unroll
+        for (int i = kBwdTile - 1; i >= 0; --i) {
+            if (i >= nv) continue;
+            const long long t = t0 + i;
+            const float uv = S(kSU, i), dt = S(kSDT, i), g = S(kSG, i);
+            dD = fmaf(g, uv, dD);
+            // four interleaved partial sums shorten the dependent chains
+            float dus[4] = {g * dsk, 0.0f, 0.0f, 0.0f}, dds[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float pb[NP], pc[NP];
+#pragma unroll
+            for (int j = 0; j < NP / 2; ++j) {
+                const float4 p = sbc[i * (NP / 2) + j];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int n = 2 * j + e;
+                    const float Bn = e ? p.y : p.x, Cn = e ? p.w : p.z;
+                    const float ht = hn[n];
+                    const float hp = i > 0 ? hist[((i - 1) * NP + n) * 32 + lane] : hs[n];
+                    hn[n] = hp;
+                    const float abar = exp_f<ACC>(dt * Ar[n]);
+                    dh[n] = fmaf(g, Cn, dh[n]);
+                    pc[n] = g * ht;
+                    const float dhd = dh[n] * dt;
+                    pb[n] = dhd * uv;
+                    dus[n & 3] = fmaf(dhd, Bn, dus[n & 3]);
+                    dds[n & 3] = fmaf(dh[n], fmaf(Ar[n] * abar, hp, Bn * uv), dds[n & 3]);
+                    dA[n] = fmaf(dhd * abar, hp, dA[n]);
+                    dh[n] *= abar;
+                }
+            }
+            const float dut = (dus[0] + dus[1]) + (dus[2] + dus[3]);
+            const float ddel = ((dds[0] + dds[1]) + (dds[2] + dds[3])) * S(kSSIG, i);
+            dbias += ddel;
+            S(kSDU, i) = dut;
+            S(kSDD, i) = ddel;
+            const float sb = warp_sum_transpose<NP>(pb, lane);
+            const float sc = warp_sum_transpose<NP>(pc, lane);
+            if (writer) {
+                pBg[t * NP + my_n] = sb;
+                pCg[t * NP + my_n] = sc;
+            }
+        }
+        if (q.ok) {   // the tile's outputs, one lane per row
+            const bool vec = a.vec8 != 0;
+            float o[kBwdTile];
+#pragma unroll
+            for (int i = 0; i < kBwdTile; ++i) o[i] = S(kSDU, i);
+            store_tile_row<T>(dur, t0, nv, vec, o);
+#pragma unroll
+            for (int i = 0; i < kBwdTile; ++i) o[i] = S(kSDD, i);
+            store_tile_row<T>(ddr, t0, nv, vec, o);
+            if constexpr (HZ) {
+#pragma unroll
+                for (int i = 0; i < kBwdTile; ++i) o[i] = S(kSDZ, i);
+                store_tile_row<T>(dzr, t0, nv, vec, o);
+            }
+        }
+        __syncwarp();   // every read of this tile's states done
+    }
+    if (q.ok) {
+#pragma unroll
+        for (int n = 0; n < NP; ++n) {
+            a.pA[q.row * NP + n] = dA[n];
+            if (a.dh0 && n < N) a.dh0[q.row * N + n] = dh[n];
+        }
+        a.pD[q.row] = dD;
+        a.pbias[q.row] = dbias;
+    }
+}
+
+// dB[b][n][t] (or dC) = sum over channel groups of the partials, in group order.
+__global__ void __launch_bounds__(kReduceThreads)
+bwd_reduce_bc_kernel(const float* __restrict__ part, float* __restrict__ out, int groups,
+                     int batch, long long L, int N, int NP) {
+    const long long total = (long long)batch * L * NP;
+    const long long stride = total;
+    for (long long i = (long long)blockIdx.x * kReduceThreads + threadIdx.x; i < total;
+         i += (long long)gridDim.x * kReduceThreads) {
+        const int n = (int)(i % NP);
+        if (n >= N) continue;
+        const long long bt = i / NP;           // b * L + t
+        const long long b = bt / L, t = bt - b * L;
+        float s = 0.0f;
+        for (int g = 0; g < groups; ++g) s += part[g * stride + i];
+        out[(b * N + n) * L + t] = s;
+    }
+}
+
+// dA[d][n] = sum_b pA, dD[d] = sum_b pD, ddt_bias[d] = sum_b pbias, in batch order.
+__global__ void __launch_bounds__(kReduceThreads)
+bwd_reduce_params_kernel(const float* __restrict__ pA, const float* __restrict__ pD,
+                         const float* __restrict__ pbias, float* __restrict__ dA,
+                         float* __restrict__ dD, float* __restrict__ dbias, int batch,
+                         long long dim, int N, int NP) {
+    const long long total = dim * NP;
+    for (long long i = (long long)blockIdx.x * kReduceThreads + threadIdx.x; i < total;
+         i += (long long)gridDim.x * kReduceThreads) {
+        const long long d = i / NP;
+        const int n = (int)(i % NP);
+        if (n < N) {
+            float s = 0.0f;
+            for (int b = 0; b < batch; ++b) s += pA[((long long)b * dim + d) * NP + n];
+            dA[d * N + n] = s;
+        }
+        if (n == 0) {
+            float sd = 0.0f, sb = 0.0f;
+            for (int b = 0; b < batch; ++b) {
+                sd += pD[(long long)b * dim + d];
+                sb += pbias[(long long)b * dim + d];
+            }
+            if (dD) dD[d] = sd;
+            if (dbias) dbias[d] = sb;
+        }
+    }
+}
+
+template <typename T, int NP, bool SP>
+cudaError_t launch_bwd(const BwdArgs& a, bool hz, cudaStream_t st) {
+    const long long warps = (long long)a.batch * a.groups;
+    {
+        ProfScope prof(kKindBwdCheckpoint, st);
+        const unsigned grid = (unsigned)((warps * 32 + kCkptThreads - 1) / kCkptThreads);
+        bwd_checkpoint_kernel<T, NP, SP><<<grid, kCkptThreads, 0, st>>>(a);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int smem = bwd_smem_floats<NP>() * (int)sizeof(float);
+    auto k = hz ? bwd_kernel<T, NP, SP, true> : bwd_kernel<T, NP, SP, false>;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    {
+        ProfScope prof(kKindBwd, st);
+        k<<<(unsigned)warps, 32, smem, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch_bwd(int np, bool sp, bool hz, const BwdArgs& a, cudaStream_t st) {
+#define X(NP_)                                                                     \
+    if (np == NP_) return sp ? launch_bwd<T, NP_, true>(a, hz, st) : launch_bwd<T, NP_, false>(a, hz, st);
+    X(4) X(8) X(16)
+#undef X
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+}  // namespace mamba
+
+using namespace mamba;
+
+extern "C" {
+
+int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io_dtype,
+                   const void* u, const void* delta, const float* dt_bias, const float* A,
+                   const void* B, const void* C, const float* D_skip, const void* z, int flags,
+                   const float* initial_state, const void* dy, const float* d_final_state,
+                   void* du, void* ddelta, float* dA, float* dB, float* dC, float* dD_skip,
+                   void* dz, float* ddt_bias, float* d_initial_state, cudaStream_t stream) {
+    if (flags & ~MAMBA_FLAG_SOFTPLUS) return MAMBA_ERR_FLAGS;
+    if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
+    if (batch < 1 || dim < 1 || dstate < 1 || dstate > kMaxN || seqlen < 0) return MAMBA_ERR_SHAPE;
+    if (batch > INT32_MAX / 2 || dim > (1ll << 40) || seqlen > (1ll << 40) ||
+        (double)batch * dim * (double)(seqlen > 0 ? seqlen : 1) > 4.0e18)
+        return MAMBA_ERR_SHAPE;
+    if (!A || !dA) return MAMBA_ERR_NULL;
+    if (seqlen > 0 && (!u || !delta || !B || !C || !dy || !du || !ddelta || !dB || !dC))
+        return MAMBA_ERR_NULL;
+    if (z && seqlen > 0 && !dz) return MAMBA_ERR_NULL;
+    const int es = esize(io_dtype);
+    const size_t big = (size_t)(batch * dim * seqlen) * es;
+    const size_t bcb = (size_t)(batch * dstate * seqlen) * es;
+    const size_t bcf = (size_t)(batch * dstate * seqlen) * 4;
+    const size_t stb = (size_t)(batch * dim * dstate) * 4;
+    const size_t ab = (size_t)(dim * dstate) * 4, vb = (size_t)dim * 4;
+    for (const void* q : {u, delta, z, dy, B, C, (const void*)du, (const void*)ddelta,
+                          (const void*)dz})
+        if (q && !aligned(q, es)) return MAMBA_ERR_ALIGN;
+    for (const void* q : {(const void*)dt_bias, (const void*)A, (const void*)D_skip,
+                          (const void*)initial_state, (const void*)d_final_state, (const void*)dA,
+                          (const void*)dB, (const void*)dC, (const void*)dD_skip,
+                          (const void*)ddt_bias, (const void*)d_initial_state})
+        if (q && !aligned(q, 4)) return MAMBA_ERR_ALIGN;
+    {
+        const void* ins[] = {u, delta, z, dy, B, C, dt_bias, A, D_skip, initial_state,
+                             d_final_state};
+        const size_t insz[] = {big, big, big, big, bcb, bcb, vb, ab, vb, stb, stb};
+        void* outs[] = {du, ddelta, dz, dA, dB, dC, dD_skip, ddt_bias, d_initial_state};
+        const size_t outsz[] = {big, big, big, ab, bcf, bcf, vb, vb, stb};
+        for (int o = 0; o < 9; ++o) {
+            for (int i = 0; i < 11; ++i)
+                if (overlaps(outs[o], outsz[o], ins[i], insz[i])) return MAMBA_ERR_ALIAS;
+            for (int p = o + 1; p < 9; ++p)
+                if (overlaps(outs[o], outsz[o], outs[p], outsz[p])) return MAMBA_ERR_ALIAS;
+        }
+    }
+    const bool sp = (flags & MAMBA_FLAG_SOFTPLUS) != 0;
+    if (seqlen == 0) {
+        // no steps: only the initial state reaches the final state
+        cudaError_t e = cudaMemsetAsync(dA, 0, ab, stream);
+        if (e == cudaSuccess && dD_skip) e = cudaMemsetAsync(dD_skip, 0, vb, stream);
+        if (e == cudaSuccess && ddt_bias) e = cudaMemsetAsync(ddt_bias, 0, vb, stream);
+        if (e == cudaSuccess && d_initial_state)
+            e = d_final_state ? cudaMemcpyAsync(d_initial_state, d_final_state, stb,
+                                                cudaMemcpyDeviceToDevice, stream)
+                              : cudaMemsetAsync(d_initial_state, 0, stb, stream);
+        return e == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
+    }
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MAMBA_ERR_CUDA;
+    const int np = dstate <= 4 ? 4 : (dstate <= 8 ? 8 : 16);
+    const int groups = (int)((dim + 31) / 32);
+    const int ntiles = (int)((seqlen + kBwdTile - 1) / kBwdTile);
+    const size_t rows = (size_t)(batch * dim);
+    const size_t sz_bc = (size_t)batch * seqlen * (np / 2) * sizeof(float4);
+    const size_t sz_ck = rows * ntiles * np * sizeof(float);
+    const size_t sz_p = (size_t)groups * batch * seqlen * np * sizeof(float);
+    const size_t sz_a = rows * np * sizeof(float);
+    const size_t sz_r = rows * sizeof(float);
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t total = up(sz_bc) + up(sz_ck) + 2 * up(sz_p) + up(sz_a) + 2 * up(sz_r);
+    cudaMemPool_t pool = nullptr;
+    int rc = get_pool(dev, &pool);
+    if (rc != MAMBA_OK) return rc;
+    void* scratch = nullptr;
+    if (cudaMallocFromPoolAsync(&scratch, total, pool, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MAMBA_ERR_ALLOC;
+    }
+    char* p = static_cast<char*>(scratch);
+    BwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.bc = reinterpret_cast<const float4*>(p); p += up(sz_bc);
+    a.ckpt = reinterpret_cast<float*>(p); p += up(sz_ck);
+    a.pB = reinterpret_cast<float*>(p); p += up(sz_p);
+    a.pC = reinterpret_cast<float*>(p); p += up(sz_p);
+    a.pA = reinterpret_cast<float*>(p); p += up(sz_a);
+    a.pD = reinterpret_cast<float*>(p); p += up(sz_r);
+    a.pbias = reinterpret_cast<float*>(p);
+    a.u = u; a.delta = delta; a.z = z; a.dy = dy;
+    a.dt_bias = dt_bias; a.A = A; a.D_skip = D_skip;
+    a.h0 = initial_state; a.dfinal = d_final_state;
+    a.du = du; a.ddelta = ddelta; a.dz = dz; a.dh0 = d_initial_state;
+    a.dim = dim; a.L = seqlen; a.batch = (int)batch; a.N = (int)dstate;
+    a.groups = groups; a.ntiles = ntiles;
+    a.vec8 = ((seqlen * es) % 8) == 0;
+    for (const void* q : {u, delta, z, dy, (const void*)du, (const void*)ddelta, (const void*)dz})
+        if (q && !aligned(q, 8)) a.vec8 = 0;
+
+    cudaError_t e = launch_pack_bc(io_dtype, B, C, const_cast<float4*>(a.bc), batch, seqlen,
+                                   (int)dstate, np, 1.0f, stream);
+    if (e == cudaSuccess)
+        e = io_dtype == MAMBA_BF16 ? dispatch_bwd<__nv_bfloat16>(np, sp, z != nullptr, a, stream)
+                                   : dispatch_bwd<float>(np, sp, z != nullptr, a, stream);
+    if (e == cudaSuccess) {
+        ProfScope prof(kKindBwdReduce, stream);
+        const int cap = 16 * sm_count(dev);
+        const long long nbc = (long long)batch * seqlen * np;
+        const int g1 = (int)std::max<long long>(1, std::min<long long>((nbc + kReduceThreads - 1) / kReduceThreads, cap));
+        bwd_reduce_bc_kernel<<<g1, kReduceThreads, 0, stream>>>(a.pB, dB, groups, (int)batch,
+                                                                seqlen, (int)dstate, np);
+        bwd_reduce_bc_kernel<<<g1, kReduceThreads, 0, stream>>>(a.pC, dC, groups, (int)batch,
+                                                                seqlen, (int)dstate, np);
+        const long long npar = dim * np;
+        const int g2 = (int)std::max<long long>(1, std::min<long long>((npar + kReduceThreads - 1) / kReduceThreads, cap));
+        bwd_reduce_params_kernel<<<g2, kReduceThreads, 0, stream>>>(
+            a.pA, a.pD, a.pbias, dA, dD_skip, ddt_bias, (int)batch, dim, (int)dstate, np);
+        e = cudaGetLastError();
+    }
+    cudaFreeAsync(scratch, stream);
+    return e == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,139 @@
+// Shared by the forward (mamba_scan.cu) and backward (mamba_scan_bwd.cu)
+// translation units of libmamba_scan.so: element conversions, the hardware
+// ex2/lg2/tanh paths, softplus and silu, argument checks, and the host-side
+// services the forward file defines once (B/C packing, the scratch pool, the
+// SM count, per-launch timing).
+#pragma once
+
+#include "mamba_scan.h"
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstddef>
+#include <cstdint>
+
+namespace mamba {
+
+constexpr int kMaxN = 16;   // largest dstate
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+
+template <typename T> struct IO;
+template <> struct IO<float> {
+    static constexpr bool kAccurate = true;
+    __device__ static void unpack(const uint4& r, float* v) {
+        v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
+        v[2] = __uint_as_float(r.z); v[3] = __uint_as_float(r.w);
+    }
+    __device__ static uint4 pack(const float* v) {
+        return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                          __float_as_uint(v[2]), __float_as_uint(v[3]));
+    }
+    __device__ static float to_f(float x) { return x; }
+    __device__ static float from_f(float x) { return x; }
+};
+template <> struct IO<__nv_bfloat16> {
+    static constexpr bool kAccurate = false;
+    __device__ static void unpack(const uint4& r, float* v) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    __device__ static uint4 pack(const float* v) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t*>(&p);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __device__ static float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+    __device__ static __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// softplus(s) = log(1 + e^s); for s > 20 it equals s to within e^-20.
+template <bool ACC>
+__device__ __forceinline__ float softplus_f(float s) {
+    float r;
+    if (ACC) {
+        r = log1pf(expf(s));
+    } else {
+        r = lg2_approx(1.0f + ex2_approx(s * kLog2e)) * kLn2;
+    }
+    return s > 20.0f ? s : r;
+}
+
+// silu(z) = z * sigmoid(z).  Accurate path: z / (1 + e^-z).  Fast path:
+// sigmoid(z) = (1 + tanh(z/2)) / 2, so silu(z) = h + h * tanh(h) with h = z/2,
+// one hardware tanh (max relative error about 2^-11).
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+template <bool ACC>
+__device__ __forceinline__ float silu_f(float z) {
+    if (ACC) return z / (1.0f + expf(-z));
+    const float h = 0.5f * z;
+    return fmaf(h, tanh_approx(h), h);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+inline int esize(int dt) { return dt == MAMBA_BF16 ? 2 : 4; }
+
+inline bool aligned(const void* p, size_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// Kinds of launch timed by mamba_profile_begin/end.
+enum LaunchKind {
+    kKindScan = 0, kKindSummary = 1, kKindCarry = 2, kKindStep = 3, kKindPack = 4,
+    kKindBwdCheckpoint = 5, kKindBwd = 6, kKindBwdReduce = 7, kKinds = 8
+};
+
+// While timing is on, brackets the launches of its scope with CUDA events
+// on `s` (defined in mamba_scan.cu).
+struct ProfScope {
+    cudaEvent_t stop = nullptr;
+    cudaStream_t st;
+    ProfScope(int kind, cudaStream_t s);
+    ~ProfScope();
+};
+
+int sm_count(int dev);
+// The library's stream-ordered pool of the device (MAMBA_OK or an error).
+int get_pool(int dev, cudaMemPool_t* out);
+// B and C (batch, N, L) in io_dtype -> fp32 rows of NP/2 float4 (s*B pair,
+// C pair) per (batch, step), entries n >= N zero.
+cudaError_t launch_pack_bc(int io_dtype, const void* B, const void* C, float4* out,
+                           long long batch, long long L, int N, int NP, float scale,
+                           cudaStream_t stream);
+
+}  // namespace mamba

@@ -172,6 +172,32 @@ def test_state_update_validation(lib):
     assert step_call(lib, x=1) == EALIAS       # state overlaps x
 
 
+def bwd_call(lib, flags=SOFTPLUS, dstate=16, extra=None, **over):
+    names = ("u", "delta", "dtb", "A", "B", "C", "Dk", "z", "h0", "dy", "dfin", "du", "ddelta",
+             "dA", "dB", "dC", "dD", "dz", "dbias", "dh0")
+    v = {k: addr(i, (extra or {}).get(k, 0)) for i, k in enumerate(names, 1)}
+    v.update(over)
+    return lib.mamba_scan_bwd(2, 16, dstate, 64, 1, v["u"], v["delta"], v["dtb"], v["A"], v["B"],
+                              v["C"], v["Dk"], v["z"], flags, v["h0"], v["dy"], v["dfin"],
+                              v["du"], v["ddelta"], v["dA"], v["dB"], v["dC"], v["dD"], v["dz"],
+                              v["dbias"], v["dh0"], None)
+
+
+def test_scan_bwd_validation(lib):
+    # every case is rejected on the host, before any CUDA call
+    assert bwd_call(lib, flags=ZOH) == EFLAGS
+    assert bwd_call(lib, flags=SOFTPLUS | NOALLOC) == EFLAGS
+    assert bwd_call(lib, dstate=17) == ESHAPE
+    for k in ("u", "delta", "A", "B", "C", "dy", "du", "ddelta", "dA", "dB", "dC"):
+        assert bwd_call(lib, **{k: None}) == ENULL, k
+    assert bwd_call(lib, dz=None) == ENULL            # z given without dz
+    assert bwd_call(lib, extra={"du": 1}) == EALIGN
+    assert bwd_call(lib, extra={"dA": 2}) == EALIGN
+    assert bwd_call(lib, du=addr(1)) == EALIAS        # du on top of u
+    assert bwd_call(lib, dB=addr(14)) == EALIAS       # dB on top of dA
+    assert bwd_call(lib, dh0=addr(9)) == EALIAS       # d_initial_state on top of initial_state
+
+
 def test_state_update_ex_flags(lib):
     def call(flags, **kw):
         v = {k: addr(i) for i, k in enumerate(("state", "x", "delta", "dtb", "A", "B", "C",
