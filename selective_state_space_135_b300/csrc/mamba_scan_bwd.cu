@@ -30,8 +30,8 @@
 namespace mamba {
 namespace {
 
-constexpr int kBwdTile = 12;        // steps between checkpoints = reverse tile (35 KB of
-                                    // shared memory per warp at dstate 16: six per SM)
+constexpr int kBwdTile = 12;        // steps between checkpoints = reverse tile (42 KB of
+                                    // shared memory per two-warp CTA at dstate 16: five per SM)
 constexpr int kCkptThreads = 128;   // checkpoint pass: four independent warps per CTA
 constexpr int kReduceThreads = 256;
 
@@ -150,60 +150,84 @@ __device__ __forceinline__ WarpUnit warp_unit(const BwdArgs& a, long long w) {
     return u;
 }
 
+// State entries of a unit are split over kBwdSplit warps (their recurrences
+// are independent); warp w of a unit holds entries [w * NPW, (w + 1) * NPW).
+constexpr int kBwdSplit = 2;
+
 template <typename T, int NP, bool SP>
 __global__ void __launch_bounds__(kCkptThreads)
 bwd_checkpoint_kernel(const BwdArgs a) {
     constexpr bool ACC = IO<T>::kAccurate;
-    // the tile's B/C rows of each warp of the CTA
-    __shared__ float4 ck_bc[kCkptThreads / 32][kBwdTile * (kMaxN / 2)];
-    const long long w = ((long long)blockIdx.x * kCkptThreads + threadIdx.x) >> 5;
-    if (w >= (long long)a.batch * a.groups) return;   // whole warps leave together
-    float4* sb = ck_bc[threadIdx.x >> 5];
-    const WarpUnit q = warp_unit(a, w);
-    const int N = a.N;
+    constexpr int NPW = NP / kBwdSplit;
+    // the tile's B/C rows of this warp's state entries, per warp of the CTA
+    __shared__ float4 ck_bc[kCkptThreads / 32][kBwdTile * (kMaxN / 2 / kBwdSplit)];
+    const long long gw = ((long long)blockIdx.x * kCkptThreads + threadIdx.x) >> 5;
+    if (gw >= (long long)a.batch * a.groups * kBwdSplit) return;   // whole warps leave together
+    const int half = (int)(gw % kBwdSplit);
+    const WarpUnit q = warp_unit(a, gw / kBwdSplit);
+    const int N = a.N, n0 = half * NPW;
     const long long L = a.L;
-    float h[NP], Ar[NP];
+    float4* sb = ck_bc[threadIdx.x >> 5];
+    float h[NPW], Ar[NPW];
 #pragma unroll
-    for (int n = 0; n < NP; ++n) {
-        const bool on = q.ok && n < N;
-        Ar[n] = on ? a.A[q.d * N + n] : 0.0f;
-        h[n] = (on && a.h0) ? a.h0[q.row * N + n] : 0.0f;
+    for (int n = 0; n < NPW; ++n) {
+        const bool on = q.ok && n0 + n < N;
+        Ar[n] = on ? a.A[q.d * N + n0 + n] : 0.0f;
+        h[n] = (on && a.h0) ? a.h0[q.row * N + n0 + n] : 0.0f;
     }
     const float bias = (q.ok && a.dt_bias) ? a.dt_bias[q.d] : 0.0f;
     const T* ur = static_cast<const T*>(a.u) + q.row * L;
     const T* dl = static_cast<const T*>(a.delta) + q.row * L;
-    const float4* bcb = a.bc + (long long)q.b * L * (NP / 2);
-    float4* ck = reinterpret_cast<float4*>(a.ckpt + q.row * a.ntiles * NP);
-    for (int k = 0; k < a.ntiles; ++k) {
-        if (q.ok) {
-#pragma unroll
-            for (int j = 0; j < NP / 4; ++j)
-                ck[k * (NP / 4) + j] = make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-        }
-        // every load of the tile issued before the recurrence uses any
-        const long long t0 = (long long)k * kBwdTile;
+    const float4* bcb = a.bc + (long long)q.b * L * (NP / 2) + n0 / 2;
+    float2* ck = reinterpret_cast<float2*>(a.ckpt + q.row * a.ntiles * NP + n0);
+    // tile k + 1's loads are issued before tile k's recurrence (registers:
+    // u, delta and this lane's share of the B/C rows)
+    constexpr int kRowsPerLane = (kBwdTile * (NPW / 2) + 31) / 32;
+    float uvs[kBwdTile], dvs[kBwdTile];
+    float4 bcr[kRowsPerLane];
+    auto fetch = [&](int kk) {
+        const long long t0 = (long long)kk * kBwdTile;
         const int nv = (int)min((long long)kBwdTile, L - t0);
-        float uvs[kBwdTile], dvs[kBwdTile];
         load_tile_row<T>(ur, t0, nv, a.vec8 != 0, q.ok, uvs);
         load_tile_row<T>(dl, t0, nv, a.vec8 != 0, q.ok, dvs);
 #pragma unroll
-        for (int r = 0; r < (kBwdTile * (NP / 2) + 31) / 32; ++r) {
+        for (int r = 0; r < kRowsPerLane; ++r) {
             const int e = r * 32 + q.lane;
-            if (e < kBwdTile * (NP / 2)) {
-                const int i = e / (NP / 2);
-                sb[e] = i < nv ? bcb[(t0 + i) * (NP / 2) + (e % (NP / 2))]
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            const int i = e / (NPW / 2);
+            bcr[r] = (e < kBwdTile * (NPW / 2) && i < nv)
+                         ? bcb[(t0 + i) * (NP / 2) + (e % (NPW / 2))]
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+    };
+    if (a.ntiles > 0) fetch(0);
+    for (int k = 0; k < a.ntiles; ++k) {
+        if (q.ok) {
+#pragma unroll
+            for (int j = 0; j < NPW / 2; ++j) ck[k * (NP / 2) + j] = make_float2(h[2 * j], h[2 * j + 1]);
+        }
+        const long long t0 = (long long)k * kBwdTile;
+        const int nv = (int)min((long long)kBwdTile, L - t0);
+        float uc[kBwdTile], dc[kBwdTile];
+#pragma unroll
+        for (int i = 0; i < kBwdTile; ++i) {
+            uc[i] = uvs[i];
+            dc[i] = dvs[i];
+        }
+#pragma unroll
+        for (int r = 0; r < kRowsPerLane; ++r) {
+            const int e = r * 32 + q.lane;
+            if (e < kBwdTile * (NPW / 2)) sb[e] = bcr[r];
+        }
+        if (k + 1 < a.ntiles) fetch(k + 1);
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < kBwdTile; ++i) {
             if (i < nv) {
-                const float dt = delta_nat<ACC, SP>(dvs[i] + bias);
-                const float du = dt * uvs[i];
+                const float dt = delta_nat<ACC, SP>(dc[i] + bias);
+                const float du = dt * uc[i];
 #pragma unroll
-                for (int j = 0; j < NP / 2; ++j) {
-                    const float4 p = sb[i * (NP / 2) + j];
+                for (int j = 0; j < NPW / 2; ++j) {
+                    const float4 p = sb[i * (NPW / 2) + j];
                     h[2 * j] = fmaf(exp_f<ACC>(dt * Ar[2 * j]), h[2 * j], du * p.x);
                     h[2 * j + 1] = fmaf(exp_f<ACC>(dt * Ar[2 * j + 1]), h[2 * j + 1], du * p.y);
                 }
@@ -213,33 +237,32 @@ bwd_checkpoint_kernel(const BwdArgs a) {
     }
 }
 
-// Sum v over the 32 lanes of the warp, NP values at once: at each of the
-// first log2(NP) levels a lane keeps half of its values and sends the other
+// Sum v over the 32 lanes of the warp, NV values at once: at each of the
+// first log2(NV) levels a lane keeps half of its values and sends the other
 // half to its partner, so every value costs one shuffle in all.  On return
-// every lane holds the full sum of v[n] for n = bwd_lane_entry<NP>(lane).
-template <int NP>
-__device__ __forceinline__ int bwd_levels() {
-    return NP == 16 ? 4 : (NP == 8 ? 3 : 2);
+// every lane holds the full sum of v[n] for n = bwd_lane_entry<NV>(lane).
+template <int NV>
+__host__ __device__ constexpr int bwd_levels() {
+    return NV == 16 ? 4 : (NV == 8 ? 3 : (NV == 4 ? 2 : 1));
 }
-template <int NP>
+template <int NV>
 __device__ __forceinline__ int bwd_lane_entry(int lane) {
-    constexpr int LV = NP == 16 ? 4 : (NP == 8 ? 3 : 2);
+    constexpr int LV = bwd_levels<NV>();
     int n = 0;
 #pragma unroll
-    for (int lev = 0; lev < LV; ++lev) n += ((lane >> (4 - lev)) & 1) * (NP >> (lev + 1));
+    for (int lev = 0; lev < LV; ++lev) n += ((lane >> (4 - lev)) & 1) * (NV >> (lev + 1));
     return n;
 }
-template <int NP>
-__device__ __forceinline__ float warp_sum_transpose(float (&v)[NP], int lane) {
-    constexpr int LV = NP == 16 ? 4 : (NP == 8 ? 3 : 2);
+template <int NV>
+__device__ __forceinline__ float warp_sum_transpose(float (&v)[NV], int lane) {
+    constexpr int LV = bwd_levels<NV>();
 #pragma unroll
     for (int lev = 0; lev < LV; ++lev) {
         const int m = 16 >> lev;
         const bool upper = (lane & m) != 0;
-        constexpr int kMax = NP / 2;
 #pragma unroll
-        for (int i = 0; i < kMax; ++i) {
-            const int half = NP >> (lev + 1);
+        for (int i = 0; i < NV / 2; ++i) {
+            const int half = NV >> (lev + 1);
             if (i < half) {
                 const float send = upper ? v[i] : v[i + half];
                 const float keep = upper ? v[i + half] : v[i];
@@ -253,38 +276,46 @@ __device__ __forceinline__ float warp_sum_transpose(float (&v)[NP], int lane) {
     return s;
 }
 
-// Shared memory of one warp, per tile: the states h_t (after step t) as
-// [kBwdTile][NP][32]; per step and lane g = dy * silu(z), u, Delta,
-// sigmoid(s) (softplus derivative), dy * silu'(z), dy and the outputs du,
-// ddelta, dz as [9][kBwdTile][32];
-// the packed B/C rows of the tile as [kBwdTile][NP / 2] float4.
-enum { kSG = 0, kSU = 1, kSDT = 2, kSSIG = 3, kSZF = 4, kSDY = 5, kSDU = 6, kSDD = 7, kSDZ = 8,
-       kSRows = 9 };
+// Shared memory of one CTA (kBwdSplit warps, one unit), per tile:
+//   hist  [warp][kBwdTile][NPW][32]   the warp's states h_t (after step t)
+//   rows  [kSRows][kBwdTile][32]      per step and lane: g = dy silu(z), u,
+//                                     Delta, sigmoid(s), dy silu'(z)
+//   parts [warp][3][kBwdTile][32]     the warp's partial sums over its
+//                                     entries: C.h, du, dDelta
+//   bc    [kBwdTile][NP / 2] float4   the tile's packed B/C rows
+enum { kSG = 0, kSU = 1, kSDT = 2, kSSIG = 3, kSZF = 4, kSRows = 5 };
+enum { kPY = 0, kPDU = 1, kPDD = 2, kPRows = 3 };
 template <int NP>
-constexpr int bwd_smem_floats() {
-    return kBwdTile * NP * 32 + kSRows * kBwdTile * 32 + kBwdTile * (NP / 2) * 4;
+__host__ __device__ constexpr int bwd_smem_floats() {
+    return kBwdTile * NP * 32 + kSRows * kBwdTile * 32 + kBwdSplit * kPRows * kBwdTile * 32 +
+           kBwdTile * (NP / 2) * 4;
 }
 
 template <typename T, int NP, bool SP, bool HZ>
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(32 * kBwdSplit)
 bwd_kernel(const BwdArgs a) {
     constexpr bool ACC = IO<T>::kAccurate;
+    constexpr int NPW = NP / kBwdSplit;
     extern __shared__ __align__(16) float bwd_smem[];
-    float* hist = bwd_smem;
-    float* sv = bwd_smem + kBwdTile * NP * 32;   // [kSRows][kBwdTile][32]
-    float4* sbc = reinterpret_cast<float4*>(sv + kSRows * kBwdTile * 32);   // [kBwdTile][NP/2]
-    auto S = [&](int r, int i) -> float& { return sv[(r * kBwdTile + i) * 32 + threadIdx.x]; };
-    const long long w = blockIdx.x;
-    const WarpUnit q = warp_unit(a, w);
-    const int lane = q.lane, N = a.N;
+    const int warp = threadIdx.x >> 5;
+    float* hist = bwd_smem + warp * (kBwdTile * NPW * 32);
+    float* rows = bwd_smem + kBwdTile * NP * 32;
+    float* parts = rows + kSRows * kBwdTile * 32;
+    float4* sbc = reinterpret_cast<float4*>(parts + kBwdSplit * kPRows * kBwdTile * 32);
+    const WarpUnit q = warp_unit(a, blockIdx.x);
+    const int lane = q.lane, N = a.N, n0 = warp * NPW;
     const long long L = a.L;
+    auto S = [&](int r, int i) -> float& { return rows[(r * kBwdTile + i) * 32 + lane]; };
+    auto P = [&](int w, int r, int i) -> float& {
+        return parts[((w * kPRows + r) * kBwdTile + i) * 32 + lane];
+    };
 
-    float Ar[NP], dh[NP], dA[NP], hs[NP];
+    float Ar[NPW], dh[NPW], dA[NPW], hs[NPW];
 #pragma unroll
-    for (int n = 0; n < NP; ++n) {
-        const bool on = q.ok && n < N;
-        Ar[n] = on ? a.A[q.d * N + n] : 0.0f;
-        dh[n] = (on && a.dfinal) ? a.dfinal[q.row * N + n] : 0.0f;
+    for (int n = 0; n < NPW; ++n) {
+        const bool on = q.ok && n0 + n < N;
+        Ar[n] = on ? a.A[q.d * N + n0 + n] : 0.0f;
+        dh[n] = (on && a.dfinal) ? a.dfinal[q.row * N + n0 + n] : 0.0f;
         dA[n] = 0.0f;
     }
     const float bias = (q.ok && a.dt_bias) ? a.dt_bias[q.d] : 0.0f;
@@ -298,156 +329,196 @@ bwd_kernel(const BwdArgs a) {
     T* ddr = static_cast<T*>(a.ddelta) + q.row * L;
     T* dzr = HZ ? static_cast<T*>(a.dz) + q.row * L : nullptr;
     const float4* bcb = a.bc + (long long)q.b * L * (NP / 2);
-    const float4* ck = reinterpret_cast<const float4*>(a.ckpt + q.row * a.ntiles * NP);
-    const int my_n = bwd_lane_entry<NP>(lane);
-    const bool writer = (lane & ((16 >> bwd_levels<NP>()) * 2 - 1)) == 0;
+    const float2* ck = reinterpret_cast<const float2*>(a.ckpt + q.row * a.ntiles * NP + n0);
+    const int my_n = n0 + bwd_lane_entry<NPW>(lane);
+    const bool writer = (lane & ((16 >> bwd_levels<NPW>()) * 2 - 1)) == 0;
     float* pBg = a.pB + ((long long)q.grp * a.batch + q.b) * L * NP;
     float* pCg = a.pC + ((long long)q.grp * a.batch + q.b) * L * NP;
+    const bool vec = a.vec8 != 0;
+
+    // Tile k - 1's global loads are issued before tile k's work: per warp two
+    // input rows (warp 0: u, delta; warp 1: dy, z), each thread's share of
+    // the B/C rows, and the warp's checkpoint, held in registers.
+    constexpr int kRowsPerThread = (kBwdTile * (NP / 2) + 32 * kBwdSplit - 1) / (32 * kBwdSplit);
+    float r1[kBwdTile], r2[kBwdTile];
+    float4 bcr[kRowsPerThread];
+    float2 ckr[NPW / 2];
+    auto fetch = [&](int kk) {
+        const long long t0 = (long long)kk * kBwdTile;
+        const int nv = (int)min((long long)kBwdTile, L - t0);
+        if (warp == 0) {
+            load_tile_row<T>(ur, t0, nv, vec, q.ok, r1);
+            load_tile_row<T>(dl, t0, nv, vec, q.ok, r2);
+        } else {
+            load_tile_row<T>(dyr, t0, nv, vec, q.ok, r1);
+            if constexpr (HZ) load_tile_row<T>(zr, t0, nv, vec, q.ok, r2);
+        }
+#pragma unroll
+        for (int r = 0; r < kRowsPerThread; ++r) {
+            const int e = r * 32 * kBwdSplit + threadIdx.x;
+            const int i = e / (NP / 2);
+            bcr[r] = (e < kBwdTile * (NP / 2) && i < nv)
+                         ? bcb[(t0 + i) * (NP / 2) + (e % (NP / 2))]
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < NPW / 2; ++j)
+            ckr[j] = q.ok ? ck[kk * (NP / 2) + j] : make_float2(0.f, 0.f);
+    };
+    if (a.ntiles > 0) fetch(a.ntiles - 1);
 
     for (int k = a.ntiles - 1; k >= 0; --k) {
         const long long t0 = (long long)k * kBwdTile;
         const int nv = (int)min((long long)kBwdTile, L - t0);
-        // (a) the tile's inputs into shared memory, every load of the tile
-        //     issued before any is used
-        {
-            const bool vec = a.vec8 != 0;
-            float uvs[kBwdTile], dvs[kBwdTile], dys[kBwdTile], zvs[kBwdTile];
-            load_tile_row<T>(ur, t0, nv, vec, q.ok, uvs);
-            load_tile_row<T>(dl, t0, nv, vec, q.ok, dvs);
-            load_tile_row<T>(dyr, t0, nv, vec, q.ok, dys);
-            if constexpr (HZ) load_tile_row<T>(zr, t0, nv, vec, q.ok, zvs);
+        // (a) the tile's per-step inputs, B/C rows and checkpoint from the
+        //     registers into shared memory, then the next loads
+        if (warp == 0) {
 #pragma unroll
             for (int i = 0; i < kBwdTile; ++i) {
-                const bool on = q.ok && i < nv;
-                const float sarg = dvs[i] + bias;
-                S(kSU, i) = uvs[i];
-                S(kSDT, i) = on ? delta_nat<ACC, SP>(sarg) : 0.0f;
+                const float sarg = r2[i] + bias;
+                S(kSU, i) = r1[i];
+                S(kSDT, i) = (q.ok && i < nv) ? delta_nat<ACC, SP>(sarg) : 0.0f;
                 S(kSSIG, i) = SP ? sigmoid_f<ACC>(sarg) : 1.0f;
-                // the gate's factors do not depend on the state
-                if constexpr (HZ) {
-                    const float zv = zvs[i], sz = sigmoid_f<ACC>(zv);
-                    S(kSG, i) = dys[i] * zv * sz;
-                    S(kSZF, i) = dys[i] * sz * fmaf(zv, 1.0f - sz, 1.0f);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kBwdTile; ++i) {
+                if constexpr (HZ) {   // the gate's factors do not depend on the state
+                    const float zv = r2[i], sz = sigmoid_f<ACC>(zv);
+                    S(kSG, i) = r1[i] * zv * sz;
+                    S(kSZF, i) = r1[i] * sz * fmaf(zv, 1.0f - sz, 1.0f);
                 } else {
-                    S(kSG, i) = dys[i];
+                    S(kSG, i) = r1[i];
                 }
-                S(kSDY, i) = dys[i];
             }
         }
 #pragma unroll
-        for (int r = 0; r < (kBwdTile * (NP / 2) + 31) / 32; ++r) {
-            const int e = r * 32 + lane;        // (step, pair) of the tile
-            if (e < kBwdTile * (NP / 2)) {
-                const int i = e / (NP / 2);
-                sbc[e] = i < nv ? bcb[(t0 + i) * (NP / 2) + (e % (NP / 2))]
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+        for (int r = 0; r < kRowsPerThread; ++r) {
+            const int e = r * 32 * kBwdSplit + threadIdx.x;
+            if (e < kBwdTile * (NP / 2)) sbc[e] = bcr[r];
         }
-        // the tile's states from its checkpoint (inactive lanes: zeros)
 #pragma unroll
-        for (int j = 0; j < NP / 4; ++j) {
-            const float4 c4 = q.ok ? ck[k * (NP / 4) + j] : make_float4(0.f, 0.f, 0.f, 0.f);
-            hs[4 * j] = c4.x; hs[4 * j + 1] = c4.y; hs[4 * j + 2] = c4.z; hs[4 * j + 3] = c4.w;
+        for (int j = 0; j < NPW / 2; ++j) {
+            hs[2 * j] = ckr[j].x;
+            hs[2 * j + 1] = ckr[j].y;
         }
-        __syncwarp();
-        // (b) recompute the tile's states and pre-gate outputs
+        if (k > 0) fetch(k - 1);
+        __syncthreads();
+        // (b) recompute this warp's states and its part of C.h (+ D u)
         {
-            float h[NP];
+            float h[NPW];
 #pragma unroll
-            for (int n = 0; n < NP; ++n) h[n] = hs[n];
+            for (int n = 0; n < NPW; ++n) h[n] = hs[n];
 #pragma unroll
             for (int i = 0; i < kBwdTile; ++i) {
                 if (i >= nv) continue;
                 const float uv = S(kSU, i), dt = S(kSDT, i);
                 const float du = dt * uv;
-                float acc = dsk * uv;
+                float acc = warp == 0 ? dsk * uv : 0.0f;
 #pragma unroll
-                for (int j = 0; j < NP / 2; ++j) {
-                    const float4 p = sbc[i * (NP / 2) + j];
+                for (int j = 0; j < NPW / 2; ++j) {
+                    const float4 p = sbc[i * (NP / 2) + n0 / 2 + j];
                     h[2 * j] = fmaf(exp_f<ACC>(dt * Ar[2 * j]), h[2 * j], du * p.x);
                     h[2 * j + 1] = fmaf(exp_f<ACC>(dt * Ar[2 * j + 1]), h[2 * j + 1], du * p.y);
                     acc = fmaf(p.z, h[2 * j], acc);
                     acc = fmaf(p.w, h[2 * j + 1], acc);
-                    hist[(i * NP + 2 * j) * 32 + lane] = h[2 * j];
-                    hist[(i * NP + 2 * j + 1) * 32 + lane] = h[2 * j + 1];
+                    hist[(i * NPW + 2 * j) * 32 + lane] = h[2 * j];
+                    hist[(i * NPW + 2 * j + 1) * 32 + lane] = h[2 * j + 1];
                 }
-                if constexpr (HZ) S(kSDZ, i) = S(kSZF, i) * acc;   // dz = dy pre silu'(z)
-                else (void)acc;
+                P(warp, kPY, i) = acc;
             }
         }
         __syncwarp();
-        // (c) backwards through the tile; h_t of step i is h_{t-1} of step
-        //     i + 1, so each state is read from shared memory once
-        float hn[NP];
+        // (c) backwards through the tile for this warp's entries; h_t of
+        //     step i is h_{t-1} of step i + 1, so each state is read once
+        float hn[NPW];
 #pragma unroll
-        for (int n = 0; n < NP; ++n) hn[n] = nv > 0 ? hist[((nv - 1) * NP + n) * 32 + lane] : 0.0f;
+        for (int n = 0; n < NPW; ++n) hn[n] = nv > 0 ? hist[((nv - 1) * NPW + n) * 32 + lane] : 0.0f;
 #pragma unroll
         for (int i = kBwdTile - 1; i >= 0; --i) {
             if (i >= nv) continue;
             const long long t = t0 + i;
             const float uv = S(kSU, i), dt = S(kSDT, i), g = S(kSG, i);
-            dD = fmaf(g, uv, dD);
-            // four interleaved partial sums shorten the dependent chains
-            float dus[4] = {g * dsk, 0.0f, 0.0f, 0.0f}, dds[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            float pb[NP], pc[NP];
+            float dus[2] = {warp == 0 ? g * dsk : 0.0f, 0.0f}, dds[2] = {0.0f, 0.0f};
+            float pb[NPW], pc[NPW];
 #pragma unroll
-            for (int j = 0; j < NP / 2; ++j) {
-                const float4 p = sbc[i * (NP / 2) + j];
+            for (int j = 0; j < NPW / 2; ++j) {
+                const float4 p = sbc[i * (NP / 2) + n0 / 2 + j];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int n = 2 * j + e;
                     const float Bn = e ? p.y : p.x, Cn = e ? p.w : p.z;
                     const float ht = hn[n];
-                    const float hp = i > 0 ? hist[((i - 1) * NP + n) * 32 + lane] : hs[n];
+                    const float hp = i > 0 ? hist[((i - 1) * NPW + n) * 32 + lane] : hs[n];
                     hn[n] = hp;
                     const float abar = exp_f<ACC>(dt * Ar[n]);
                     dh[n] = fmaf(g, Cn, dh[n]);
                     pc[n] = g * ht;
                     const float dhd = dh[n] * dt;
                     pb[n] = dhd * uv;
-                    dus[n & 3] = fmaf(dhd, Bn, dus[n & 3]);
-                    dds[n & 3] = fmaf(dh[n], fmaf(Ar[n] * abar, hp, Bn * uv), dds[n & 3]);
+                    dus[e] = fmaf(dhd, Bn, dus[e]);
+                    dds[e] = fmaf(dh[n], fmaf(Ar[n] * abar, hp, Bn * uv), dds[e]);
                     dA[n] = fmaf(dhd * abar, hp, dA[n]);
                     dh[n] *= abar;
                 }
             }
-            const float dut = (dus[0] + dus[1]) + (dus[2] + dus[3]);
-            const float ddel = ((dds[0] + dds[1]) + (dds[2] + dds[3])) * S(kSSIG, i);
-            dbias += ddel;
-            S(kSDU, i) = dut;
-            S(kSDD, i) = ddel;
-            const float sb = warp_sum_transpose<NP>(pb, lane);
-            const float sc = warp_sum_transpose<NP>(pc, lane);
+            P(warp, kPDU, i) = dus[0] + dus[1];
+            P(warp, kPDD, i) = dds[0] + dds[1];
+            const float sb = warp_sum_transpose<NPW>(pb, lane);
+            const float sc = warp_sum_transpose<NPW>(pc, lane);
             if (writer) {
                 pBg[t * NP + my_n] = sb;
                 pCg[t * NP + my_n] = sc;
             }
         }
-        if (q.ok) {   // the tile's outputs, one lane per row
-            const bool vec = a.vec8 != 0;
+        __syncthreads();
+        // (d) the tile's outputs, one lane per row: warp 0 du and ddelta,
+        //     warp 1 dz; partial sums added in warp order
+        if (warp == 0) {
+            float o[kBwdTile], od[kBwdTile];
+#pragma unroll
+            for (int i = 0; i < kBwdTile; ++i) {
+                float su = 0.0f, sd = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kBwdSplit; ++w) {
+                    su += P(w, kPDU, i);
+                    sd += P(w, kPDD, i);
+                }
+                const bool on = i < nv;
+                o[i] = su;
+                od[i] = sd * S(kSSIG, i);
+                if (on) {
+                    dbias += od[i];
+                    dD = fmaf(S(kSG, i), S(kSU, i), dD);
+                }
+            }
+            if (q.ok) {
+                store_tile_row<T>(dur, t0, nv, vec, o);
+                store_tile_row<T>(ddr, t0, nv, vec, od);
+            }
+        } else if constexpr (HZ) {
             float o[kBwdTile];
 #pragma unroll
-            for (int i = 0; i < kBwdTile; ++i) o[i] = S(kSDU, i);
-            store_tile_row<T>(dur, t0, nv, vec, o);
+            for (int i = 0; i < kBwdTile; ++i) {
+                float sy = 0.0f;
 #pragma unroll
-            for (int i = 0; i < kBwdTile; ++i) o[i] = S(kSDD, i);
-            store_tile_row<T>(ddr, t0, nv, vec, o);
-            if constexpr (HZ) {
-#pragma unroll
-                for (int i = 0; i < kBwdTile; ++i) o[i] = S(kSDZ, i);
-                store_tile_row<T>(dzr, t0, nv, vec, o);
+                for (int w = 0; w < kBwdSplit; ++w) sy += P(w, kPY, i);
+                o[i] = S(kSZF, i) * sy;   // dz = dy (C.h + D u) silu'(z)
             }
+            if (q.ok) store_tile_row<T>(dzr, t0, nv, vec, o);
         }
-        __syncwarp();   // every read of this tile's states done
+        __syncthreads();   // shared memory is rewritten by the next tile
     }
     if (q.ok) {
 #pragma unroll
-        for (int n = 0; n < NP; ++n) {
-            a.pA[q.row * NP + n] = dA[n];
-            if (a.dh0 && n < N) a.dh0[q.row * N + n] = dh[n];
+        for (int n = 0; n < NPW; ++n) {
+            a.pA[q.row * NP + n0 + n] = dA[n];
+            if (a.dh0 && n0 + n < N) a.dh0[q.row * N + n0 + n] = dh[n];
         }
-        a.pD[q.row] = dD;
-        a.pbias[q.row] = dbias;
+        if (warp == 0) {
+            a.pD[q.row] = dD;
+            a.pbias[q.row] = dbias;
+        }
     }
 }
 
@@ -499,10 +570,11 @@ bwd_reduce_params_kernel(const float* __restrict__ pA, const float* __restrict__
 
 template <typename T, int NP, bool SP>
 cudaError_t launch_bwd(const BwdArgs& a, bool hz, cudaStream_t st) {
-    const long long warps = (long long)a.batch * a.groups;
+    const long long units = (long long)a.batch * a.groups;
     {
         ProfScope prof(kKindBwdCheckpoint, st);
-        const unsigned grid = (unsigned)((warps * 32 + kCkptThreads - 1) / kCkptThreads);
+        const long long threads = units * kBwdSplit * 32;
+        const unsigned grid = (unsigned)((threads + kCkptThreads - 1) / kCkptThreads);
         bwd_checkpoint_kernel<T, NP, SP><<<grid, kCkptThreads, 0, st>>>(a);
     }
     cudaError_t e = cudaGetLastError();
@@ -513,7 +585,7 @@ cudaError_t launch_bwd(const BwdArgs& a, bool hz, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     {
         ProfScope prof(kKindBwd, st);
-        k<<<(unsigned)warps, 32, smem, st>>>(a);
+        k<<<(unsigned)units, 32 * kBwdSplit, smem, st>>>(a);
     }
     return cudaGetLastError();
 }
