@@ -150,21 +150,29 @@ __device__ __forceinline__ WarpUnit warp_unit(const BwdArgs& a, long long w) {
     return u;
 }
 
-// State entries of a unit are split over kBwdSplit warps (their recurrences
-// are independent); warp w of a unit holds entries [w * NPW, (w + 1) * NPW).
+// State entries of a unit are split over kBwdSplit warps in the reverse pass
+// and ckpt_split<NP>() warps in the checkpoint pass (their recurrences are
+// independent); warp w of a unit holds entries [w * NPW, (w + 1) * NPW).
+// Measured on B300, four warps per unit make the checkpoint pass slower
+// (0.50 -> 0.58 ms on the Mamba-2.8B layer), so both use two.
 constexpr int kBwdSplit = 2;
+template <int NP>
+__host__ __device__ constexpr int ckpt_split() {
+    return 2;
+}
 
 template <typename T, int NP, bool SP>
 __global__ void __launch_bounds__(kCkptThreads)
 bwd_checkpoint_kernel(const BwdArgs a) {
     constexpr bool ACC = IO<T>::kAccurate;
-    constexpr int NPW = NP / kBwdSplit;
+    constexpr int CS = ckpt_split<NP>();
+    constexpr int NPW = NP / CS;
     // the tile's B/C rows of this warp's state entries, per warp of the CTA
-    __shared__ float4 ck_bc[kCkptThreads / 32][kBwdTile * (kMaxN / 2 / kBwdSplit)];
+    __shared__ float4 ck_bc[kCkptThreads / 32][kBwdTile * (NPW / 2)];
     const long long gw = ((long long)blockIdx.x * kCkptThreads + threadIdx.x) >> 5;
-    if (gw >= (long long)a.batch * a.groups * kBwdSplit) return;   // whole warps leave together
-    const int half = (int)(gw % kBwdSplit);
-    const WarpUnit q = warp_unit(a, gw / kBwdSplit);
+    if (gw >= (long long)a.batch * a.groups * CS) return;   // whole warps leave together
+    const int half = (int)(gw % CS);
+    const WarpUnit q = warp_unit(a, gw / CS);
     const int N = a.N, n0 = half * NPW;
     const long long L = a.L;
     float4* sb = ck_bc[threadIdx.x >> 5];
@@ -434,7 +442,9 @@ bwd_kernel(const BwdArgs a) {
         float hn[NPW];
 #pragma unroll
         for (int n = 0; n < NPW; ++n) hn[n] = nv > 0 ? hist[((nv - 1) * NPW + n) * 32 + lane] : 0.0f;
-#pragma unroll
+        // (kept rolled: the unrolled tile's code overflows the instruction
+        // cache; measured on B300 6% slower)
+#pragma unroll 1
         for (int i = kBwdTile - 1; i >= 0; --i) {
             if (i >= nv) continue;
             const long long t = t0 + i;
@@ -573,7 +583,7 @@ cudaError_t launch_bwd(const BwdArgs& a, bool hz, cudaStream_t st) {
     const long long units = (long long)a.batch * a.groups;
     {
         ProfScope prof(kKindBwdCheckpoint, st);
-        const long long threads = units * kBwdSplit * 32;
+        const long long threads = units * ckpt_split<NP>() * 32;
         const unsigned grid = (unsigned)((threads + kCkptThreads - 1) / kCkptThreads);
         bwd_checkpoint_kernel<T, NP, SP><<<grid, kCkptThreads, 0, st>>>(a);
     }
