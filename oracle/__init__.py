@@ -15,7 +15,9 @@ closed forms and independent formulations (Theorem 1's gated RNN, the
 keep/reset limits, the explicitly unrolled sum, the time-invariant
 convolution, linearity, causality); the backward pass ``scan_bwd`` by
 ``tests/test_oracle_bwd_pins.py`` (central finite differences of the
-forward for every input, and exact adjoint identities).
+forward for every input, and exact adjoint identities); the causal
+convolution ``conv1d`` by ``tests/test_oracle_conv_pins.py``
+(numpy.convolve, a hand-worked example, continuation through the state).
 """
 
 from __future__ import annotations
@@ -65,6 +67,8 @@ def _load():
             lib.oracle_scan_bwd_f64.argtypes = [i64, i64, i64, i64] + [P] * 8 + [ctypes.c_int] \
                 + [P] * 12
             lib.oracle_scan_bwd_f64.restype = ctypes.c_int
+            lib.oracle_conv1d_f64.argtypes = [i64, i64, i64, i64, P, P, P, P, ctypes.c_int, P, P]
+            lib.oracle_conv1d_f64.restype = ctypes.c_int
             lib.oracle_softplus_f64.argtypes = [ctypes.c_double]
             lib.oracle_softplus_f64.restype = ctypes.c_double
             lib.oracle_zoh_weight_f64.argtypes = [ctypes.c_double, ctypes.c_double]
@@ -151,6 +155,26 @@ def scan_bwd(u, delta, A, B, C, dy, dt_bias=None, D_skip=None, z=None, softplus:
     if rc != 0:
         raise RuntimeError(f"oracle_scan_bwd_f64 failed: {rc}")
     return out
+
+
+def conv1d(x, weight, bias=None, state=None, silu: bool = True):
+    """Causal depthwise convolution (width W = weight.shape[1]) with an
+    optional SiLU, in fp64.  x: (batch, D, L); weight: (D, W); bias: (D,);
+    state: optional (batch, D, W - 1), the inputs before t = 0, oldest first.
+    Returns (out (batch, D, L), state after the last input (batch, D, W - 1))."""
+    x, weight, bias, state = map(_f64, (x, weight, bias, state))
+    bt, d, l = x.shape
+    w = weight.shape[1]
+    assert weight.shape == (d, w)
+    if state is not None:
+        assert state.shape == (bt, d, w - 1)
+    out = np.empty((bt, d, l))
+    st = np.empty((bt, d, w - 1))
+    rc = _load().oracle_conv1d_f64(bt, d, l, w, _ptr(x), _ptr(weight), _ptr(bias), _ptr(state),
+                                   int(bool(silu)), _ptr(out), _ptr(st))
+    if rc != 0:
+        raise RuntimeError(f"oracle_conv1d_f64 failed: {rc}")
+    return out, st
 
 
 def state_update(state, x, delta, A, B, C, dt_bias=None, D_skip=None, z=None,

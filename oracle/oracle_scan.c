@@ -357,3 +357,54 @@ int oracle_scan_bwd_f64(int64_t batch, int64_t dim, int64_t dstate, int64_t seql
     free(dh);
     return 0;
 }
+
+/*
+ * Causal depthwise convolution over time with an optional SiLU: the short
+ * convolution of the Mamba block's H3-derived branch, in front of the scan
+ * (page "Mamba: linear-time sequence modeling with selective state spaces",
+ * "What they did", Architecture bullet: the block merges the H3 block and a
+ * gated MLP; the pages print no formula for it, so this is the plain
+ * reading: one width-W filter per channel, causal, bias, then SiLU).
+ *
+ *   xp(t)      = x[b,d,t] for t >= 0, state[b,d,W-1+t] for -(W-1) <= t < 0
+ *                (zero without a state)
+ *   out[b,d,t] = act( bias[d] + sum_{k=0}^{W-1} w[d,k] * xp(t - (W-1) + k) )
+ *
+ * state (batch, dim, W-1) holds the last W-1 inputs before t = 0, oldest
+ * first; state_out receives the last W-1 inputs of xp up to t = L-1.
+ * Layouts: x, out (batch, dim, L); w (dim, W); bias (dim).
+ */
+int oracle_conv1d_f64(int64_t batch, int64_t dim, int64_t seqlen, int64_t width,
+                      const double *x, const double *w, const double *bias,
+                      const double *state, int silu, double *out, double *state_out)
+{
+    if (batch < 0 || dim < 0 || seqlen < 0 || width < 1)
+        return -2;
+    if (!x || !w || !out)
+        return -1;
+    const int64_t L = seqlen, W = width, S = width - 1;
+    for (int64_t row = 0; row < batch * dim; ++row) {
+        const int64_t d = row % dim;
+        const double *xr = x + row * L;
+        for (int64_t t = 0; t < L; ++t) {
+            double acc = bias ? bias[d] : 0.0;
+            for (int64_t k = 0; k < W; ++k) {
+                const int64_t s = t - (W - 1) + k;
+                double v;
+                if (s >= 0)
+                    v = xr[s];
+                else
+                    v = state ? state[row * S + (S + s)] : 0.0;
+                acc += w[d * W + k] * v;
+            }
+            out[row * L + t] = silu ? oracle_silu_f64(acc) : acc;
+        }
+        if (state_out) {
+            for (int64_t j = 0; j < S; ++j) {
+                const int64_t s = L - S + j;   /* position of the j-th kept input */
+                state_out[row * S + j] = s >= 0 ? xr[s] : (state ? state[row * S + (S + s)] : 0.0);
+            }
+        }
+    }
+    return 0;
+}
