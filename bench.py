@@ -359,6 +359,8 @@ def run_ours(args, shape):
         line["ext"] = ext_leg(shape, (u, delta, dtb, A, B, C, dsk, z), y, fin, dev, stream, mm)
     if not args.no_bwd and rank == 0:
         line["bwd"] = bwd_leg(shape, (u, delta, dtb, A, B, C, dsk, z), dev, stream, mm)
+    if not args.no_conv and rank == 0:
+        line["conv"] = conv_leg(shape, u, dev, stream, mm)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, thr, nrows, secs = oracle_rate(inp, shape, args.cpu_seconds)
         line["cpu_baseline"] = {
@@ -502,6 +504,66 @@ def bwd_leg(shape, ins, dev, stream, mm, steps=10, warmup=3):
             "note": "checkpoint pass + reverse pass (recomputes each 12-step tile) + reductions"}
 
 
+def conv_leg(shape, x, dev, stream, mm, width=4, steps=50, warmup=5):
+    """The causal width-4 convolution + SiLU on the workload's input tensor
+    (one read of x, one write of the output, plus the carried state), and its
+    generation step on the decode workload's (batch, dim).  HBM-bound: the
+    roofline is the measured copy bandwidth."""
+    import torch
+    g = torch.Generator(device=dev).manual_seed(13)
+    w = torch.randn((shape.dim, width), device=dev, generator=g) / 2
+    bias = torch.randn((shape.dim,), device=dev, generator=g)
+    out = torch.empty_like(x)
+    fin = torch.empty((shape.batch, shape.dim, width - 1), dtype=x.dtype, device=dev)
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+
+    def timed(fn, n):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / n
+
+    ms = timed(lambda: mm.mamba_conv1d_fwd(x, w, bias, silu=True, out=out, final_conv_state=fin,
+                                           stream=stream), steps)
+    nbytes = 2 * x.numel() * x.element_size() + fin.numel() * fin.element_size()
+    dshp = synth.DECODE
+    xs = torch.randn((dshp.batch, dshp.dim), device=dev, generator=g).to(x.dtype)
+    st = torch.zeros((dshp.batch, dshp.dim, width - 1), dtype=x.dtype, device=dev)
+    wd = torch.randn((dshp.dim, width), device=dev, generator=g) / 2
+    ys = torch.empty_like(xs)
+    # the generation step from a captured graph of 200 steps (no launch cost)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            mm.mamba_conv1d_update(st, xs, wd, None, out=ys, stream=side)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for _ in range(200):
+            mm.mamba_conv1d_update(st, xs, wd, None, out=ys, stream=side)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    graph.replay()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms_step = e0.elapsed_time(e1) / 200
+    step_bytes = 2 * xs.numel() * xs.element_size() + 2 * st.numel() * st.element_size()
+    return {"width": width, "ms_per_call": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+            "hbm_frac": nbytes / (ms * 1e-3) / 1e9 / hbm, "bytes_per_call": nbytes,
+            "step_us": ms_step * 1e3, "step_GB/s": step_bytes / (ms_step * 1e-3) / 1e9,
+            "step_workload": f"decode b{dshp.batch} d{dshp.dim}", "peak_source": src}
+
+
 def decode_leg(dev, mm):
     """Batched generation: (128, 5120, 16) fp32 state, single-token steps,
     1024 steps replayed from one CUDA graph; 16 distinct input sets cycled."""
@@ -568,6 +630,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-ext", action="store_true")
     ap.add_argument("--no-bwd", action="store_true")
+    ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -261,6 +261,40 @@ int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
                    float *dD_skip, void *dz, float *ddt_bias,
                    float *d_initial_state, cudaStream_t stream);
 
+/*
+ * Causal depthwise convolution with optional SiLU: the short convolution in
+ * front of the scan in the Mamba block (paper "Mamba: linear-time sequence
+ * modeling with selective state spaces", "What they did": the block merges
+ * the H3 block and a gated MLP; the pages print no formula, so this is the
+ * plain reading, one width-W filter per channel):
+ *
+ *   xp(t)      = x[b,d,t] for t >= 0, conv_state[b,d,W-1+t] for t < 0 (zero without one)
+ *   out[b,d,t] = act(bias[d] + sum_{k<W} weight[d,k] * xp(t - (W-1) + k)),  act = silu or identity
+ *
+ *   x, out           : (batch, dim, seqlen)   io_dtype
+ *   weight           : (dim, width)           fp32      1 <= width <= 8
+ *   bias             : (dim)                  fp32      nullable
+ *   conv_state       : (batch, dim, width-1)  io_dtype  nullable: the W-1 inputs before t = 0, oldest first
+ *   final_conv_state : (batch, dim, width-1)  io_dtype  nullable: the W-1 inputs up to t = seqlen-1
+ *
+ * final_conv_state must not overlap conv_state (MAMBA_ERR_ALIAS): ping-pong
+ * two buffers to chain pieces of a sequence.  Allocates nothing.
+ */
+int mamba_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int width, int io_dtype,
+                     const void *x, const float *weight, const float *bias,
+                     const void *conv_state, int silu, void *out, void *final_conv_state,
+                     cudaStream_t stream);
+
+/*
+ * One generation step of the convolution: out[b,d] from x[b,d] and the
+ * row's W-1 previous inputs in conv_state (batch, dim, width-1), which is
+ * then shifted by one and gets x[b,d] as its newest entry, in place.
+ * Arguments as in mamba_conv1d_fwd (x, out: (batch, dim)).
+ */
+int mamba_conv1d_update(int64_t batch, int64_t dim, int width, int io_dtype, void *conv_state,
+                        const void *x, const float *weight, const float *bias, int silu,
+                        void *out, cudaStream_t stream);
+
 /* Static, human-readable name of a mamba_status_t value. */
 const char *mamba_status_string(int status);
 
@@ -308,7 +342,7 @@ int mamba_scan_set_tuning(int tail, int stages, int chunks);
  * 0 = scan, 1 = chunk summary, 2 = chunk carry, 3 = state update,
  * 4 = B/C packing (one per scan or backward call), 5 = backward checkpoint
  * pass, 6 = backward reverse pass, 7 = backward reductions (one timing for
- * the three reduction launches of a call).
+ * the three reduction launches of a call), 8 = causal convolution.
  * Either output may be NULL.  Not meant for use during stream capture.
  */
 int mamba_profile_begin(void);

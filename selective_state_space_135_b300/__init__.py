@@ -18,6 +18,8 @@ from ._lib import (  # noqa: F401
     MambaError,
     lib_path,
     load,
+    mamba_conv1d_fwd,
+    mamba_conv1d_update,
     mamba_device_status,
     mamba_profile_begin,
     mamba_profile_end,

@@ -16,7 +16,7 @@ MAMBA_BF16 = 1
 
 # every symbol the header declares
 EXPORTS = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_ex", "mamba_scan_bwd",
-           "mamba_state_update",
+           "mamba_conv1d_fwd", "mamba_conv1d_update", "mamba_state_update",
            "mamba_state_update_ex", "mamba_status_string", "mamba_device_status",
            "mamba_selftest_wait_timeout", "mamba_version", "mamba_scan_set_tuning",
            "mamba_profile_begin", "mamba_profile_end")
@@ -27,7 +27,7 @@ MAMBA_FLAG_ZOH = 2
 MAMBA_FLAG_NOALLOC = 4
 
 KIND_NAMES = ("scan", "chunk_summary", "chunk_carry", "state_update", "pack_bc",
-              "bwd_checkpoint", "bwd", "bwd_reduce")
+              "bwd_checkpoint", "bwd", "bwd_reduce", "conv1d")
 
 
 class MambaError(RuntimeError):
@@ -70,6 +70,10 @@ def load():
         lib.mamba_scan_bwd.argtypes = [i64, i64, i64, i64, i32] + [vp] * 8 + [i32] + [vp] * 3 \
             + [vp] * 9 + [vp]
         lib.mamba_scan_bwd.restype = i32
+        lib.mamba_conv1d_fwd.argtypes = [i64, i64, i64, i32, i32, vp, vp, vp, vp, i32, vp, vp, vp]
+        lib.mamba_conv1d_fwd.restype = i32
+        lib.mamba_conv1d_update.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, i32, vp, vp]
+        lib.mamba_conv1d_update.restype = i32
         lib.mamba_status_string.argtypes = [i32]
         lib.mamba_status_string.restype = ctypes.c_char_p
         lib.mamba_device_status.argtypes = [vp]
@@ -286,6 +290,59 @@ def mamba_scan_bwd(u, delta, dt_bias, A, B, C, D_skip, z, dy, softplus: bool = T
     if rc != 0:
         raise MambaError(rc, "mamba_scan_bwd")
     return o
+
+
+def mamba_conv1d_fwd(x, weight, bias=None, conv_state=None, silu: bool = True, out=None,
+                     final_conv_state=None, stream=None):
+    """Causal depthwise convolution (+ SiLU).  x: (batch, dim, L); weight:
+    (dim, W) fp32; bias (dim,) fp32 or None; conv_state (batch, dim, W-1) in
+    x's dtype or None; final_conv_state, if given, gets the W-1 last inputs.
+    Returns out (allocated if None)."""
+    torch = _torch()
+    lib = load()
+    batch, dim, L = x.shape
+    W = weight.shape[1]
+    dev = x.device
+    io = _io_dtype(x)
+    if out is None:
+        out = torch.empty_like(x)
+    args = (_ptr(x, "x", x.dtype, (batch, dim, L), dev),
+            _ptr(weight, "weight", torch.float32, (dim, W), dev),
+            _ptr(bias, "bias", torch.float32, (dim,), dev),
+            _ptr(conv_state, "conv_state", x.dtype, (batch, dim, W - 1), dev))
+    op = _ptr(out, "out", x.dtype, (batch, dim, L), dev)
+    fp = _ptr(final_conv_state, "final_conv_state", x.dtype, (batch, dim, W - 1), dev)
+    with torch.cuda.device(dev):
+        st = _stream_handle(stream, dev)
+        rc = lib.mamba_conv1d_fwd(batch, dim, L, W, io, *args, int(bool(silu)), op, fp, st)
+    if rc != 0:
+        raise MambaError(rc, "mamba_conv1d_fwd")
+    return out
+
+
+def mamba_conv1d_update(conv_state, x, weight, bias=None, silu: bool = True, out=None,
+                        stream=None):
+    """One generation step of the convolution; conv_state (batch, dim, W-1)
+    is updated in place.  x: (batch, dim).  Returns out (batch, dim)."""
+    torch = _torch()
+    lib = load()
+    batch, dim = x.shape
+    W = weight.shape[1]
+    dev = x.device
+    io = _io_dtype(x)
+    if out is None:
+        out = torch.empty_like(x)
+    sp = _ptr(conv_state, "conv_state", x.dtype, (batch, dim, W - 1), dev) if W > 1 else None
+    args = (_ptr(x, "x", x.dtype, (batch, dim), dev),
+            _ptr(weight, "weight", torch.float32, (dim, W), dev),
+            _ptr(bias, "bias", torch.float32, (dim,), dev))
+    op = _ptr(out, "out", x.dtype, (batch, dim), dev)
+    with torch.cuda.device(dev):
+        st = _stream_handle(stream, dev)
+        rc = lib.mamba_conv1d_update(batch, dim, W, io, sp, *args, int(bool(silu)), op, st)
+    if rc != 0:
+        raise MambaError(rc, "mamba_conv1d_update")
+    return out
 
 
 def mamba_state_update(state, x, delta, dt_bias, A, B, C, D_skip, z, y=None, stream=None):

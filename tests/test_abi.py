@@ -198,6 +198,32 @@ def test_scan_bwd_validation(lib):
     assert bwd_call(lib, dh0=addr(9)) == EALIAS       # d_initial_state on top of initial_state
 
 
+def test_conv1d_validation(lib):
+    # rejected on the host, before any CUDA call
+    def fwd(width=4, **kw):
+        v = dict(x=addr(1), w=addr(2), b=addr(3), st=addr(4), out=addr(5), fin=addr(6))
+        v.update(kw)
+        return lib.mamba_conv1d_fwd(2, 16, 64, width, 1, v["x"], v["w"], v["b"], v["st"], 1,
+                                    v["out"], v["fin"], None)
+    assert fwd(width=0) == ESHAPE
+    assert fwd(width=9) == ESHAPE
+    assert fwd(x=None) == ENULL
+    assert fwd(w=None) == ENULL
+    assert fwd(out=addr(1)) == EALIAS            # out on top of x
+    assert fwd(fin=addr(4)) == EALIAS            # final state on top of the state
+    assert fwd(w=addr(2) + 2) == EALIGN
+    assert fwd(x=addr(1) + 1) == EALIGN
+
+    def upd(width=4, **kw):
+        v = dict(st=addr(1), x=addr(2), w=addr(3), b=addr(4), out=addr(5))
+        v.update(kw)
+        return lib.mamba_conv1d_update(2, 16, width, 1, v["st"], v["x"], v["w"], v["b"], 1,
+                                       v["out"], None)
+    assert upd(width=9) == ESHAPE
+    assert upd(st=None) == ENULL
+    assert upd(out=addr(2)) == EALIAS
+
+
 def test_state_update_ex_flags(lib):
     def call(flags, **kw):
         v = {k: addr(i) for i, k in enumerate(("state", "x", "delta", "dtb", "A", "B", "C",
