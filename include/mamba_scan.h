@@ -22,6 +22,19 @@
  * Modeling with Selective State Spaces", "Architecture": producing a token
  * needs only one update of the state).
  *
+ * Entry points
+ *   mamba_scan_fwd          the scan from a zero state (the hot path)
+ *   mamba_scan_fwd_ex       the scan from an initial state, with per-entry
+ *                           lengths, zero-order hold and the no-allocation
+ *                           scratch as options
+ *   mamba_scan_fwd_noalloc  mamba_scan_fwd with fixed scratch, no allocation
+ *   mamba_state_update(_ex) one generation step on a caller-held state
+ *   mamba_scan_bwd          gradients of every scan input (state recomputed)
+ *   mamba_conv1d_fwd        the causal convolution in front of the scan
+ *   mamba_conv1d_update     its generation step
+ *   plus status strings, the device error word and its self-test, tuning
+ *   and per-launch timing.
+ *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers on the current CUDA device and
  *     are dense row-major with the shapes given below.  The caller owns
