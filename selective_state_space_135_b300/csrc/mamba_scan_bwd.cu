@@ -127,10 +127,12 @@ __device__ __forceinline__ float sigmoid_f(float s) {
     if constexpr (ACC) return 1.0f / (1.0f + expf(-s));
     else return __fdividef(1.0f, 1.0f + ex2_approx(-s * kLog2e));
 }
+// Abar = exp(Delta * A).  dtl is Delta / ln 2, formed once per step, so the
+// fast path needs one multiply and one ex2 per state entry.
 template <bool ACC>
-__device__ __forceinline__ float exp_f(float x) {
-    if constexpr (ACC) return expf(x);
-    else return ex2_approx(x * kLog2e);
+__device__ __forceinline__ float abar_of(float dt, float dtl, float a) {
+    if constexpr (ACC) return expf(dt * a);
+    else return ex2_approx(dtl * a);
 }
 
 // Warp unit of both passes: 32 consecutive channels of one batch entry.
@@ -232,12 +234,13 @@ bwd_checkpoint_kernel(const BwdArgs a) {
         for (int i = 0; i < kBwdTile; ++i) {
             if (i < nv) {
                 const float dt = delta_nat<ACC, SP>(dc[i] + bias);
+                const float dtl = dt * kLog2e;
                 const float du = dt * uc[i];
 #pragma unroll
                 for (int j = 0; j < NPW / 2; ++j) {
                     const float4 p = sb[i * (NPW / 2) + j];
-                    h[2 * j] = fmaf(exp_f<ACC>(dt * Ar[2 * j]), h[2 * j], du * p.x);
-                    h[2 * j + 1] = fmaf(exp_f<ACC>(dt * Ar[2 * j + 1]), h[2 * j + 1], du * p.y);
+                    h[2 * j] = fmaf(abar_of<ACC>(dt, dtl, Ar[2 * j]), h[2 * j], du * p.x);
+                    h[2 * j + 1] = fmaf(abar_of<ACC>(dt, dtl, Ar[2 * j + 1]), h[2 * j + 1], du * p.y);
                 }
             }
         }
@@ -421,13 +424,14 @@ bwd_kernel(const BwdArgs a) {
             for (int i = 0; i < kBwdTile; ++i) {
                 if (i >= nv) continue;
                 const float uv = S(kSU, i), dt = S(kSDT, i);
+                const float dtl = dt * kLog2e;
                 const float du = dt * uv;
                 float acc = warp == 0 ? dsk * uv : 0.0f;
 #pragma unroll
                 for (int j = 0; j < NPW / 2; ++j) {
                     const float4 p = sbc[i * (NP / 2) + n0 / 2 + j];
-                    h[2 * j] = fmaf(exp_f<ACC>(dt * Ar[2 * j]), h[2 * j], du * p.x);
-                    h[2 * j + 1] = fmaf(exp_f<ACC>(dt * Ar[2 * j + 1]), h[2 * j + 1], du * p.y);
+                    h[2 * j] = fmaf(abar_of<ACC>(dt, dtl, Ar[2 * j]), h[2 * j], du * p.x);
+                    h[2 * j + 1] = fmaf(abar_of<ACC>(dt, dtl, Ar[2 * j + 1]), h[2 * j + 1], du * p.y);
                     acc = fmaf(p.z, h[2 * j], acc);
                     acc = fmaf(p.w, h[2 * j + 1], acc);
                     hist[(i * NPW + 2 * j) * 32 + lane] = h[2 * j];
@@ -449,6 +453,7 @@ bwd_kernel(const BwdArgs a) {
             if (i >= nv) continue;
             const long long t = t0 + i;
             const float uv = S(kSU, i), dt = S(kSDT, i), g = S(kSG, i);
+            const float dtl = dt * kLog2e;
             float dus[2] = {warp == 0 ? g * dsk : 0.0f, 0.0f}, dds[2] = {0.0f, 0.0f};
             float pb[NPW], pc[NPW];
 #pragma unroll
@@ -461,7 +466,7 @@ bwd_kernel(const BwdArgs a) {
                     const float ht = hn[n];
                     const float hp = i > 0 ? hist[((i - 1) * NPW + n) * 32 + lane] : hs[n];
                     hn[n] = hp;
-                    const float abar = exp_f<ACC>(dt * Ar[n]);
+                    const float abar = abar_of<ACC>(dt, dtl, Ar[n]);
                     dh[n] = fmaf(g, Cn, dh[n]);
                     pc[n] = g * ht;
                     const float dhd = dh[n] * dt;
