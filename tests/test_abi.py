@@ -266,3 +266,28 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises(ValueError):
         mm.mamba_scan_fwd(u, u, None, torch.zeros(4, 2), torch.zeros(1, 2, 8),
                           torch.zeros(1, 2, 8), None, None)
+
+
+def test_header_is_plain_c(tmp_path):
+    # The boundary is a C ABI: a C11 translation unit that includes the
+    # header and takes the address of every entry point must compile and link
+    # against the library, with no C++ or torch types involved.
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda_inc = "/usr/local/cuda/include"
+    if gcc is None or not os.path.isdir(cuda_inc):
+        pytest.skip("gcc or the CUDA headers are not available")
+    names = declared_functions()
+    src = tmp_path / "abi_check.c"
+    src.write_text('#include "mamba_scan.h"\n#include <stdio.h>\n'
+                   "int main(void) {\n    const void* fns[] = {\n"
+                   + "".join(f"        (const void*)&{n},\n" for n in names)
+                   + "    };\n    printf(\"%d\\n\", (int)(sizeof(fns) / sizeof(fns[0])));\n"
+                   "    return 0;\n}\n")
+    exe = tmp_path / "abi_check"
+    lib = _lib.lib_path()
+    cmd = [gcc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+           str(src), "-o", str(exe), lib, f"-Wl,-rpath,{os.path.dirname(lib)}"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
