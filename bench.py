@@ -15,7 +15,10 @@ all ranks (each rank scans its own independently seeded batch: weak scaling).
 The line carries the roofline of the dominant kernel (timed per launch with
 CUDA events on its stream), an end-to-end figure through pinned host memory,
 SM clocks sampled during the timed region, the decode step, and the fp64 CPU
-oracle timed on a bounded sample of the same workload.
+oracle timed on a bounded sample of the same workload.  Further objects time,
+on the same inputs, the extended scan (initial state; Euler and zero-order
+hold), the backward pass and the causal convolution with its generation
+step (--no-ext, --no-bwd, --no-conv skip them).
 """
 
 from __future__ import annotations
