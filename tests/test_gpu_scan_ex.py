@@ -326,3 +326,21 @@ def test_euler_ex_equals_plain_entry_point():
                            f32_dev(inp["D_skip"]), z, True, final_state=f2)
     torch.cuda.synchronize()
     assert torch.equal(y1, y2) and torch.equal(f1, f2)
+
+
+def test_extended_modes_on_a_full_wave_with_a_side_stream_tail():
+    # 3 x 3200 channels are 300 tiles of 32: whole-sequence tiles on the
+    # caller's stream and the 4 leftover tiles cut into time chunks on the
+    # library's side stream (tail mode 3), with an initial state, per-entry
+    # lengths and both discretisations
+    import selective_state_space_135_b300 as mm
+    shp, inp = _problem(synth.BF16, 3, 3200, 16, 1024, seed=43)
+    h0 = _h0(shp, 44)
+    lens = np.array([1024, 517, 800], np.int32)
+    mm.mamba_scan_set_tuning(3, 0, 0)
+    for zoh in (False, True):
+        y, fin = gpu_ex(inp, zoh=zoh, h0=h0, lens=lens)
+        yr, hr = oracle_ex(inp, zoh=zoh, h0=h0, lens=lens)
+        assert_close(to_f64(y), yr, synth.BF16)
+        assert_close(to_f64(fin), hr, synth.BF16, "final_state")
+    assert mm.mamba_device_status() == 0
