@@ -4,12 +4,16 @@
 // recomputes it instead of reading it back (page "Mamba: linear-time
 // sequence modeling with selective state spaces", "What they did").  Here:
 //
-//   1. checkpoint pass: one lane per channel holding all N state entries
-//      runs the forward recurrence and stores the state before every tile of
-//      kBwdTile steps (B x D x ceil(L / kBwdTile) x N fp32);
-//   2. reverse pass: per tile, last to first, the lane recomputes the tile's
-//      states from its checkpoint into shared memory, then walks the tile
-//      backwards carrying dh = dJ/dh:
+//   1. checkpoint pass: one lane per channel, the N state entries split over
+//      two warps (their recurrences are independent), runs the forward
+//      recurrence and stores the state before every tile of kBwdTile steps
+//      (B x D x ceil(L / kBwdTile) x N fp32);
+//   2. reverse pass: one two-warp CTA per 32 channels, each warp holding half
+//      of the entries.  Per tile, last to first, the tile's inputs are staged
+//      in shared memory, each warp recomputes its entries' states from the
+//      checkpoint into shared memory, then walks the tile backwards carrying
+//      dh = dJ/dh (the warps add their partial sums over entries -- C.h, du,
+//      dDelta -- through shared memory):
 //        g_t   = dy_t * silu(z_t)             dz_t = dy_t * pre_t * silu'(z_t)
 //        dh   += g_t C_t                       dC_t += g_t h_t,  dB_t += dh Delta_t u_t
 //        du_t  = g_t D + sum_n dh Delta_t B_t  dDelta_t = sum_n dh (A Abar h_{t-1} + B_t u_t)
