@@ -8,6 +8,7 @@ Every step of the computation runs in the library's CUDA kernels: there is
 no CPU or PyTorch fallback, and calling without the built library raises.
 """
 
+from .autograd import mamba_scan_fn  # noqa: F401
 from ._lib import (  # noqa: F401
     KIND_NAMES,
     MAMBA_BF16,

@@ -158,3 +158,39 @@ def test_bwd_zero_length():
                           d_final_state=dfin, want_initial_state_grad=True)
     torch.cuda.synchronize()
     assert bool((g["dA"] == 0).all()) and bool((g["d_initial_state"] == dfin).all())
+
+
+def test_autograd_wrapper_matches_the_backward_call():
+    # torch autograd through mamba_scan_fn gives exactly mamba_scan_bwd's
+    # gradients (same kernels, same inputs), cast to each input's dtype
+    import selective_state_space_135_b300 as mm
+    torch = torch_mod()
+    shp, inp = _inputs(synth.BF16, 2, 70, 16, 150, seed=99)
+    dt = inp["dtype"]
+    u, delta, z, B, C = (to_dev(inp[k], dt).requires_grad_() for k in ("u", "delta", "z", "B", "C"))
+    A, dtb, dsk, h0 = (f32_dev(inp[k]).requires_grad_() for k in ("A", "dt_bias", "D_skip", "h0"))
+    dy = to_dev(inp["dy"], dt)
+    dfin = f32_dev(inp["dfinal"])
+    y, fin = mm.mamba_scan_fn(u, delta, A, B, C, D_skip=dsk, z=z, dt_bias=dtb, initial_state=h0,
+                              return_final_state=True)
+    ((y.float() * dy.float()).sum() + (fin * dfin).sum()).backward()
+    g = mm.mamba_scan_bwd(u.detach(), delta.detach(), dtb.detach(), A.detach(), B.detach(),
+                          C.detach(), dsk.detach(), z.detach(), dy, initial_state=h0.detach(),
+                          d_final_state=dfin, want_initial_state_grad=True)
+    y2 = mm.mamba_scan_fwd_ex(u.detach(), delta.detach(), dtb.detach(), A.detach(), B.detach(),
+                              C.detach(), dsk.detach(), z.detach(), initial_state=h0.detach())
+    torch.cuda.synchronize()
+    assert torch.equal(y.detach(), y2)
+    for t, k in ((u, "du"), (delta, "ddelta"), (z, "dz"), (A, "dA"), (dtb, "ddt_bias"),
+                 (dsk, "dD_skip"), (h0, "d_initial_state")):
+        assert torch.equal(t.grad, g[k].to(t.dtype)), k
+    for t, k in ((B, "dB"), (C, "dC")):
+        assert torch.equal(t.grad, g[k].to(t.dtype)), k
+    # without the final state only y is returned and differentiable
+    u.grad = None
+    y3 = mm.mamba_scan_fn(u, delta, A, B, C, D_skip=dsk, z=z, dt_bias=dtb)
+    (y3.float() * dy.float()).sum().backward()
+    g3 = mm.mamba_scan_bwd(u.detach(), delta.detach(), dtb.detach(), A.detach(), B.detach(),
+                           C.detach(), dsk.detach(), z.detach(), dy)
+    torch.cuda.synchronize()
+    assert torch.equal(u.grad, g3["du"])
