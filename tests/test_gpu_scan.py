@@ -43,6 +43,9 @@ def test_tiny_fp32_full():
     yr, hr = oracle_full(inp)
     assert_close(to_f64(y), yr, synth.F32)
     assert_close(to_f64(fin), hr, synth.F32, "final_state")
+    # the workload's own bound, plain: max-abs 1e-5
+    assert np.max(np.abs(to_f64(y) - yr)) <= TOL_F32_ABS
+    assert np.max(np.abs(to_f64(fin) - hr)) <= TOL_F32_ABS
 
 
 def test_theorem1_case_fp32():
