@@ -69,16 +69,27 @@ __device__ __forceinline__ float lg2_approx(float x) {
     return y;
 }
 
+// Softplus in log2 units on the hardware ex2/lg2 path: log2(1 + 2^t), i.e.
+// softplus(s) / ln 2 for t = s / ln 2, accurate in relative terms for every
+// t.  It is evaluated as max(t, 0) + log2(1 + x) with x = 2^-|t| in (0, 1],
+// so 2^t never overflows and, for very negative t (a step that keeps the
+// state), the result is x / ln 2 to full relative precision instead of the
+// rounded 1 + x.  log2(1 + x) = (x - x^2/2 + x^3/3 - ...) / ln 2; for
+// x < 2^-7 the first two terms are taken (relative error below x^2/3 <
+// 2e-5), otherwise lg2.approx(1 + x) (absolute error about 2^-22 against a
+// result of at least 0.011, relative error below 2.2e-5).
+__device__ __forceinline__ float softplus_log2_fast(float t) {
+    const float x = ex2_approx(-fabsf(t));
+    const float series = x * fmaf(x, -0.5f * kLog2e, kLog2e);
+    const float full = lg2_approx(1.0f + x);
+    return fmaxf(t, 0.0f) + (x < 0.0078125f ? series : full);
+}
+
 // softplus(s) = log(1 + e^s); for s > 20 it equals s to within e^-20.
 template <bool ACC>
 __device__ __forceinline__ float softplus_f(float s) {
-    float r;
-    if (ACC) {
-        r = log1pf(expf(s));
-    } else {
-        r = lg2_approx(1.0f + ex2_approx(s * kLog2e)) * kLn2;
-    }
-    return s > 20.0f ? s : r;
+    if (ACC) return s > 20.0f ? s : log1pf(expf(s));
+    return softplus_log2_fast(s * kLog2e) * kLn2;
 }
 
 // silu(z) = z * sigmoid(z).  Accurate path: z / (1 + e^-z).  Fast path:
