@@ -251,6 +251,55 @@ def run_reference(args, shape):
 
 
 # --------------------------------------------------------------------------
+# arithmetic rates (the denominators of the scan's roofline)
+
+PIPE_KINDS = {0: "ex2", 1: "lg2", 2: "tanh", 3: "ffma2 (lane-ops)", 4: "ffma",
+              5: "scan state update (2 ex2 + 4 packed ops per 2 updates)"}
+
+
+def run_pipe_rates():
+    """Sustained per-SM rates, in lane operations per SM clock, of each kind
+    of arithmetic the scan uses, with 1 to 8 warps per SM sub-partition and
+    8 or 16 independent chains per thread (1 to 16 for the scan's state
+    update, whose chains are the state pairs a thread holds) (the library's
+    mamba_probe_pipe_rate, clock64 inside the kernel)."""
+    import torch
+    import selective_state_space_135_b300 as mm
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    torch.cuda.set_device(0)
+    rows = []
+    for kind in sorted(PIPE_KINDS):
+        for wps in (1, 2, 3, 4, 5, 8):
+            for chains in (1, 2, 4, 8, 16):
+                if kind != 5 and chains not in (8, 16):
+                    continue
+                try:
+                    rate, cyc = mm.mamba_probe_pipe_rate(kind, wps, chains, iters=4096)
+                except mm.MambaError:
+                    continue   # more registers than the SM has at this warp count
+                rows.append({"kind": PIPE_KINDS[kind], "warps_per_subpartition": wps,
+                             "chains": chains, "ops_per_clk_sm": round(rate, 3),
+                             "cycles": int(cyc)})
+    peaks, src = load_peaks()
+    smax = float(peaks.get("sm_max_mhz", 2032.0))
+    best = {}
+    for r in rows:
+        best[r["kind"]] = max(best.get(r["kind"], 0.0), r["ops_per_clk_sm"])
+    scan = best[PIPE_KINDS[5]]
+    print(json.dumps({
+        "pipe_rates": rows, "best_ops_per_clk_sm": best,
+        "scan_core_ceiling": {
+            "state_updates_per_clk_sm": scan,
+            "T_updates_per_s": scan * N_SM * smax * 1e6 / 1e12,
+            "m2p8_us": synth.M2P8.batch * synth.M2P8.dim * synth.M2P8.seqlen * synth.M2P8.dstate
+                       / (scan * N_SM * smax * 1e6) * 1e6,
+            "at_mhz": smax, "sm_count": N_SM},
+    }), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------
 # our arm
 
 def run_ours(args, shape):
@@ -266,6 +315,7 @@ def run_ours(args, shape):
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
     import selective_state_space_135_b300 as mm
+    mm.mamba_scan_set_tuning(0, 0, 0, args.layout)
 
     seed = rank_seed(shape, rank)
     inp = synth.scan_inputs(shape, seed=seed)
@@ -635,7 +685,14 @@ def main():
     ap.add_argument("--no-bwd", action="store_true")
     ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layout", type=int, choices=[0, 1, 2], default=0,
+                    help="scan kernel for dstate 9..16: 0 automatic, 1 lane per channel, "
+                         "2 state split over four warps")
+    ap.add_argument("--pipe-rates", action="store_true",
+                    help="only measure the per-SM arithmetic rates the roofline is built on")
     args = ap.parse_args()
+    if args.pipe_rates:
+        return run_pipe_rates()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     shape = synth.SCAN_SHAPES[args.workload]

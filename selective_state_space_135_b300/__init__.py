@@ -23,6 +23,7 @@ from ._lib import (  # noqa: F401
     mamba_conv1d_update,
     mamba_device_status,
     mamba_profile_begin,
+    mamba_probe_pipe_rate,
     mamba_profile_end,
     mamba_scan_bwd,
     mamba_scan_fwd,

@@ -19,7 +19,7 @@ EXPORTS = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_ex", "mam
            "mamba_conv1d_fwd", "mamba_conv1d_update", "mamba_state_update",
            "mamba_state_update_ex", "mamba_status_string", "mamba_device_status",
            "mamba_selftest_wait_timeout", "mamba_version", "mamba_scan_set_tuning",
-           "mamba_profile_begin", "mamba_profile_end")
+           "mamba_profile_begin", "mamba_profile_end", "mamba_probe_pipe_rate")
 
 # flags of the extended entry points
 MAMBA_FLAG_SOFTPLUS = 1
@@ -82,13 +82,17 @@ def load():
         lib.mamba_selftest_wait_timeout.restype = i32
         lib.mamba_version.argtypes = []
         lib.mamba_version.restype = i32
-        lib.mamba_scan_set_tuning.argtypes = [i32, i32, i32]
+        lib.mamba_scan_set_tuning.argtypes = [i32, i32, i32, i32]
         lib.mamba_scan_set_tuning.restype = i32
         lib.mamba_profile_begin.argtypes = []
         lib.mamba_profile_begin.restype = i32
         lib.mamba_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double),
                                           ctypes.POINTER(ctypes.c_int64), i32]
         lib.mamba_profile_end.restype = i32
+        lib.mamba_probe_pipe_rate.argtypes = [i32, i32, i32, i64,
+                                              ctypes.POINTER(ctypes.c_double),
+                                              ctypes.POINTER(ctypes.c_double), vp]
+        lib.mamba_probe_pipe_rate.restype = i32
         _lib = lib
         return lib
 
@@ -426,10 +430,27 @@ def mamba_selftest_wait_timeout(limit_us: int, stream=None) -> None:
         raise MambaError(rc, "mamba_selftest_wait_timeout")
 
 
-def mamba_scan_set_tuning(tail: int = 0, stages: int = 0, chunks: int = 0) -> None:
-    rc = load().mamba_scan_set_tuning(int(tail), int(stages), int(chunks))
+def mamba_scan_set_tuning(tail: int = 0, stages: int = 0, chunks: int = 0,
+                          layout: int = 0) -> None:
+    rc = load().mamba_scan_set_tuning(int(tail), int(stages), int(chunks), int(layout))
     if rc != 0:
         raise MambaError(rc, "mamba_scan_set_tuning")
+
+
+def mamba_probe_pipe_rate(kind: int, warps_per_subpartition: int, chains: int,
+                          iters: int = 4096, stream=None):
+    """Measurement support (not part of the scan): sustained lane operations
+    per SM clock of one kind of arithmetic; returns (rate, median CTA cycles)."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    rate = ctypes.c_double(0.0)
+    cyc = ctypes.c_double(0.0)
+    rc = load().mamba_probe_pipe_rate(int(kind), int(warps_per_subpartition), int(chains),
+                                      int(iters), ctypes.byref(rate), ctypes.byref(cyc),
+                                      _stream_handle(stream, dev))
+    if rc != 0:
+        raise MambaError(rc, "mamba_probe_pipe_rate")
+    return rate.value, cyc.value
 
 
 def mamba_profile_begin() -> None:
