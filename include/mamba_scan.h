@@ -119,7 +119,7 @@ typedef enum {
  * on the same stream.
  */
 int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
-                   int io_dtype,
+                   mamba_dtype_t io_dtype,
                    const void *u, const void *delta, const float *dt_bias,
                    const float *A, const void *B, const void *C,
                    const float *D_skip, const void *z, int softplus,
@@ -152,7 +152,7 @@ int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
  * clearing between calls.
  */
 int mamba_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
-                           int io_dtype,
+                           mamba_dtype_t io_dtype,
                            const void *u, const void *delta, const float *dt_bias,
                            const float *A, const void *B, const void *C,
                            const float *D_skip, const void *z, int softplus,
@@ -191,7 +191,7 @@ int mamba_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t dstate, int64_t s
  * is 0, final_state (if given) receives initial_state (or zeros).
  */
 int mamba_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
-                      int io_dtype,
+                      mamba_dtype_t io_dtype,
                       const void *u, const void *delta, const float *dt_bias,
                       const float *A, const void *B, const void *C,
                       const float *D_skip, const void *z, int flags,
@@ -212,7 +212,7 @@ int mamba_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen
  * Delta = softplus(delta + dt_bias) always (the generation step has no flag).
  * `state` must not overlap y or any input.  Allocates nothing.
  */
-int mamba_state_update(int64_t batch, int64_t dim, int64_t dstate, int io_dtype,
+int mamba_state_update(int64_t batch, int64_t dim, int64_t dstate, mamba_dtype_t io_dtype,
                        float *state, const void *x, const void *delta,
                        const float *dt_bias, const float *A,
                        const void *B, const void *C, const float *D_skip,
@@ -226,7 +226,7 @@ int mamba_state_update(int64_t batch, int64_t dim, int64_t dstate, int io_dtype,
  * With flags = MAMBA_FLAG_SOFTPLUS it is mamba_state_update.  The step that
  * follows a mamba_scan_fwd_ex prefill takes the same SOFTPLUS and ZOH bits.
  */
-int mamba_state_update_ex(int64_t batch, int64_t dim, int64_t dstate, int io_dtype,
+int mamba_state_update_ex(int64_t batch, int64_t dim, int64_t dstate, mamba_dtype_t io_dtype,
                           float *state, const void *x, const void *delta,
                           const float *dt_bias, const float *A,
                           const void *B, const void *C, const float *D_skip,
@@ -264,7 +264,7 @@ int mamba_state_update_ex(int64_t batch, int64_t dim, int64_t dstate, int io_dty
  * not overlap inputs or each other.
  */
 int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
-                   int io_dtype,
+                   mamba_dtype_t io_dtype,
                    const void *u, const void *delta, const float *dt_bias,
                    const float *A, const void *B, const void *C,
                    const float *D_skip, const void *z, int flags,
@@ -293,7 +293,7 @@ int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
  * final_conv_state must not overlap conv_state (MAMBA_ERR_ALIAS): ping-pong
  * two buffers to chain pieces of a sequence.  Allocates nothing.
  */
-int mamba_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int width, int io_dtype,
+int mamba_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int width, mamba_dtype_t io_dtype,
                      const void *x, const float *weight, const float *bias,
                      const void *conv_state, int silu, void *out, void *final_conv_state,
                      cudaStream_t stream);
@@ -304,7 +304,7 @@ int mamba_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int width, int 
  * then shifted by one and gets x[b,d] as its newest entry, in place.
  * Arguments as in mamba_conv1d_fwd (x, out: (batch, dim)).
  */
-int mamba_conv1d_update(int64_t batch, int64_t dim, int width, int io_dtype, void *conv_state,
+int mamba_conv1d_update(int64_t batch, int64_t dim, int width, mamba_dtype_t io_dtype, void *conv_state,
                         const void *x, const float *weight, const float *bias, int silu,
                         void *out, cudaStream_t stream);
 
@@ -339,12 +339,31 @@ int mamba_version(void);
  * time chunks, 3 cut into time chunks whose passes run on a library-owned
  * side stream beside the whole-sequence units; mamba_scan_fwd_noalloc
  * treats 3 as 2), stages = depth of the shared-memory input ring (1..4),
- * chunks = fixed number of time chunks for every channel tile.  0 restores
- * the automatic choice for that knob.  Results do not depend on these
- * settings beyond fp32 rounding order.  Returns MAMBA_ERR_SHAPE for values
- * out of range.
+ * chunks = fixed number of time chunks for every channel tile, layout =
+ * how the state of a channel is split for dstate 9..16 (1 over two warps,
+ * 8 entries a lane and 64 channels per CTA; 2 over four warps, 4 entries a
+ * lane and 32 channels per CTA, the automatic choice).  0 restores the
+ * automatic choice for that knob.  Results do not depend on these settings beyond fp32 rounding
+ * order.  Returns MAMBA_ERR_SHAPE for values out of range.
  */
-int mamba_scan_set_tuning(int tail, int stages, int chunks);
+int mamba_scan_set_tuning(int tail, int stages, int chunks, int layout);
+
+/*
+ * Measurement support, not part of the scan: the sustained per-SM rate of
+ * one kind of arithmetic, in lane operations per SM clock cycle, measured
+ * with the SM cycle counter (independent of the clock frequency).  One CTA
+ * per SM with warps_per_subpartition (1 to 8) warps on each of the four SM
+ * sub-partitions, `chains` (1, 2, 4, 8 or 16) independent dependency
+ * chains per thread, `iters` (1 .. 2^24) iterations of 16 operations per
+ * chain.  kind: 0 ex2.approx, 1 lg2.approx, 2 tanh.approx, 3 packed f32x2
+ * FMA (2 lane operations each), 4 fp32 FMA, 5 the scan's state update of a
+ * pair of entries (2 ex2 and 4 packed multiply/FMAs, counted as 2 state
+ * updates).  Writes the rate and the median CTA cycle count;
+ * allocates (cudaMalloc) a small buffer per call and synchronises `stream`.
+ * Returns MAMBA_ERR_SHAPE for arguments out of range.
+ */
+int mamba_probe_pipe_rate(int kind, int warps_per_subpartition, int chains, int64_t iters,
+                          double *ops_per_clk_sm, double *cycles_median, cudaStream_t stream);
 
 /*
  * Per-launch timing (process-wide).  After mamba_profile_begin, every kernel

@@ -214,7 +214,7 @@ using namespace mamba;
 
 extern "C" {
 
-int mamba_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int width, int io_dtype,
+int mamba_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int width, mamba_dtype_t io_dtype,
                      const void* x, const float* weight, const float* bias,
                      const void* conv_state, int silu, void* out, void* final_conv_state,
                      cudaStream_t stream) {
@@ -268,7 +268,7 @@ int mamba_conv1d_fwd(int64_t batch, int64_t dim, int64_t seqlen, int width, int 
     return e == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
 
-int mamba_conv1d_update(int64_t batch, int64_t dim, int width, int io_dtype, void* conv_state,
+int mamba_conv1d_update(int64_t batch, int64_t dim, int width, mamba_dtype_t io_dtype, void* conv_state,
                         const void* x, const float* weight, const float* bias, int silu, void* out,
                         cudaStream_t stream) {
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;

@@ -13,31 +13,35 @@
 // whose cost is one exp and four fp32 multiply/adds per state entry and step):
 //   * A CTA is four warps (one per SM sub-partition).  SPLIT warps share a
 //     block of 32 channels, one lane per channel, each warp holding 1/SPLIT
-//     of the N state entries in registers (SPLIT = 4 for dstate > 8: a CTA
-//     covers 32 channels; SPLIT = 2 otherwise: 64 channels).  Every B/C load
-//     of a warp is therefore a single-address broadcast, and the SM gets
-//     several warps per sub-partition even on the Mamba-2.8B layer.  The
-//     CTA walks time in tiles of one 64-byte row per channel (32 bf16 or 16
-//     fp32 steps).
+//     of the padded state in registers: for dstate > 8, SPLIT = 2 (8 entries
+//     a lane, 64 channels per CTA) when the channel tiles give every SM at
+//     least two, else SPLIT = 4 (4 entries a lane, 32 channels per CTA);
+//     SPLIT = 2 for dstate <= 8.  Every B/C load of a warp is therefore a
+//     single-address broadcast, and each SM sub-partition runs two or more
+//     warps (one warp alone cannot issue packed FMAs back to back).  The CTA
+//     walks time in tiles of one 32-byte row per channel (16 bf16 or 8 fp32
+//     steps).
 //   * u, delta, z and y tiles move by tensor-map bulk copies
-//     (cp.async.bulk.tensor, completion on an mbarrier ring), 64-byte swizzled
-//     so that the per-lane 16-byte row accesses are bank-conflict free.
+//     (cp.async.bulk.tensor, completion on an mbarrier ring), 32-byte
+//     swizzled so that the per-lane row accesses are bank-conflict free.
 //   * B and C (shared by all channels of a batch entry) are packed once per
 //     call by a small kernel into fp32 rows of (B pair, C pair) per step and
 //     staged by the same bulk copies.
 //   * Per tile each slice computes Delta and Delta*u for 1/SPLIT of the
-//     steps into shared memory, every slice runs the recurrence over the
-//     tile, and each slice finishes 1/SPLIT of the outputs (all partial sums
-//     C.h in a fixed order, skip term, gate): no per-token work is done twice.
+//     steps, two steps at a time with packed fp32x2 arithmetic, and writes
+//     them to shared memory as the duplicated operand pairs the step's
+//     packed multiplies take; every slice runs the recurrence over the
+//     tile; and each slice finishes 1/SPLIT of the outputs (all partial sums
+//     C.h in slice order, skip term, gate), again two steps at a time: no
+//     per-token work is done twice.
 //   * The expanded (b, d, t, n) tensor is never materialised: Abar and the
 //     input term live only in registers; the state leaves the SM only at the
 //     end of a work unit.
-//   * Work units are channel tiles over the whole sequence, one wave per SM;
-//     tiles that do not fill a whole wave, and all tiles when there are fewer
-//     than SMs, are cut into time chunks: a summary pass computes each
-//     chunk's (prod Abar, end state from zero), a carry pass composes them in
-//     order, and the main pass restarts every chunk from its exact
-//     carried-in state.
+//   * Work units are channel tiles over the whole sequence; tiles that do
+//     not fill a whole wave, and all tiles when there are fewer than SMs,
+//     are cut into time chunks: a summary pass computes each chunk's
+//     (prod Abar, end state from zero), a carry pass composes them in order,
+//     and the main pass restarts every chunk from its exact carried-in state.
 //   * bf16 I/O keeps Delta in log2 units (Delta' = Delta / ln 2, B scaled by
 //     ln 2 when packed) so that Abar = ex2(Delta' * A) needs one multiply and
 //     one hardware ex2; fp32 I/O uses the library expf/log1pf.  State and
@@ -163,25 +167,62 @@ constexpr int channels_per_cta() { return 32 * kScanWarps / SPLIT; }
 
 // One 16-byte chunk of a row <-> fp32 values (8 for bf16, 4 for fp32).
 template <typename T> struct Chunk;
+// One 16-byte chunk of a row <-> fp32 pairs of consecutive steps (4 pairs
+// for bf16, 2 for fp32), the operands of packed fp32x2 arithmetic.
 template <> struct Chunk<float> {
     static constexpr int G = 4;
-    __device__ static void load(const unsigned char* p, float* v) {
+    __device__ static void load(const unsigned char* p, float2* v) {
         const float4 r = *reinterpret_cast<const float4*>(p);
-        v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
+        v[0] = make_float2(r.x, r.y);
+        v[1] = make_float2(r.z, r.w);
     }
-    __device__ static void store(unsigned char* p, const float* v) {
-        *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+    __device__ static void store(unsigned char* p, const float2* v) {
+        *reinterpret_cast<float4*>(p) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
     }
 };
 template <> struct Chunk<__nv_bfloat16> {
     static constexpr int G = 8;
-    __device__ static void load(const unsigned char* p, float* v) {
-        IO<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(p), v);
+    __device__ static void load(const unsigned char* p, float2* v) {
+        const uint4 r = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            v[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
     }
-    __device__ static void store(unsigned char* p, const float* v) {
-        *reinterpret_cast<uint4*>(p) = IO<__nv_bfloat16>::pack(v);
+    __device__ static void store(unsigned char* p, const float2* v) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 q = __floats2bfloat162_rn(v[i].x, v[i].y);
+            w[i] = *reinterpret_cast<uint32_t*>(&q);
+        }
+        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 };
+
+// Softplus of two steps in log2 units: element by element the arithmetic
+// of softplus_log2_fast (each half of a packed operation rounds as the
+// scalar one), with the multiplies and adds packed in pairs.
+__device__ __forceinline__ float2 softplus2_log2(float2 t) {
+    const float2 x = make_float2(ex2_approx(-fabsf(t.x)), ex2_approx(-fabsf(t.y)));
+    const float2 series =
+        __fmul2_rn(x, __ffma2_rn(x, make_float2(-0.5f * kLog2e, -0.5f * kLog2e),
+                                 make_float2(kLog2e, kLog2e)));
+    const float2 xp1 = __fadd2_rn(x, make_float2(1.0f, 1.0f));
+    const float2 full = make_float2(lg2_approx(xp1.x), lg2_approx(xp1.y));
+    const float2 r = make_float2(x.x < 0.0078125f ? series.x : full.x,
+                                 x.y < 0.0078125f ? series.y : full.y);
+    return __fadd2_rn(make_float2(fmaxf(t.x, 0.0f), fmaxf(t.y, 0.0f)), r);
+}
+
+// silu of two values (silu_f, packed): accurate z / (1 + e^-z), or on the
+// fast path h + h * tanh(h) with h = z / 2.
+template <bool ACC>
+__device__ __forceinline__ float2 silu2(float2 z) {
+    if (ACC) return make_float2(silu_f<true>(z.x), silu_f<true>(z.y));
+    const float2 h = __fmul2_rn(z, make_float2(0.5f, 0.5f));
+    return __ffma2_rn(h, make_float2(tanh_approx(h.x), tanh_approx(h.y)), h);
+}
 
 // Packs B and C of every step into one fp32 row of 2*NP values, in the order
 // the scan reads them: for each pair j of state entries the float4
@@ -291,7 +332,8 @@ __device__ __forceinline__ Unit decode_unit(const ScanArgs& a, int idx) {
 //   [0, 1024)       stage mbarriers
 //   stage s         u | delta | z tiles (CH x 64 B each) | packed B/C (TT x 2*NP fp32)
 //   y tile          CH x 64 B
-//   du              (Delta, Delta*u) of every (step, channel) of a tile, float2
+//   du              (Delta, Delta*u) of every (step, channel) of a tile, as
+//                   float4 (Delta_t, Delta_t+1, du_t, du_t+1) per pair of steps
 //   part            sum_n C*h of each slice of the state for the steps other
 //                   slices finish, [SPLIT][TT - TT/SPLIT][CH] fp32
 template <typename T, int NT, int SPLIT>
@@ -376,7 +418,7 @@ __device__ __forceinline__ float2 input_term(int i, const float2& ab, const floa
 // bc holds the step's NT/2 float4 (B pair, C pair), the same for every lane
 // of the warp (on the fast path B carries the factor ln 2 that turns the
 // log2-unit Delta back into natural units).  All input terms are formed
-// before the state updates, and two accumulators halve the dependent chain.
+// before the state updates; sum_n C*h is one packed multiply-add chain.
 template <int NT, bool ACC, bool ZOH, bool STATE_ONLY>
 __device__ __forceinline__ float state_step(float2 (&h2)[NT / 2], const float2 (&ab)[NT / 2],
                                             const float2 (&a2)[NT / 2], const ZohK<NT>& zk,
@@ -389,19 +431,10 @@ __device__ __forceinline__ float state_step(float2 (&h2)[NT / 2], const float2 (
     if constexpr (STATE_ONLY) {
         return 0.0f;
     } else {
-        float2 acc0 = __fmul2_rn(make_float2(bc[0].z, bc[0].w), h2[0]);
-        if constexpr (NT == 2) {
-            return acc0.x + acc0.y;
-        } else {
-            float2 acc1 = __fmul2_rn(make_float2(bc[1].z, bc[1].w), h2[1]);
+        float2 acc = __fmul2_rn(make_float2(bc[0].z, bc[0].w), h2[0]);
 #pragma unroll
-            for (int i = 2; i < NT / 2; i += 2) {
-                acc0 = __ffma2_rn(make_float2(bc[i].z, bc[i].w), h2[i], acc0);
-                acc1 = __ffma2_rn(make_float2(bc[i + 1].z, bc[i + 1].w), h2[i + 1], acc1);
-            }
-            const float2 acc = __fadd2_rn(acc0, acc1);
-            return acc.x + acc.y;
-        }
+        for (int i = 1; i < NT / 2; ++i) acc = __ffma2_rn(make_float2(bc[i].z, bc[i].w), h2[i], acc);
+        return acc.x + acc.y;
     }
 }
 
@@ -416,7 +449,7 @@ __device__ __forceinline__ float fused_step(float2 (&h2)[NT / 2], const float2 (
                                             float du, const float4 (&bc)[NT / 2]) {
     const float2 dt2 = make_float2(dt_next, dt_next);
     const float2 du2 = make_float2(du, du);
-    float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
+    float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int i = 0; i < NT / 2; ++i) {
         if constexpr (ACC) {
@@ -431,18 +464,10 @@ __device__ __forceinline__ float fused_step(float2 (&h2)[NT / 2], const float2 (
         h2[i] = __ffma2_rn(ab[i], h2[i], bx);
         if constexpr (!STATE_ONLY) {
             const float2 cp = make_float2(bc[i].z, bc[i].w);
-            if (i & 1) acc1 = (i == 1) ? __fmul2_rn(cp, h2[i]) : __ffma2_rn(cp, h2[i], acc1);
-            else acc0 = (i == 0) ? __fmul2_rn(cp, h2[i]) : __ffma2_rn(cp, h2[i], acc0);
+            acc = i == 0 ? __fmul2_rn(cp, h2[i]) : __ffma2_rn(cp, h2[i], acc);
         }
     }
-    if constexpr (STATE_ONLY) {
-        return 0.0f;
-    } else if constexpr (NT == 2) {
-        return acc0.x + acc0.y;
-    } else {
-        const float2 acc = __fadd2_rn(acc0, acc1);
-        return acc.x + acc.y;
-    }
+    return STATE_ONLY ? 0.0f : acc.x + acc.y;
 }
 
 template <int NT>
@@ -514,7 +539,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     unsigned char* yt = smem + Lay::ybuf(stages);
-    float2* du_s = reinterpret_cast<float2*>(smem + Lay::du(stages));      // [TT][CH]
+    float4* du_s = reinterpret_cast<float4*>(smem + Lay::du(stages));      // [TT/2][CH]
     // [SPLIT][TT - HT][CH]: slice q's partial of step t sits at row
     // (t < q*HT ? t : t - HT), skipping the steps slice q finishes itself
     float* part_s = reinterpret_cast<float*>(smem + Lay::part(stages));
@@ -553,7 +578,9 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     }
     const float bias0 = (chan_ok && a.dt_bias) ? a.dt_bias[d] : 0.0f;
     const float bias = ACC ? bias0 : bias0 * kLog2e;
+    const float2 bias2 = make_float2(bias, bias);
     const float dsk = (chan_ok && a.D_skip) ? a.D_skip[d] : 0.0f;
+    const float2 dsk2 = make_float2(dsk, dsk);
     float dsum = 0.0f;  // sum of Delta over the unit (summary pass)
 
     const int ntens = has_z ? 3 : 2;
@@ -627,35 +654,41 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
         return false;
     };
 
-    // Delta (log2 units on the fast path) of one step from the raw delta value
-    auto delta_of = [&](float dv) -> float {
+    // Delta (log2 units on the fast path) of two steps from the raw delta values
+    auto delta2_of = [&](float2 dv) -> float2 {
         if constexpr (ACC) {
-            const float sarg = dv + bias;
-            return SOFTPLUS ? (sarg > 20.0f ? sarg : log1pf(expf(sarg))) : sarg;
+            const float2 sarg = __fadd2_rn(dv, bias2);
+            if (!SOFTPLUS) return sarg;
+            return make_float2(sarg.x > 20.0f ? sarg.x : log1pf(expf(sarg.x)),
+                               sarg.y > 20.0f ? sarg.y : log1pf(expf(sarg.y)));
         } else {
             // s * log2(e); softplus in log2 units: log2(1 + 2^tl)
-            const float tl = fmaf(dv, kLog2e, bias);
-            return SOFTPLUS ? (tl > 30.0f ? tl : lg2_approx(1.0f + ex2_approx(tl))) : tl;
+            const float2 tl = __ffma2_rn(dv, make_float2(kLog2e, kLog2e), bias2);
+            return SOFTPLUS ? softplus2_log2(tl) : tl;
         }
     };
 
     // (1) Delta and Delta*u (Euler) or u (zero-order hold) of this slice's
-    //     steps [hh*HT, hh*HT + HT) of a tile into du_s: independent chains,
-    //     back to back
+    //     steps [hh*HT, hh*HT + HT) of a tile into du_s, two steps at a time
+    //     with packed arithmetic: independent chains, back to back
     auto phase1 = [&](const unsigned char* st_, int nv_) {
 #pragma unroll
         for (int q = 0; q < QC; ++q) {
             const int ck = hh * QC + q;
             const int off = swz(c, ck);
-            float uv[G], dv[G];
+            float2 uv[G / 2], dv[G / 2];
             CK::load(st_ + Lay::kRows + off, dv);
             CK::load(st_ + off, uv);
 #pragma unroll
-            for (int j = 0; j < G; ++j) {
-                float v = delta_of(dv[j]);
-                const int t = ck * G + j;
-                if (t >= nv_) v = 0.0f;   // past the live steps: the state is kept
-                du_s[t * CH + c] = make_float2(v, ZOH ? (t >= nv_ ? 0.0f : uv[j]) : v * uv[j]);
+            for (int j = 0; j < G / 2; ++j) {
+                float2 v = delta2_of(dv[j]);
+                float2 du = ZOH ? uv[j] : __fmul2_rn(v, uv[j]);
+                const int t = ck * G + 2 * j;
+                if (nv_ < TT) {   // past the live steps the state is kept (uniform branch)
+                    if (t >= nv_) v.x = du.x = 0.0f;
+                    if (t + 1 >= nv_) v.y = du.y = 0.0f;
+                }
+                du_s[(t / 2) * CH + c] = make_float4(v.x, v.y, du.x, du.y);
             }
         }
     };
@@ -698,41 +731,43 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
             }
             (void)pseg;
             (void)mine;
-            float2 d0 = du_s[c];
-            float2 d1 = du_s[CH + c];
-            float2 ab[kNPair];
-            float4 bc[kNPair];
-            abar_step<NT, ACC>(ab, a2, d0.x);
-            load_bc<NT>(bc, bct);
+            // (Delta, Delta*u) of the pairs of steps in a ring of three
+            // (pair t/2 in slot (t/2) % 3, loaded two pairs ahead), Abar and
+            // the B/C row of the current and the next step in rings of two:
+            // every index is a compile-time constant of the unrolled loop, so
+            // nothing is copied from one step to the next
+            float4 qa[3];
+            float2 abuf[2][kNPair];
+            float4 bbuf[2][kNPair];
+            qa[0] = du_s[c];
+            qa[1] = du_s[CH + c];
+            qa[2] = qa[1];
+            abar_step<NT, ACC>(abuf[0], a2, qa[0].x);
+            load_bc<NT>(bbuf[0], bct);
 #pragma unroll
             for (int t = 0; t < TT; ++t) {
-                float2 d2 = d1;
-                float2 an[kNPair];
-                float4 bn[kNPair];
-                if (t + 2 < TT) d2 = du_s[(t + 2) * CH + c];
+                const int cur = t & 1, nxt = cur ^ 1;
+                const float4& q = qa[(t / 2) % 3];
+                const float dt = (t & 1) ? q.y : q.x;
+                const float du = (t & 1) ? q.w : q.z;
+                const float dtn = (t & 1) ? qa[(t / 2 + 1) % 3].x : q.y;   // Delta of step t+1
+                if (!(t & 1) && t + 4 < TT) qa[(t / 2 + 2) % 3] = du_s[(t / 2 + 2) * CH + c];
                 float pt;
                 if (t + 1 < TT) {
-                    load_bc<NT>(bn, bct + (t + 1) * (NP / 2));
-                    pt = fused_step<NT, ACC, ZOH, STATE_ONLY>(h2, ab, an, a2, zk, d1.x, d0.x, d0.y, bc);
+                    load_bc<NT>(bbuf[nxt], bct + (t + 1) * (NP / 2));
+                    pt = fused_step<NT, ACC, ZOH, STATE_ONLY>(h2, abuf[cur], abuf[nxt], a2, zk, dtn,
+                                                              dt, du, bbuf[cur]);
                 } else {
-                    pt = state_step<NT, ACC, ZOH, STATE_ONLY>(h2, ab, a2, zk, d0.x, d0.y, bc);
+                    pt = state_step<NT, ACC, ZOH, STATE_ONLY>(h2, abuf[cur], a2, zk, dt, du,
+                                                              bbuf[cur]);
                 }
                 if constexpr (STATE_ONLY) {
-                    dsum += d0.x;
+                    dsum += dt;
                 } else {
                     if (mine[t / HT])
                         own[t % HT] = pt;
                     else
                         pseg[t / HT][t * CH] = pt;
-                }
-                if (t + 1 < TT) {
-                    d0 = d1;
-                    d1 = d2;
-#pragma unroll
-                    for (int i = 0; i < kNPair; ++i) {
-                        ab[i] = an[i];
-                        bc[i] = bn[i];
-                    }
                 }
             }
         }
@@ -763,24 +798,26 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
             for (int q = 0; q < QC; ++q) {
                 const int ck = hh * QC + q;
                 const int off = swz(c, ck);
-                float uv[G], zv[G], ov[G];
+                float2 uv[G / 2], zv[G / 2], ov[G / 2];
                 (void)zv;
                 CK::load(ut + off, uv);
                 if constexpr (has_z) CK::load(zt + off, zv);
 #pragma unroll
-                for (int j = 0; j < G; ++j) {
-                    // own partial, then the other slices' in a fixed rotation
-                    float o = own[q * G + j];
+                for (int j = 0; j < G / 2; ++j) {
+                    // two steps: own partials, then the other slices' in a
+                    // fixed rotation
+                    const int i = q * G + 2 * j;
+                    float2 o = make_float2(own[i], own[i + 1]);
 #pragma unroll
-                    for (int k = 1; k < SPLIT; ++k) o += pk[k - 1][(q * G + j) * CH];
-                    o = fmaf(dsk, uv[j], o);
-                    if constexpr (has_z) o *= silu_f<ACC>(zv[j]);
+                    for (int k = 1; k < SPLIT; ++k)
+                        o = __fadd2_rn(o, make_float2(pk[k - 1][i * CH], pk[k - 1][(i + 1) * CH]));
+                    o = __ffma2_rn(dsk2, uv[j], o);
+                    if constexpr (has_z) o = __fmul2_rn(o, silu2<ACC>(zv[j]));
+                    if (EXT && ylim < TT) {   // uniform over the CTA
+                        if (i + hh * HT >= ylim) o.x = 0.0f;
+                        if (i + 1 + hh * HT >= ylim) o.y = 0.0f;
+                    }
                     ov[j] = o;
-                }
-                if (EXT && ylim < TT) {   // uniform over the CTA
-#pragma unroll
-                    for (int j = 0; j < G; ++j)
-                        if (q * G + j + hh * HT >= ylim) ov[j] = 0.0f;
                 }
                 CK::store(yt + off, ov);
             }
@@ -817,8 +854,11 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     if (tma) {
         if (aborted && tid == 0) {
             atomicExch(&g_error_word, 1);
-            // let copies still in flight land before the CTA's memory is released
-            for (int it = 0; it < issued; ++it)
+            // let copies still in flight land before the CTA's memory is
+            // released; only the last `stages` tiles issued can be in flight
+            // (every older one was consumed), and waiting on the parity of an
+            // older phase of the same barrier would not return until the bound
+            for (int it = max(0, issued - stages); it < issued; ++it)
                 (void)mbar_wait_bounded(smem_u32(&bars[it % stages]), (uint32_t)((it / stages) & 1));
         }
         if (!STATE_ONLY && tid == 0) bulk_wait_all();
@@ -988,7 +1028,7 @@ state_update16_kernel(const StepArgs a) {
             dtn = dt;
         } else {
             const float tl = fmaf(dv, kLog2e, bias * kLog2e);
-            dt = !SP ? tl : (tl > 30.0f ? tl : lg2_approx(1.0f + ex2_approx(tl)));
+            dt = SP ? softplus_log2_fast(tl) : tl;
             dtn = dt * kLn2;
         }
         du = dtn * xv;
@@ -1052,9 +1092,16 @@ struct Tuning {
     int tail = 0;    // 0 automatic, 1 whole units only, 2 chunk the tail, 3 ... on a side stream
     int stages = 0;  // ring depth (0 = automatic)
     int chunks = 0;  // time chunks for every group (0 = automatic)
+    int layout = 0;  // 0 automatic, 1 lane-per-channel kernel, 2 split-state kernel
 };
+
 Tuning g_tuning;
 std::mutex g_mu;
+
+Tuning get_tuning() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_tuning;
+}
 std::vector<cudaMemPool_t> g_pools;
 
 // Optional per-launch timing: while enabled, every kernel launch is bracketed
@@ -1174,15 +1221,8 @@ cudaError_t launch_scan(const ScanArgs& a, int grid, int smem, cudaStream_t st) 
 }
 
 // (state entries per lane NT, warps sharing a channel block SPLIT): padded
-// state NT * SPLIT of 4 -> (2, 2), 8 -> (4, 2), 16 -> (4, 4).  Measured on
-// B300 for dstate 16, four slices of 4 beat two of 8: half the channels per
-// CTA (45 KB of shared memory, five CTAs per SM) give each SM sub-partition
-// twice the warps to hide latency with, at about 6% more instructions.
-#if MAMBA_SPLIT16 == 2
-#define MAMBA_VARIANTS(X) X(2, 2) X(4, 2) X(8, 2)
-#else
-#define MAMBA_VARIANTS(X) X(2, 2) X(4, 2) X(4, 4)
-#endif
+// state NT * SPLIT of 4 -> (2, 2), 8 -> (4, 2), 16 -> (8, 2) or (4, 4).
+#define MAMBA_VARIANTS(X) X(2, 2) X(4, 2) X(8, 2) X(4, 4)
 
 // The summary pass reads no z, so it has no HAS_Z instances.
 template <typename T, bool STATE_ONLY, int NT, int S, int MODE>
@@ -1240,10 +1280,6 @@ int smem_bytes(int dt, int nt, int split, int stages) {
                             : smem_bytes_t<float>(nt, split, stages);
 }
 
-#ifndef MAMBA_SPLIT16
-#define MAMBA_SPLIT16 4
-#endif
-
 int smem_per_sm(int dev) {
     static std::vector<int> cache;
     std::lock_guard<std::mutex> lk(g_mu);
@@ -1279,25 +1315,28 @@ int smem_per_sm(int dev) {
 // chunks > 0 cuts every tile into that many chunks.  side_ok is false for
 // the no-allocation entry point, which uses the caller's stream only.
 Plan make_plan(int dev, int dt, long long batch, long long dim, int N, long long L, bool tma,
-               bool side_ok) {
-    Tuning tn;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        tn = g_tuning;
-    }
+               bool side_ok, const Tuning& tn) {
     Plan p;
     p.concurrent = false;
-    // padded state 4, 8 or 16; dstate > 8 splits it MAMBA_SPLIT16 ways
-    p.split = N > 8 ? MAMBA_SPLIT16 : 2;
+    const int sms = sm_count(dev);
+    // Padded state 4, 8 or 16, split over two warps (each lane holds 2 or 4
+    // entries; a CTA covers 64 channels) or, for dstate > 8, over four
+    // warps (4 entries per lane, 32 channels per CTA).  Measured on B300 for
+    // dstate 16, four slices of 4 beat two of 8 on both Mamba layer
+    // workloads: twice the warps per SM sub-partition hide the latency of
+    // the recurrence, and the two-way split reads about as much shared memory
+    // per state update as the four-way one saves in instructions.  layout 1
+    // forces the two-way split of 8 entries a lane.
     p.np = N <= 4 ? 4 : (N <= 8 ? 8 : 16);
+    const bool split4 = N > 8 && tn.layout != 1;
+    p.split = split4 ? 4 : 2;
     p.nt = p.np / p.split;
     p.ch = 32 * kScanWarps / p.split;
     p.tt = 64 / esize(dt);
-    const int sms = sm_count(dev);
     // at least two stages: the next tile is filled while this one finishes
     int stages = tma ? (tn.stages > 1 ? std::min(tn.stages, kMaxStages) : 2) : 2;
     int per_sm = smem_per_sm(dev) / (smem_bytes(dt, p.nt, p.split, stages) + 1024);
-    per_sm = std::max(1, std::min(per_sm, 16));
+    per_sm = std::max(1, std::min(per_sm, kScanMinBlocks));
     p.stages = stages;
     p.smem = smem_bytes(dt, p.nt, p.split, stages);
     p.groups_per_batch = (int)((dim + p.ch - 1) / p.ch);
@@ -1367,9 +1406,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 3-D map over a (d2, d1, d0) row-major tensor of `es`-byte elements, box
-// {b0, b1, 1}.
+// {b0, b1, 1}, with the 32- or 64-byte swizzle (swizzle = 32 or 64) or none (0).
 bool encode_map(CUtensorMap* m, const void* ptr, int es, bool is_bf16, long long d0,
-                long long d1, long long d2, int b0, int b1, bool swizzle) {
+                long long d1, long long d2, int b0, int b1, int swizzle) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
@@ -1380,7 +1419,9 @@ bool encode_map(CUtensorMap* m, const void* ptr, int es, bool is_bf16, long long
                                       : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                            3, const_cast<void*>(ptr), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           swizzle ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                           swizzle == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                         : (swizzle == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                          : CU_TENSOR_MAP_SWIZZLE_NONE),
                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1521,13 +1562,15 @@ int mamba_selftest_wait_timeout(int64_t limit_us, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
 
-int mamba_scan_set_tuning(int tail, int stages, int chunks) {
-    if (tail < 0 || tail > 3 || stages < 0 || stages > kMaxStages || chunks < 0)
+int mamba_scan_set_tuning(int tail, int stages, int chunks, int layout) {
+    if (tail < 0 || tail > 3 || stages < 0 || stages > kMaxStages || chunks < 0 || layout < 0 ||
+        layout > 2)
         return MAMBA_ERR_SHAPE;
     std::lock_guard<std::mutex> lk(g_mu);
     g_tuning.tail = tail;
     g_tuning.stages = stages;
     g_tuning.chunks = chunks;
+    g_tuning.layout = layout;
     return MAMBA_OK;
 }
 
@@ -1590,7 +1633,24 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     for (const void* q : {u, delta, z, (const void*)y})
         if (q && !aligned(q, 16)) tma = false;
 
-    Plan pl = make_plan(dev, io_dtype, batch, dim, (int)dstate, seqlen, tma, !no_alloc);
+    // The tuning is read once for the whole call.  The tensor maps of u,
+    // delta, z and y are encoded before anything is sized from the plan:
+    // if one cannot be encoded, the call is planned again without tensor
+    // maps, before any scratch is sized or allocated.
+    const Tuning tn = get_tuning();
+    Plan pl = make_plan(dev, io_dtype, batch, dim, (int)dstate, seqlen, tma, !no_alloc, tn);
+    ScanArgs a;
+    std::memset(&a, 0, sizeof(a));
+    if (tma) {
+        const bool bf = io_dtype == MAMBA_BF16;
+        const int tt = pl.tt;
+        const int sw = 64;   // the tile's row bytes: one 64-byte row per channel
+        tma = encode_map(&a.m_u, u, es, bf, seqlen, dim, batch, tt, pl.ch, sw) &&
+              encode_map(&a.m_dl, delta, es, bf, seqlen, dim, batch, tt, pl.ch, sw) &&
+              (!z || encode_map(&a.m_z, z, es, bf, seqlen, dim, batch, tt, pl.ch, sw)) &&
+              encode_map(&a.m_y, y, es, bf, seqlen, dim, batch, tt, pl.ch, sw);
+        if (!tma) pl = make_plan(dev, io_dtype, batch, dim, (int)dstate, seqlen, false, !no_alloc, tn);
+    }
     const bool chunked = pl.n_full < pl.n_groups && pl.nchunks > 1;
     const bool acc = io_dtype == MAMBA_F32;
 
@@ -1614,23 +1674,17 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
         }
     }
 
-    ScanArgs a;
-    std::memset(&a, 0, sizeof(a));
     a.bc = static_cast<const float4*>(scratch);
     if (chunked) {
         a.ws_P = reinterpret_cast<float*>(static_cast<char*>(scratch) + bc_bytes);
         a.ws_h = a.ws_P + entries * (pl.nchunks - 1);
     }
-    if (tma) {
-        const bool bf = io_dtype == MAMBA_BF16;
-        const int tt = pl.tt;
-        tma = encode_map(&a.m_u, u, es, bf, seqlen, dim, batch, tt, pl.ch, true) &&
-              encode_map(&a.m_dl, delta, es, bf, seqlen, dim, batch, tt, pl.ch, true) &&
-              (!z || encode_map(&a.m_z, z, es, bf, seqlen, dim, batch, tt, pl.ch, true)) &&
-              encode_map(&a.m_y, y, es, bf, seqlen, dim, batch, tt, pl.ch, true) &&
-              encode_map(&a.m_bc, scratch, 4, false, 2 * pl.np, seqlen, batch, 2 * pl.np, tt,
-                         false);
-        if (!tma) pl = make_plan(dev, io_dtype, batch, dim, (int)dstate, seqlen, false, !no_alloc);
+    // the packed table's map needs the scratch address (16-byte aligned from
+    // either source); the plan is fixed by now, so a failure is an error
+    if (tma && !encode_map(&a.m_bc, scratch, 4, false, 2 * pl.np, seqlen, batch, 2 * pl.np,
+                           pl.tt, 0)) {
+        if (!no_alloc) cudaFreeAsync(scratch, stream);
+        return MAMBA_ERR_CUDA;
     }
     a.u = u; a.delta = delta; a.z = z;
     a.dt_bias = dt_bias; a.A = A; a.D_skip = D_skip; a.y = y; a.final_state = final_state;
@@ -1701,7 +1755,7 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     return e == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
 
-int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io_dtype,
+int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, mamba_dtype_t io_dtype,
                    const void* u, const void* delta, const float* dt_bias, const float* A,
                    const void* B, const void* C, const float* D_skip, const void* z,
                    int softplus, void* y, float* final_state, cudaStream_t stream) {
@@ -1711,7 +1765,7 @@ int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, i
 }
 
 int mamba_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
-                           int io_dtype, const void* u, const void* delta,
+                           mamba_dtype_t io_dtype, const void* u, const void* delta,
                            const float* dt_bias, const float* A, const void* B, const void* C,
                            const float* D_skip, const void* z, int softplus, void* y,
                            float* final_state, cudaStream_t stream) {
@@ -1720,7 +1774,7 @@ int mamba_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t dstate, int64_t s
                            true);
 }
 
-int mamba_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io_dtype,
+int mamba_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, mamba_dtype_t io_dtype,
                       const void* u, const void* delta, const float* dt_bias, const float* A,
                       const void* B, const void* C, const float* D_skip, const void* z,
                       int flags, const float* initial_state, const int32_t* seqlens, void* y,
@@ -1793,7 +1847,7 @@ static int state_update_common(int64_t batch, int64_t dim, int64_t dstate, int i
     return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
 
-int mamba_state_update(int64_t batch, int64_t dim, int64_t dstate, int io_dtype, float* state,
+int mamba_state_update(int64_t batch, int64_t dim, int64_t dstate, mamba_dtype_t io_dtype, float* state,
                        const void* x, const void* delta, const float* dt_bias, const float* A,
                        const void* B, const void* C, const float* D_skip, const void* z, void* y,
                        cudaStream_t stream) {
@@ -1801,7 +1855,7 @@ int mamba_state_update(int64_t batch, int64_t dim, int64_t dstate, int io_dtype,
                                D_skip, z, MAMBA_FLAG_SOFTPLUS, y, stream);
 }
 
-int mamba_state_update_ex(int64_t batch, int64_t dim, int64_t dstate, int io_dtype,
+int mamba_state_update_ex(int64_t batch, int64_t dim, int64_t dstate, mamba_dtype_t io_dtype,
                           float* state, const void* x, const void* delta, const float* dt_bias,
                           const float* A, const void* B, const void* C, const float* D_skip,
                           const void* z, int flags, void* y, cudaStream_t stream) {

@@ -625,7 +625,7 @@ using namespace mamba;
 
 extern "C" {
 
-int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io_dtype,
+int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, mamba_dtype_t io_dtype,
                    const void* u, const void* delta, const float* dt_bias, const float* A,
                    const void* B, const void* C, const float* D_skip, const void* z, int flags,
                    const float* initial_state, const void* dy, const float* d_final_state,

@@ -239,12 +239,15 @@ def test_state_update_ex_flags(lib):
 
 
 def test_tuning_validation(lib):
-    assert lib.mamba_scan_set_tuning(4, 0, 0) == ESHAPE
-    assert lib.mamba_scan_set_tuning(-1, 0, 0) == ESHAPE
-    assert lib.mamba_scan_set_tuning(3, 0, 0) == OK
-    assert lib.mamba_scan_set_tuning(0, 9, 0) == ESHAPE
-    assert lib.mamba_scan_set_tuning(0, 0, -1) == ESHAPE
-    assert lib.mamba_scan_set_tuning(0, 0, 0) == OK
+    assert lib.mamba_scan_set_tuning(4, 0, 0, 0) == ESHAPE
+    assert lib.mamba_scan_set_tuning(-1, 0, 0, 0) == ESHAPE
+    assert lib.mamba_scan_set_tuning(3, 0, 0, 0) == OK
+    assert lib.mamba_scan_set_tuning(0, 9, 0, 0) == ESHAPE
+    assert lib.mamba_scan_set_tuning(0, 0, -1, 0) == ESHAPE
+    assert lib.mamba_scan_set_tuning(0, 0, 0, 3) == ESHAPE
+    assert lib.mamba_scan_set_tuning(0, 0, 0, -1) == ESHAPE
+    assert lib.mamba_scan_set_tuning(0, 0, 0, 2) == OK
+    assert lib.mamba_scan_set_tuning(0, 0, 0, 0) == OK
 
 
 def test_selftest_rejects_bad_limits(lib):
