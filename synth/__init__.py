@@ -127,6 +127,11 @@ class ScanShape:
     softplus: bool = True
     gate: bool = True
     seed: int = 1000
+    # u, delta and z drawn from one stream per (tensor, batch entry, channel)
+    # instead of one per tensor: any row can be regenerated alone, so
+    # sequences of a million steps need neither a full host copy nor a
+    # transfer back from the device to check sampled rows
+    rowwise: bool = False
 
     @property
     def elems(self) -> int:
@@ -172,7 +177,11 @@ LONG = ScanShape("long b1 d1536 n16 l262144", 1, 1536, 16, 262144,
                  dt_lo=-6.0, dt_hi=-4.0, seed=1003)
 DECODE = DecodeShape("decode b128 d5120 n16 x1024", 128, 5120, 16, 1024, seed=1004)
 
-SCAN_SHAPES = {"tiny": TINY, "m130": M130, "m2p8": M2P8, "long": LONG}
+# the length the induction-head result on the pages extrapolates to
+LONG1M = ScanShape("long1m b1 d1536 n16 l1048576", 1, 1536, 16, 1 << 20,
+                   dt_lo=-6.0, dt_hi=-4.0, seed=1005, rowwise=True)
+
+SCAN_SHAPES = {"tiny": TINY, "m130": M130, "m2p8": M2P8, "long": LONG, "long1m": LONG1M}
 
 
 def s4d_real_A(dim: int, dstate: int) -> np.ndarray:
@@ -188,6 +197,11 @@ def scan_inputs(shape: ScanShape, seed: Optional[int] = None) -> Dict[str, np.nd
     """
     s = shape.seed if seed is None else seed
     bt, d, n, l = shape.batch, shape.dim, shape.dstate, shape.seqlen
+    if shape.rowwise:
+        out = rowwise_small_inputs(shape, seed)
+        for k in ("u", "delta", "z"):
+            out[k] = np.stack([rows_block(shape, k, b, 0, d, seed) for b in range(bt)])
+        return out
     out = {
         "u": store(normal(s, "u", (bt, d, l)), shape.dtype),
         "delta": store(normal(s, "delta", (bt, d, l), shape.delta_scale), shape.dtype),
@@ -200,6 +214,73 @@ def scan_inputs(shape: ScanShape, seed: Optional[int] = None) -> Dict[str, np.nd
     }
     out["dtype"] = shape.dtype
     out["softplus"] = shape.softplus
+    return out
+
+
+def rows_block(shape: ScanShape, name: str, b: int, d0: int, d1: int,
+               seed: Optional[int] = None) -> np.ndarray:
+    """Storage-form rows [d0, d1) of batch entry b of tensor `name` (u, delta
+    or z) of a row-wise shape, shape (d1 - d0, L): row (b, d) comes from its
+    own stream keyed by (seed, name, b, d)."""
+    assert shape.rowwise
+    s = shape.seed if seed is None else seed
+    scale = shape.delta_scale if name == "delta" else 1.0
+    out = np.empty((d1 - d0, shape.seqlen), np.float32)
+    for i, d in enumerate(range(d0, d1)):
+        out[i] = normal(s, name, (shape.seqlen,), scale, b, d)
+    return store(out, shape.dtype)
+
+
+def rowwise_to_device(shape: ScanShape, name: str, device="cuda", seed: Optional[int] = None,
+                      block_rows: int = 32, threads: Optional[int] = None):
+    """Tensor `name` (u, delta or z) of a row-wise shape as a torch tensor on
+    `device`, generated in blocks of rows by a pool of host threads (numpy's
+    generators release the GIL) and copied block by block, so that no full
+    host copy is ever held."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    import torch
+    tdt = torch.bfloat16 if shape.dtype == BF16 else torch.float32
+    out = torch.empty((shape.batch, shape.dim, shape.seqlen), dtype=tdt, device=device)
+    jobs = [(b, d0, min(shape.dim, d0 + block_rows))
+            for b in range(shape.batch) for d0 in range(0, shape.dim, block_rows)]
+    nthr = threads or min(16, os.cpu_count() or 1)
+    with ThreadPoolExecutor(max_workers=nthr) as pool:
+        for (b, d0, d1), blk in zip(jobs, pool.map(
+                lambda j: rows_block(shape, name, j[0], j[1], j[2], seed), jobs)):
+            out[b, d0:d1].copy_(to_torch(blk, shape.dtype, "cpu"))
+    return out
+
+
+def rowwise_small_inputs(shape: ScanShape, seed: Optional[int] = None) -> Dict[str, np.ndarray]:
+    """The inputs of a row-wise shape other than u, delta and z: B, C, A,
+    dt_bias, D_skip (storage form / fp32), plus 'dtype' and 'softplus'."""
+    assert shape.rowwise
+    s = shape.seed if seed is None else seed
+    bt, d, n, l = shape.batch, shape.dim, shape.dstate, shape.seqlen
+    return {"B": store(normal(s, "B", (bt, n, l)), shape.dtype),
+            "C": store(normal(s, "C", (bt, n, l)), shape.dtype),
+            "A": s4d_real_A(d, n),
+            "dt_bias": uniform(s, "dt_bias", (d,), shape.dt_lo, shape.dt_hi),
+            "D_skip": normal(s, "D_skip", (d,)),
+            "dtype": shape.dtype, "softplus": shape.softplus}
+
+
+def rowwise_sample(shape: ScanShape, rows, seed: Optional[int] = None) -> Dict[str, np.ndarray]:
+    """The sampled rows (flat b*D + d indices, all of one batch entry) of a
+    row-wise shape as a problem of its own: batch 1, one channel per sampled
+    row, in the layout of scan_inputs (u, delta, z (1, R, L); B, C (1, N, L);
+    A (R, N); dt_bias, D_skip (R,))."""
+    small = rowwise_small_inputs(shape, seed)
+    rows = np.asarray(rows, np.int64)
+    bs, ds = rows // shape.dim, rows % shape.dim
+    assert np.all(bs == bs[0]), "rows of one batch entry"
+    b = int(bs[0])
+    out = {k: np.stack([rows_block(shape, k, b, int(d), int(d) + 1, seed)[0] for d in ds])[None]
+           for k in ("u", "delta", "z")}
+    out.update(B=small["B"][b:b + 1], C=small["C"][b:b + 1], A=small["A"][ds],
+               dt_bias=small["dt_bias"][ds], D_skip=small["D_skip"][ds],
+               dtype=shape.dtype, softplus=shape.softplus)
     return out
 
 

@@ -110,6 +110,35 @@ def test_long_bf16_sampled_rows():
     print("long", st)
 
 
+@pytest.mark.slow
+def test_long1m_bf16_sampled_rows():
+    """The million-step scan (the length the induction-head result on the
+    pages extrapolates to): 1 x 1536 channels x 1,048,576 steps, time-chunked
+    with a carry pass; 48 sampled rows against the oracle in full length,
+    plus every channel of the first and the last channel tile."""
+    torch = torch_mod()
+    import selective_state_space_135_b300 as mm
+    shp = synth.LONG1M
+    small = synth.rowwise_small_inputs(shp)
+    u, delta, z = (synth.rowwise_to_device(shp, k) for k in ("u", "delta", "z"))
+    y = torch.empty_like(u)
+    fin = torch.empty((shp.batch, shp.dim, shp.dstate), device="cuda")
+    mm.mamba_scan_fwd(u, delta, f32_dev(small["dt_bias"]), f32_dev(small["A"]),
+                      to_dev(small["B"], shp.dtype), to_dev(small["C"], shp.dtype),
+                      f32_dev(small["D_skip"]), z, True, y=y, final_state=fin)
+    torch.cuda.synchronize()
+    assert mm.mamba_device_status() == 0
+    rows = np.unique(np.concatenate([synth.sample_rows(9, shp.batch, shp.dim, 40),
+                                     [0, 1, 31, 32, shp.dim - 33, shp.dim - 1]]))
+    sub = synth.rowwise_sample(shp, rows)
+    w = oracle.scan_inputs_f64(sub)
+    yr, hr, _ = oracle.scan(w["u"], w["delta"], w["A"], w["B"], w["C"], dt_bias=w["dt_bias"],
+                            D_skip=w["D_skip"], z=w["z"])
+    assert_close(to_f64(y.reshape(-1, shp.seqlen)[rows]), yr[0], shp.dtype)
+    assert_close(to_f64(fin.reshape(-1, shp.dstate)[rows]), hr[0], shp.dtype, "final_state")
+    assert bool(torch.isfinite(y.float()).all())
+
+
 # --------------------------------------------------------------------------
 # odd shapes, ragged tails, nullable arguments
 

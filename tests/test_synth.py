@@ -7,6 +7,8 @@
   independent across names and steps.
 * The workload recipe: shapes, dtypes, A = -(n + 1), dt_bias within its
   range, and the means and spreads of the normal draws.
+* Row-wise streams (the million-step workload): any sampled rows equal the
+  same rows of the full tensors.
 """
 
 import numpy as np
@@ -89,3 +91,28 @@ def test_sample_rows():
     assert rows.min() >= 0 and rows.max() < 4 * 5120
     np.testing.assert_array_equal(rows, synth.sample_rows(5, 4, 5120, 384))
     assert len(synth.sample_rows(5, 1, 10, 50)) == 10
+
+
+def test_rowwise_streams_sample_equals_full():
+    # a row-wise shape draws every (batch, channel) row from its own stream:
+    # a sampled sub-problem equals the same rows of the full tensors, rows do
+    # not depend on the channel count, and the torch copy keeps the bits
+    shp = synth.ScanShape("rowwise", 2, 9, 4, 40, rowwise=True, seed=17)
+    full = synth.scan_inputs(shp)
+    rows = np.array([9 + 2, 9 + 5, 9 + 8])       # batch entry 1, channels 2, 5, 8
+    sub = synth.rowwise_sample(shp, rows)
+    for k in ("u", "delta", "z"):
+        assert np.array_equal(sub[k][0], full[k][1, [2, 5, 8]])
+    assert np.array_equal(sub["B"][0], full["B"][1]) and np.array_equal(sub["C"][0], full["C"][1])
+    assert np.array_equal(sub["A"], full["A"][[2, 5, 8]])
+    assert np.array_equal(sub["dt_bias"], full["dt_bias"][[2, 5, 8]])
+    wider = synth.ScanShape("rowwise", 2, 12, 4, 40, rowwise=True, seed=17)
+    assert np.array_equal(synth.rows_block(wider, "u", 1, 2, 3)[0], full["u"][1, 2])
+    again = synth.scan_inputs(shp)
+    assert all(np.array_equal(again[k], full[k]) for k in ("u", "delta", "z", "B", "C"))
+    import torch
+    dev = synth.rowwise_to_device(shp, "delta", device="cpu", block_rows=4, threads=3)
+    assert np.array_equal(dev.view(torch.int16).numpy().view(np.uint16), full["delta"])
+    # the 0.5 scale of delta and unit scale of u
+    assert abs(np.std(synth.widen(full["delta"], shp.dtype)) - 0.5) < 0.1
+    assert abs(np.std(synth.widen(full["u"], shp.dtype)) - 1.0) < 0.2
