@@ -143,9 +143,11 @@ int mamba_scan_fwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
  * 32 for dstate <= 4), so batch * seqlen up to 131072 fits at dstate 16
  * when no time chunks are needed.
  *
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls share the one array: calls whose
+ * Every call looks up the array's device address (cudaGetSymbolAddress,
+ * which allocates nothing) for the calling thread's current device and
+ * context, so the address is never stale.  The first call on a device may
+ * load the library's device code; make it before any stream capture.  All
+ * calls share the one array: calls whose
  * work overlaps on the GPU (different streams, or different host threads)
  * race on it and must be serialised by the caller.  Every byte a call reads
  * from the array is written earlier in the same call, so nothing needs

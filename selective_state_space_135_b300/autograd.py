@@ -47,6 +47,7 @@ class _ScanFn:
                 return y, final
 
             @staticmethod
+            @torch.autograd.function.once_differentiable
             def backward(ctx, dy, dfinal):
                 u, delta, dt_bias, A, B, C, D_skip, z, h0 = ctx.saved_tensors
                 if dy is None:

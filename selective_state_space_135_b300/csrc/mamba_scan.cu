@@ -159,7 +159,10 @@ constexpr int kScanWarps = 4;   // warps per CTA, one per SM sub-partition
 // each); saying so lets ptxas spend up to 102 registers a thread on running
 // the exponentials of the coming steps further ahead.  Measured on B300: the
 // Mamba-130M layer scan 187 -> 163 us, the Mamba-2.8B layer 234 -> 218 us.
-constexpr int kScanMinBlocks = 5;
+#ifndef MAMBA_SCAN_MIN_BLOCKS
+#define MAMBA_SCAN_MIN_BLOCKS 5
+#endif
+constexpr int kScanMinBlocks = MAMBA_SCAN_MIN_BLOCKS;
 // SPLIT warps share a block of 32 channels, each holding 1/SPLIT of the
 // state; a CTA therefore covers 32 * kScanWarps / SPLIT channels.
 template <int SPLIT>
@@ -1437,22 +1440,17 @@ bool encode_map(CUtensorMap* m, const void* ptr, int es, bool is_bf16, long long
 // cudaGetSymbolAddress (noalloc_scratch below).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MAMBA_NOALLOC_SCRATCH_BYTES];
 
-std::vector<void*> g_noalloc_ptr;   // device address of g_noalloc_scratch, per device
-
-// Device address of the fixed scratch on `dev` (the current device).  The
-// first call on a device looks it up; later calls reuse it.
-int noalloc_scratch(int dev, void** out) {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if ((int)g_noalloc_ptr.size() <= dev) g_noalloc_ptr.resize(dev + 1, nullptr);
-    if (!g_noalloc_ptr[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
-            cudaGetLastError();
-            return MAMBA_ERR_CUDA;
-        }
-        g_noalloc_ptr[dev] = ptr;
+// Device address of the fixed scratch for the calling thread's current
+// device and context.  It is looked up on every call (a host-side lookup
+// that allocates nothing), so it is never stale: not after cudaDeviceReset,
+// nor when a caller switches contexts.
+int noalloc_scratch(void** out) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return MAMBA_ERR_CUDA;
     }
-    *out = g_noalloc_ptr[dev];
+    *out = ptr;
     return MAMBA_OK;
 }
 
@@ -1662,7 +1660,7 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     void* scratch = nullptr;
     if (no_alloc) {
         if (bc_bytes + ws_bytes > (size_t)MAMBA_NOALLOC_SCRATCH_BYTES) return MAMBA_ERR_TOO_BIG;
-        const int rc = noalloc_scratch(dev, &scratch);
+        const int rc = noalloc_scratch(&scratch);
         if (rc != MAMBA_OK) return rc;
     } else {
         cudaMemPool_t pool = nullptr;

@@ -194,3 +194,16 @@ def test_autograd_wrapper_matches_the_backward_call():
                            C.detach(), dsk.detach(), z.detach(), dy)
     torch.cuda.synchronize()
     assert torch.equal(u.grad, g3["du"])
+
+
+@pytest.mark.slow
+def test_bwd_fills_the_gpu_bf16():
+    """bf16, batch 2 x 1536 channels x N 16 x 2048 steps: 96 groups of 32
+    channels, more than one per SM, so the dB / dC reductions over the
+    channels add many per-warp partials.  Every gradient, with an initial
+    state and a final-state gradient, element by element against the oracle."""
+    shp, inp = _inputs(synth.BF16, 2, 1536, 16, 2048, seed=61)
+    grads, ref = _run(inp, h0=True, dfinal=True)
+    _check(grads, ref, synth.BF16)
+    import selective_state_space_135_b300 as mm
+    assert mm.mamba_device_status() == 0
