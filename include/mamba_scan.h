@@ -87,7 +87,8 @@ typedef enum {
     MAMBA_ERR_DTYPE = -7,    /* io_dtype is not one of mamba_dtype_t */
     MAMBA_ERR_ALIAS = -8,    /* an output overlaps an input */
     MAMBA_ERR_TOO_BIG = -9,  /* needs more than MAMBA_NOALLOC_SCRATCH_BYTES of scratch */
-    MAMBA_ERR_FLAGS = -10    /* a flags argument has a bit the call does not know */
+    MAMBA_ERR_FLAGS = -10,   /* a flags argument has a bit the call does not know */
+    MAMBA_ERR_BOUNDS = -11   /* a debug build's index check failed (mamba_device_status) */
 } mamba_status_t;
 
 /* Bits of the `flags` argument of the extended entry points. */
@@ -315,10 +316,33 @@ const char *mamba_status_string(int status);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error
- * word.  Returns MAMBA_OK, MAMBA_ERR_TIMEOUT (a bounded device wait gave up;
- * the affected outputs are incomplete) or MAMBA_ERR_CUDA.
+ * words.  Returns MAMBA_OK, MAMBA_ERR_TIMEOUT (a bounded device wait gave up;
+ * the affected outputs are incomplete), MAMBA_ERR_BOUNDS (debug builds only:
+ * an index check failed and its access was skipped) or MAMBA_ERR_CUDA.
  */
 int mamba_device_status(cudaStream_t stream);
+
+/*
+ * Debug builds.  The library built with -DMAMBA_DEBUG (libmamba_scan_debug.so
+ * beside libmamba_scan.so; the Python binding loads it when the environment
+ * has MAMBA_SCAN_LIBRARY=debug) checks the element index of every global
+ * load and store of the scan, generation-step, B/C packing, carry and
+ * convolution kernels against the extent of its buffer, and of every
+ * tensor-map copy's box origin.  A failed check skips the access (a load
+ * reads 0), records the source line and makes the next mamba_device_status
+ * return MAMBA_ERR_BOUNDS; nothing traps.  In a release build the checks
+ * compile to nothing.
+ *
+ * mamba_debug_build returns 1 in a debug build, 0 otherwise, and writes the
+ * source line of the last failed check that mamba_device_status reported
+ * (0 if none) to *last_failed_line when that is not NULL.
+ * mamba_selftest_bounds launches one thread that checks an index one past
+ * the end of an extent without accessing any memory: in a debug build the
+ * next mamba_device_status returns MAMBA_ERR_BOUNDS, in a release build it
+ * returns MAMBA_OK.
+ */
+int mamba_debug_build(int *last_failed_line);
+int mamba_selftest_bounds(cudaStream_t stream);
 
 /*
  * Self-test of the failure path of the bounded device waits.  Launches one

@@ -21,6 +21,7 @@ from ._lib import (  # noqa: F401
     load,
     mamba_conv1d_fwd,
     mamba_conv1d_update,
+    mamba_debug_build,
     mamba_device_status,
     mamba_profile_begin,
     mamba_probe_pipe_rate,
@@ -30,6 +31,7 @@ from ._lib import (  # noqa: F401
     mamba_scan_fwd_ex,
     mamba_scan_fwd_noalloc,
     mamba_scan_set_tuning,
+    mamba_selftest_bounds,
     mamba_selftest_wait_timeout,
     mamba_state_update,
     mamba_state_update_ex,

@@ -7,7 +7,10 @@ import os
 import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB = os.path.join(HERE, "libmamba_scan.so")
+# MAMBA_SCAN_LIBRARY=debug selects the build whose kernels check the index
+# of every global access (same entry points, same results)
+_LIB = os.path.join(HERE, "libmamba_scan_debug.so" if os.environ.get("MAMBA_SCAN_LIBRARY") == "debug"
+                    else "libmamba_scan.so")
 _lock = threading.Lock()
 _lib = None
 
@@ -19,7 +22,8 @@ EXPORTS = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_ex", "mam
            "mamba_conv1d_fwd", "mamba_conv1d_update", "mamba_state_update",
            "mamba_state_update_ex", "mamba_status_string", "mamba_device_status",
            "mamba_selftest_wait_timeout", "mamba_version", "mamba_scan_set_tuning",
-           "mamba_profile_begin", "mamba_profile_end", "mamba_probe_pipe_rate")
+           "mamba_profile_begin", "mamba_profile_end", "mamba_probe_pipe_rate",
+           "mamba_debug_build", "mamba_selftest_bounds")
 
 # flags of the extended entry points
 MAMBA_FLAG_SOFTPLUS = 1
@@ -93,6 +97,10 @@ def load():
                                               ctypes.POINTER(ctypes.c_double),
                                               ctypes.POINTER(ctypes.c_double), vp]
         lib.mamba_probe_pipe_rate.restype = i32
+        lib.mamba_debug_build.argtypes = [ctypes.POINTER(ctypes.c_int)]
+        lib.mamba_debug_build.restype = i32
+        lib.mamba_selftest_bounds.argtypes = [vp]
+        lib.mamba_selftest_bounds.restype = i32
         _lib = lib
         return lib
 
@@ -451,6 +459,23 @@ def mamba_probe_pipe_rate(kind: int, warps_per_subpartition: int, chains: int,
     if rc != 0:
         raise MambaError(rc, "mamba_probe_pipe_rate")
     return rate.value, cyc.value
+
+
+def mamba_debug_build():
+    """(is this the debug build, source line of the last failed index check
+    reported by mamba_device_status or 0)."""
+    line = ctypes.c_int(0)
+    flag = load().mamba_debug_build(ctypes.byref(line))
+    return bool(flag), line.value
+
+
+def mamba_selftest_bounds(stream=None) -> None:
+    """Launch the index-check self-test (see include/mamba_scan.h)."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    rc = load().mamba_selftest_bounds(_stream_handle(stream, dev))
+    if rc != 0:
+        raise MambaError(rc, "mamba_selftest_bounds")
 
 
 def mamba_profile_begin() -> None:

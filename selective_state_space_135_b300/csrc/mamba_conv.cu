@@ -65,17 +65,18 @@ conv1d_kernel(const T* __restrict__ x, const float* __restrict__ w, const float*
     const long long row = blockIdx.x;
     const long long d = row % dim;
     const int lane = threadIdx.x & 31;
-    const T* xr = x + row * L;
-    const T* sr = state ? state + row * S : nullptr;
-    T* orow = out + row * L;
+    // extents for the index checks of debug builds (one CTA per row)
+    const long long rows = gridDim.x, nx = rows * L, ns = rows * S;
+    (void)nx; (void)ns;
     float wk[W];
 #pragma unroll
-    for (int k = 0; k < W; ++k) wk[k] = w[d * W + k];
-    const float b0 = bias ? bias[d] : 0.0f;
+    for (int k = 0; k < W; ++k) wk[k] = MAMBA_LD(w, d * W + k, dim * W);
+    const float b0 = bias ? MAMBA_LD(bias, d, dim) : 0.0f;
     const long long runs = (L + kConvRun - 1) / kConvRun;
     // the input at position s of the padded row (s < 0: the carried state)
     auto xp = [&](long long s) -> float {
-        return s >= 0 ? IO<T>::to_f(xr[s]) : (sr ? IO<T>::to_f(sr[S + s]) : 0.0f);
+        return s >= 0 ? IO<T>::to_f(MAMBA_LD(x, row * L + s, nx))
+                      : (state ? IO<T>::to_f(MAMBA_LD(state, row * S + S + s, ns)) : 0.0f);
     };
     for (long long r0 = 0; r0 < runs; r0 += kConvThreads) {   // uniform over the CTA
         const long long c = r0 + threadIdx.x;
@@ -85,13 +86,16 @@ conv1d_kernel(const T* __restrict__ x, const float* __restrict__ w, const float*
         float v[kConvRun + S];
         if (act && vec && full) {
             float r[kConvRun];
-            load_run<T>(xr + t0, r);
+#pragma unroll
+            for (int j = 0; j < kConvRun; ++j) r[j] = 0.0f;
+            if (MAMBA_IN(row * L + t0, nx) && MAMBA_IN(row * L + t0 + kConvRun - 1, nx))
+                load_run<T>(x + row * L + t0, r);
 #pragma unroll
             for (int j = 0; j < kConvRun; ++j) v[S + j] = r[j];
         } else {
 #pragma unroll
             for (int j = 0; j < kConvRun; ++j)
-                v[S + j] = (act && t0 + j < L) ? IO<T>::to_f(xr[t0 + j]) : 0.0f;
+                v[S + j] = (act && t0 + j < L) ? IO<T>::to_f(MAMBA_LD(x, row * L + t0 + j, nx)) : 0.0f;
         }
 #pragma unroll
         for (int j = 0; j < S; ++j) {
@@ -108,19 +112,22 @@ conv1d_kernel(const T* __restrict__ x, const float* __restrict__ w, const float*
             o[j] = conv_act<ACC>(acc, SILU);
         }
         if (vec && full) {
-            store_run<T>(orow + t0, o);
+            if (MAMBA_IN(row * L + t0, nx) && MAMBA_IN(row * L + t0 + kConvRun - 1, nx))
+                store_run<T>(out + row * L + t0, o);
         } else {
 #pragma unroll
             for (int j = 0; j < kConvRun; ++j)
-                if (t0 + j < L) orow[t0 + j] = IO<T>::from_f(o[j]);
+                if (t0 + j < L) MAMBA_ST(out, row * L + t0 + j, nx, IO<T>::from_f(o[j]));
         }
         // the run holding t = L-1 writes the state after the last input
         if (state_out && c == runs - 1) {
 #pragma unroll
             for (int j = 0; j < S; ++j) {
                 const long long s = L - S + j;
-                state_out[row * S + j] =
-                    s >= 0 ? xr[s] : (sr ? sr[S + s] : IO<T>::from_f(0.0f));
+                MAMBA_ST(state_out, row * S + j, ns,
+                         s >= 0 ? MAMBA_LD(x, row * L + s, nx)
+                                : (state ? MAMBA_LD(state, row * S + S + s, ns)
+                                         : IO<T>::from_f(0.0f)));
             }
         }
     }
@@ -136,18 +143,21 @@ conv1d_update_kernel(T* __restrict__ state, const T* __restrict__ x, const float
     const long long row = (long long)blockIdx.x * kConvThreads + threadIdx.x;
     if (row >= rows) return;
     const long long d = row % dim;
+    const long long ns = rows * S;   // extent of the state (debug index checks)
+    (void)ns;
     float v[W];
 #pragma unroll
-    for (int j = 0; j < S; ++j) v[j] = IO<T>::to_f(state[row * S + j]);
-    const T xv = x[row];
+    for (int j = 0; j < S; ++j) v[j] = IO<T>::to_f(MAMBA_LD(state, row * S + j, ns));
+    const T xv = MAMBA_LD(x, row, rows);
     v[S] = IO<T>::to_f(xv);
-    float acc = bias ? bias[d] : 0.0f;
+    float acc = bias ? MAMBA_LD(bias, d, dim) : 0.0f;
 #pragma unroll
-    for (int k = 0; k < W; ++k) acc = fmaf(w[d * W + k], v[k], acc);
-    out[row] = IO<T>::from_f(conv_act<ACC>(acc, SILU));
+    for (int k = 0; k < W; ++k) acc = fmaf(MAMBA_LD(w, d * W + k, dim * W), v[k], acc);
+    MAMBA_ST(out, row, rows, IO<T>::from_f(conv_act<ACC>(acc, SILU)));
 #pragma unroll
-    for (int j = 0; j + 1 < S; ++j) state[row * S + j] = state[row * S + j + 1];
-    if constexpr (S > 0) state[row * S + S - 1] = xv;
+    for (int j = 0; j + 1 < S; ++j)
+        MAMBA_ST(state, row * S + j, ns, MAMBA_LD(state, row * S + j + 1, ns));
+    if constexpr (S > 0) MAMBA_ST(state, row * S + S - 1, ns, xv);
 }
 
 template <typename T, int W>
@@ -208,6 +218,9 @@ cudaError_t dispatch_conv_update(int width, bool silu, void* state, const void* 
 }
 
 }  // namespace
+
+int conv_take_debug_word() { return take_debug_word(); }
+
 }  // namespace mamba
 
 using namespace mamba;

@@ -54,6 +54,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <type_traits>
@@ -244,14 +245,15 @@ __global__ void pack_bc_kernel(const T* __restrict__ B, const T* __restrict__ C,
         const long long b = bj / half;
         const int j = (int)(bj - b * half);
         const int n0 = 2 * j, n1 = 2 * j + 1;
-        const T* Bb = B + b * N * L + t;
-        const T* Cb = C + b * N * L + t;
+        const long long nbc = batch * N * L;   // extent of B and C
+        (void)nbc;
+        const long long i0 = b * N * L + (long long)n0 * L + t, i1 = i0 + L;
         float4 v;
-        v.x = n0 < N ? scale * IO<T>::to_f(Bb[(long long)n0 * L]) : 0.0f;
-        v.y = n1 < N ? scale * IO<T>::to_f(Bb[(long long)n1 * L]) : 0.0f;
-        v.z = n0 < N ? IO<T>::to_f(Cb[(long long)n0 * L]) : 0.0f;
-        v.w = n1 < N ? IO<T>::to_f(Cb[(long long)n1 * L]) : 0.0f;
-        out[(b * L + t) * half + j] = v;
+        v.x = n0 < N ? scale * IO<T>::to_f(MAMBA_LD(B, i0, nbc)) : 0.0f;
+        v.y = n1 < N ? scale * IO<T>::to_f(MAMBA_LD(B, i1, nbc)) : 0.0f;
+        v.z = n0 < N ? IO<T>::to_f(MAMBA_LD(C, i0, nbc)) : 0.0f;
+        v.w = n1 < N ? IO<T>::to_f(MAMBA_LD(C, i1, nbc)) : 0.0f;
+        MAMBA_ST(out, (b * L + t) * half + j, total, v);
     }
 }
 
@@ -533,11 +535,16 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     const bool tma = a.use_tma != 0;
     const int ntiles = (int)((w.t1 - w.t0 + TT - 1) / TT);
     const int wrow = (w.tail >= 0) ? w.tail * CH + c : 0;
+    // extents for the index checks of debug builds
+    const long long big_extent = (long long)a.batch * dim * L_;
+    const long long ws_extent = (long long)(a.nchunks - 1) * a.tail_rows * N;
+    (void)big_extent;
+    (void)ws_extent;
     // steps in use for this batch entry: past them Delta is 0 (the state is
     // kept) and y is 0
     long long t_end = w.t1;   // end of the live steps of this unit
     if constexpr (EXT) {
-        if (a.seqlens) t_end = min(t_end, max(0LL, (long long)a.seqlens[w.b]));
+        if (a.seqlens) t_end = min(t_end, max(0LL, (long long)MAMBA_LD(a.seqlens, w.b, a.batch)));
     }
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -561,13 +568,15 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
         for (int j = 0; j < 2; ++j) {
             const int n = hh * NT + 2 * i + j;
             const bool ok = chan_ok && n < N;
-            av[j] = ok ? a.A[(long long)d * N + n] : 0.0f;
+            av[j] = ok ? MAMBA_LD(a.A, (long long)d * N + n, dim * N) : 0.0f;
             float h0 = 0.0f;
             if (ok) {
                 if (w.tail >= 0 && w.k > 0) {
-                    if (!STATE_ONLY) h0 = a.ws_h[((long long)(w.k - 1) * a.tail_rows + wrow) * N + n];
+                    if (!STATE_ONLY)
+                        h0 = MAMBA_LD(a.ws_h, ((long long)(w.k - 1) * a.tail_rows + wrow) * N + n,
+                                      ws_extent);
                 } else if (EXT && a.h0) {
-                    h0 = a.h0[row * N + n];
+                    h0 = MAMBA_LD(a.h0, row * N + n, (long long)a.batch * dim * N);
                 }
             }
             hv[j] = h0;
@@ -579,10 +588,10 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
         zk.ia[i] = make_float2(iv[0], iv[1]);
         zk.e[i] = make_float2(ev[0], ev[1]);
     }
-    const float bias0 = (chan_ok && a.dt_bias) ? a.dt_bias[d] : 0.0f;
+    const float bias0 = (chan_ok && a.dt_bias) ? MAMBA_LD(a.dt_bias, d, dim) : 0.0f;
     const float bias = ACC ? bias0 : bias0 * kLog2e;
     const float2 bias2 = make_float2(bias, bias);
-    const float dsk = (chan_ok && a.D_skip) ? a.D_skip[d] : 0.0f;
+    const float dsk = (chan_ok && a.D_skip) ? MAMBA_LD(a.D_skip, d, dim) : 0.0f;
     const float2 dsk2 = make_float2(dsk, dsk);
     float dsum = 0.0f;  // sum of Delta over the unit (summary pass)
 
@@ -591,6 +600,8 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     // thread 0: tensor-map copies of tile `it` into stage `s`
     auto issue_tile = [&](int it, int s) {
         const int tt0 = (int)(w.t0 + (long long)it * TT);
+        // box origins inside the tensors (the copies themselves clip)
+        (void)(MAMBA_IN(tt0, L_) && MAMBA_IN(w.d0, dim) && MAMBA_IN(w.b, a.batch));
         const uint32_t bar = smem_u32(&bars[s]);
         unsigned char* st = smem + Lay::stage(s);
         mbar_arrive_expect_tx(bar, (uint32_t)(ntens * Lay::kRows + Lay::kBCBytes));
@@ -611,14 +622,16 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
             const int cc = rem / TT, t = rem % TT;
             const T* src = static_cast<const T*>(tsr == 0 ? a.u : (tsr == 1 ? a.delta : a.z));
             T v = IO<T>::from_f(0.0f);
-            if (cc < rows_valid && t < nv) v = src[((long long)w.b * dim + w.d0 + cc) * L_ + tt0 + t];
+            if (cc < rows_valid && t < nv)
+                v = MAMBA_LD(src, ((long long)w.b * dim + w.d0 + cc) * L_ + tt0 + t, big_extent);
             const int byte = t * (int)sizeof(T);
             *reinterpret_cast<T*>(st + tsr * Lay::kRows + swz(cc, byte >> 4) + (byte & 15)) = v;
         }
         float4* bcs = reinterpret_cast<float4*>(st + 3 * Lay::kRows);
         for (int e = tid; e < TT * (NP / 2); e += kNThr) {
             const int t = e / (NP / 2), j = e % (NP / 2);
-            bcs[e] = t < nv ? a.bc[((long long)w.b * L_ + tt0 + t) * (NP / 2) + j]
+            bcs[e] = t < nv ? MAMBA_LD(a.bc, ((long long)w.b * L_ + tt0 + t) * (NP / 2) + j,
+                                       (long long)a.batch * L_ * (NP / 2))
                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
     };
@@ -840,8 +853,9 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                     const int cc = e / TT, t = e % TT;
                     if (cc < rows_valid && t < nv) {
                         const int byte = t * (int)sizeof(T);
-                        static_cast<T*>(a.y)[((long long)w.b * dim + w.d0 + cc) * L_ + tt0 + t] =
-                            *reinterpret_cast<const T*>(yt + swz(cc, byte >> 4) + (byte & 15));
+                        MAMBA_ST(static_cast<T*>(a.y),
+                                 ((long long)w.b * dim + w.d0 + cc) * L_ + tt0 + t, big_extent,
+                                 *reinterpret_cast<const T*>(yt + swz(cc, byte >> 4) + (byte & 15)));
                     }
                 }
             }
@@ -883,10 +897,10 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
             if (STATE_ONLY) {
                 const long long idx = ((long long)w.k * a.tail_rows + wrow) * N + n;
                 const float an = j ? a2[i].y : a2[i].x;
-                a.ws_P[idx] = ACC ? expf(an * dsum) : ex2_approx(an * dsum);
-                a.ws_h[idx] = hv;
+                MAMBA_ST(a.ws_P, idx, ws_extent, ACC ? expf(an * dsum) : ex2_approx(an * dsum));
+                MAMBA_ST(a.ws_h, idx, ws_extent, hv);
             } else if (a.final_state && w.t1 == L_) {
-                a.final_state[row * N + n] = hv;
+                MAMBA_ST(a.final_state, row * N + n, (long long)a.batch * dim * N, hv);
             }
         }
     }
@@ -901,8 +915,10 @@ __global__ void carry_kernel(float* __restrict__ ws_P, float* __restrict__ ws_h,
     float h = 0.0f;
     for (int k = 0; k + 1 < nchunks; ++k) {
         const long long idx = (long long)k * entries + i;
-        h = ws_P[idx] * h + ws_h[idx];
-        ws_h[idx] = h;
+        const long long ext = (long long)(nchunks - 1) * entries;
+        (void)ext;
+        h = MAMBA_LD(ws_P, idx, ext) * h + MAMBA_LD(ws_h, idx, ext);
+        MAMBA_ST(ws_h, idx, ext, h);
     }
 }
 
@@ -950,39 +966,50 @@ state_update_kernel(const StepArgs a) {
     const bool ok = row < a.rows;
     const int N = a.dstate;
     float acc = 0.0f, xv = 0.0f, zv = 0.0f, dsk = 0.0f;
+    // extents for the index checks of debug builds
+    const long long nrow = a.rows, nbn = a.rows / a.dim * N, ndn = a.dim * N, nst = a.rows * N;
+    (void)nrow; (void)nbn; (void)ndn; (void)nst;
     if (ok) {
         const long long b = row / a.dim, d = row % a.dim;
-        xv = IO<T>::to_f(static_cast<const T*>(a.x)[row]);
-        const float s = IO<T>::to_f(static_cast<const T*>(a.delta)[row]) +
-                        (a.dt_bias ? a.dt_bias[d] : 0.0f);
+        const T* xp = static_cast<const T*>(a.x);
+        const T* dp = static_cast<const T*>(a.delta);
+        const T* zp = static_cast<const T*>(a.z);
+        const T* Bp = static_cast<const T*>(a.B);
+        const T* Cp = static_cast<const T*>(a.C);
+        xv = IO<T>::to_f(MAMBA_LD(xp, row, nrow));
+        const float s = IO<T>::to_f(MAMBA_LD(dp, row, nrow)) +
+                        (a.dt_bias ? MAMBA_LD(a.dt_bias, d, a.dim) : 0.0f);
         const float dt = SP ? softplus_f<ACC>(s) : s;
         const float du = dt * xv;
-        if (a.z) zv = IO<T>::to_f(static_cast<const T*>(a.z)[row]);
-        dsk = a.D_skip ? a.D_skip[d] : 0.0f;
-        const T* Bb = static_cast<const T*>(a.B) + b * N;
-        const T* Cb = static_cast<const T*>(a.C) + b * N;
-        const float* Ad = a.A + d * N;
-        float* h = a.state + row * N;
+        if (a.z) zv = IO<T>::to_f(MAMBA_LD(zp, row, nrow));
+        dsk = a.D_skip ? MAMBA_LD(a.D_skip, d, a.dim) : 0.0f;
         const int n0 = 4 * q;
         if (a.vec_state && n0 < N) {
-            float4 hv = *reinterpret_cast<const float4*>(h + n0);
+            float4 hv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            const long long hi = row * N + n0;
+            if (MAMBA_IN(hi, nst) && MAMBA_IN(hi + 3, nst))
+                hv = *reinterpret_cast<const float4*>(a.state + hi);
             float hs[4] = {hv.x, hv.y, hv.z, hv.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int n = n0 + j;
-                const float dA = ACC ? expf(dt * Ad[n]) : ex2_approx(dt * (Ad[n] * kLog2e));
-                const float bin = ZOH ? zoh_weight<ACC>(dA, dt, Ad[n]) * xv : du;
-                hs[j] = fmaf(dA, hs[j], bin * IO<T>::to_f(Bb[n]));
-                acc = fmaf(IO<T>::to_f(Cb[n]), hs[j], acc);
+                const float An = MAMBA_LD(a.A, d * N + n, ndn);
+                const float dA = ACC ? expf(dt * An) : ex2_approx(dt * (An * kLog2e));
+                const float bin = ZOH ? zoh_weight<ACC>(dA, dt, An) * xv : du;
+                hs[j] = fmaf(dA, hs[j], bin * IO<T>::to_f(MAMBA_LD(Bp, b * N + n, nbn)));
+                acc = fmaf(IO<T>::to_f(MAMBA_LD(Cp, b * N + n, nbn)), hs[j], acc);
             }
-            *reinterpret_cast<float4*>(h + n0) = make_float4(hs[0], hs[1], hs[2], hs[3]);
+            if (MAMBA_IN(hi, nst) && MAMBA_IN(hi + 3, nst))
+                *reinterpret_cast<float4*>(a.state + hi) = make_float4(hs[0], hs[1], hs[2], hs[3]);
         } else {
             for (int n = n0; n < n0 + 4 && n < N; ++n) {
-                const float dA = ACC ? expf(dt * Ad[n]) : ex2_approx(dt * (Ad[n] * kLog2e));
-                const float bin = ZOH ? zoh_weight<ACC>(dA, dt, Ad[n]) * xv : du;
-                const float hn = fmaf(dA, h[n], bin * IO<T>::to_f(Bb[n]));
-                h[n] = hn;
-                acc = fmaf(IO<T>::to_f(Cb[n]), hn, acc);
+                const float An = MAMBA_LD(a.A, d * N + n, ndn);
+                const float dA = ACC ? expf(dt * An) : ex2_approx(dt * (An * kLog2e));
+                const float bin = ZOH ? zoh_weight<ACC>(dA, dt, An) * xv : du;
+                const float hn = fmaf(dA, MAMBA_LD(a.state, row * N + n, nst),
+                                      bin * IO<T>::to_f(MAMBA_LD(Bp, b * N + n, nbn)));
+                MAMBA_ST(a.state, row * N + n, nst, hn);
+                acc = fmaf(IO<T>::to_f(MAMBA_LD(Cp, b * N + n, nbn)), hn, acc);
             }
         }
     }
@@ -991,7 +1018,7 @@ state_update_kernel(const StepArgs a) {
     if (ok && q == 0) {
         float o = acc + dsk * xv;
         if (a.z) o *= silu_f<ACC>(zv);
-        static_cast<T*>(a.y)[row] = IO<T>::from_f(o);
+        MAMBA_ST(static_cast<T*>(a.y), row, nrow, IO<T>::from_f(o));
     }
 }
 
@@ -1016,13 +1043,21 @@ state_update16_kernel(const StepArgs a) {
     const long long batch = a.rows / a.dim;
     const bool ok = d < a.dim && b < batch;
     float acc = 0.0f, xv = 0.0f, zv = 0.0f, dsk = 0.0f;
-    if (ok) {
+    // extents for the index checks of debug builds
+    const long long nrow = a.rows, nbn = batch * N, ndn = a.dim * N, nst = a.rows * N;
+    (void)nrow; (void)nbn; (void)ndn; (void)nst;
+    // the 8-entry vector accesses of this lane's half of the row
+    const bool vok = !ok || (MAMBA_IN(b * N + H * q, nbn) && MAMBA_IN(b * N + H * q + H - 1, nbn) &&
+                             MAMBA_IN(d * N + H * q, ndn) && MAMBA_IN(d * N + H * q + H - 1, ndn) &&
+                             MAMBA_IN((b * a.dim + d) * N + H * q, nst) &&
+                             MAMBA_IN((b * a.dim + d) * N + H * q + H - 1, nst));
+    if (ok && vok) {
         const long long row = b * a.dim + d;
-        xv = IO<T>::to_f(static_cast<const T*>(a.x)[row]);
-        const float dv = IO<T>::to_f(static_cast<const T*>(a.delta)[row]);
-        const float bias = a.dt_bias ? a.dt_bias[d] : 0.0f;
-        if (a.z) zv = IO<T>::to_f(static_cast<const T*>(a.z)[row]);
-        dsk = a.D_skip ? a.D_skip[d] : 0.0f;
+        xv = IO<T>::to_f(MAMBA_LD(static_cast<const T*>(a.x), row, nrow));
+        const float dv = IO<T>::to_f(MAMBA_LD(static_cast<const T*>(a.delta), row, nrow));
+        const float bias = a.dt_bias ? MAMBA_LD(a.dt_bias, d, a.dim) : 0.0f;
+        if (a.z) zv = IO<T>::to_f(MAMBA_LD(static_cast<const T*>(a.z), row, nrow));
+        dsk = a.D_skip ? MAMBA_LD(a.D_skip, d, a.dim) : 0.0f;
         // Delta (log2 units on the fast path), Delta (natural units), Delta*u
         float dt, dtn, du;
         if constexpr (ACC) {
@@ -1072,13 +1107,21 @@ state_update16_kernel(const StepArgs a) {
     if (ok && q == 0) {
         float o = acc + dsk * xv;
         if (a.z) o *= silu_f<ACC>(zv);
-        static_cast<T*>(a.y)[b * a.dim + d] = IO<T>::from_f(o);
+        MAMBA_ST(static_cast<T*>(a.y), b * a.dim + d, nrow, IO<T>::from_f(o));
     }
 }
 
 // Self-test of the bounded wait: one thread waits on an mbarrier that no
 // copy and no thread ever completes, with a short limit, then records the
 // timeout in the device error word exactly as the scan does, and returns.
+// Self-test of the index checks of debug builds: one thread checks an index
+// one past the end of an extent, the check records it in the debug word and
+// no memory is accessed at all.  In release builds the check is compiled
+// out and the kernel does nothing.
+__global__ void bounds_selftest_kernel(long long extent) {
+    if (threadIdx.x == 0) (void)MAMBA_IN(extent, extent);
+}
+
 __global__ void wait_timeout_selftest_kernel(unsigned long long limit_ns) {
     __shared__ __align__(8) uint64_t bar;
     if (threadIdx.x != 0) return;
@@ -1100,6 +1143,8 @@ struct Tuning {
 
 Tuning g_tuning;
 std::mutex g_mu;
+// source line of the last failed index check seen by mamba_device_status
+std::atomic<int> g_debug_last_line{0};
 
 Tuning get_tuning() {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -1502,6 +1547,8 @@ const char* mamba_status_string(int status) {
         case MAMBA_ERR_TOO_BIG:
             return "the call needs more scratch than the fixed MAMBA_NOALLOC_SCRATCH_BYTES";
         case MAMBA_ERR_FLAGS: return "a flags argument has an unknown bit";
+        case MAMBA_ERR_BOUNDS:
+            return "a debug build's index check failed (the access was skipped)";
         default: return "unknown status";
     }
 }
@@ -1514,9 +1561,29 @@ int mamba_device_status(cudaStream_t stream) {
         const int zero = 0;
         if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess)
             return MAMBA_ERR_CUDA;
-        return MAMBA_ERR_TIMEOUT;
     }
+    // the index checks of debug builds (always zero in release builds)
+    const int dbg_scan = take_debug_word(), dbg_conv = conv_take_debug_word();
+    if (dbg_scan < 0 || dbg_conv < 0) return MAMBA_ERR_CUDA;
+    const int dbg = dbg_scan ? dbg_scan : dbg_conv;
+    if (dbg) g_debug_last_line.store(dbg & ~kDebugBoundsFlag);
+    if (v) return MAMBA_ERR_TIMEOUT;
+    if (dbg) return MAMBA_ERR_BOUNDS;
     return MAMBA_OK;
+}
+
+int mamba_debug_build(int* last_failed_line) {
+    if (last_failed_line) *last_failed_line = g_debug_last_line.load();
+#ifdef MAMBA_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+int mamba_selftest_bounds(cudaStream_t stream) {
+    bounds_selftest_kernel<<<1, 32, 0, stream>>>(1000);
+    return cudaGetLastError() == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
 }
 
 int mamba_profile_begin(void) {

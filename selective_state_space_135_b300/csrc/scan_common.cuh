@@ -13,6 +13,7 @@
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
+#include <type_traits>
 
 namespace mamba {
 
@@ -108,10 +109,61 @@ __device__ __forceinline__ float silu_f(float z) {
 }
 
 // ---------------------------------------------------------------------------
+// debug builds: index checks on global accesses
+// ---------------------------------------------------------------------------
+//
+// Built with -DMAMBA_DEBUG, every global access of the scan, generation-step
+// and convolution kernels checks its element index against the extent of
+// its buffer.  A failed check records kDebugBoundsFlag | source line in the
+// translation unit's debug word (the first failure wins) and the access is
+// skipped: a load reads 0, a store writes nothing.  Nothing traps, so the
+// context stays usable; the host reads and clears the words through
+// mamba_device_status.  In release builds the checks compile to nothing.
+
+constexpr int kDebugBoundsFlag = 0x40000000;
+
+// One debug word per translation unit (file-scope static).
+static __device__ int g_debug_word;
+
+__device__ __forceinline__ bool debug_in_bounds(long long i, long long n, int line) {
+    if (i >= 0 && i < n) return true;
+    atomicCAS(&g_debug_word, 0, kDebugBoundsFlag | line);
+    return false;
+}
+
+// Reads and clears this translation unit's debug word (host side).
+static inline int take_debug_word() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_debug_word, sizeof(int)) != cudaSuccess) return -1;
+    if (v) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_debug_word, &zero, sizeof(int)) != cudaSuccess) return -1;
+    }
+    return v;
+}
+
+#ifdef MAMBA_DEBUG
+#define MAMBA_IN(i, n) ::mamba::debug_in_bounds((long long)(i), (long long)(n), __LINE__)
+#else
+#define MAMBA_IN(i, n) true
+#endif
+// element i of p (extent n), or a zero value when the check fails
+#define MAMBA_LD(p, i, n) \
+    (MAMBA_IN((i), (n)) ? (p)[(i)] : std::remove_cv_t<std::remove_reference_t<decltype((p)[0])>>{})
+// store v at element i of p (extent n) when the check passes
+#define MAMBA_ST(p, i, n, v)                  \
+    do {                                      \
+        if (MAMBA_IN((i), (n))) (p)[(i)] = (v); \
+    } while (0)
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
 inline int esize(int dt) { return dt == MAMBA_BF16 ? 2 : 4; }
+
+// The debug word of the convolution's translation unit (mamba_conv.cu).
+int conv_take_debug_word();
 
 inline bool aligned(const void* p, size_t a) {
     return (reinterpret_cast<uintptr_t>(p) % a) == 0;

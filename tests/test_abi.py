@@ -16,6 +16,7 @@ HEADER = os.path.join(ROOT, "include", "mamba_scan.h")
 OK, ENULL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EALLOC, EDTYPE, EALIAS = 0, -1, -2, -3, -4, -5, -6, -7, -8
 ETOOBIG = -9
 EFLAGS = -10
+EBOUNDS = -11
 SOFTPLUS, ZOH, NOALLOC = 1, 2, 4
 
 
@@ -42,9 +43,19 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_debug_library_exports_every_declared_symbol():
+    # the build with index checks (MAMBA_SCAN_LIBRARY=debug) has the same ABI
+    import ctypes
+    path = os.path.join(os.path.dirname(_lib.lib_path()), "libmamba_scan_debug.so")
+    assert os.path.exists(path), "build the library: python -m selective_state_space_135_b300.build"
+    dbg = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+
+
 def test_status_strings(lib):
     for code in (OK, ENULL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EALLOC, EDTYPE, EALIAS, ETOOBIG,
-                 EFLAGS):
+                 EFLAGS, EBOUNDS):
         s = mm.mamba_status_string(code)
         assert s and s != "unknown status"
     assert mm.mamba_status_string(12345) == "unknown status"
