@@ -272,6 +272,9 @@ struct ScanArgs {
     float* ws_h;  // chunk end states, then carried-in states (same layout)
     const float* h0;       // initial state (batch, dim, N), or null for zero
     const int* seqlens;    // per batch entry: steps in use, or null for all
+    float* ckpt;           // checkpoint mode: [row][ck_tiles][NP], the state before
+                           // every step that is a multiple of kBwdTile
+    int ck_tiles;
     long long dim;
     long long seqlen;
     long long chunk_len;  // multiple of the time tile
@@ -499,7 +502,9 @@ __device__ __forceinline__ void load_bc(float4 (&bc)[NT / 2], const float4* row)
 // per-entry lengths) or kModeExtZoh (the same with the zero-order-hold input
 // term).  The plain mode is compiled without the extensions: their per-tile
 // bookkeeping costs about 2% on B300.
-enum { kModePlain = 0, kModeExt = 1, kModeExtZoh = 2 };
+// kModeCkpt: the Euler scan from an initial state with no outputs, writing
+// state checkpoints for the backward pass.
+enum { kModePlain = 0, kModeExt = 1, kModeExtZoh = 2, kModeCkpt = 3 };
 template <typename T, int NT, int SPLIT, bool STATE_ONLY, bool SOFTPLUS, bool HAS_Z, int MODE>
 __global__ void __launch_bounds__(32 * kScanWarps, kScanMinBlocks)
 scan_kernel(const __grid_constant__ ScanArgs a) {
@@ -510,7 +515,10 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     constexpr int kNThr = 32 * kScanWarps;
     constexpr bool ACC = IO<T>::kAccurate;
     constexpr int kNPair = NT / 2;
-    constexpr bool has_z = !STATE_ONLY && HAS_Z;
+    constexpr bool CKPT = MODE == kModeCkpt;
+    constexpr bool OUT = !STATE_ONLY && !CKPT;   // y (and the partial sums it needs)
+    constexpr bool CKW = CKPT && !STATE_ONLY;    // writes checkpoints
+    constexpr bool has_z = OUT && HAS_Z;
     constexpr bool EXT = MODE != kModePlain;
     constexpr bool ZOH = MODE == kModeExtZoh;
     static_assert(NT % 2 == 0 && NP <= kMaxN, "bad state size");
@@ -644,7 +652,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
             prefetch_map(&a.m_dl);
             prefetch_map(&a.m_bc);
             if constexpr (has_z) prefetch_map(&a.m_z);
-            if (!STATE_ONLY) prefetch_map(&a.m_y);
+            if (OUT) prefetch_map(&a.m_y);
         }
         __syncthreads();
         if (tid == 0)
@@ -709,6 +717,25 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
         }
     };
 
+    // checkpoint mode: this warp's NT entries of the state before step `step`
+    // (a multiple of kBwdTile) into ckpt[(row * ck_tiles + step / kBwdTile) * NP + hh * NT]
+    auto write_ckpt = [&](long long step) {
+        if (!chan_ok || step >= L_) return;
+        const long long k = step / kBwdTile;
+        const long long base = (row * a.ck_tiles + k) * NP + hh * NT;
+        const long long ext = (long long)a.batch * dim * a.ck_tiles * NP;
+        (void)ext;
+        if (MAMBA_IN(base, ext) && MAMBA_IN(base + NT - 1, ext)) {
+            float2* p2 = reinterpret_cast<float2*>(a.ckpt + base);
+#pragma unroll
+            for (int i = 0; i < kNPair; ++i) p2[i] = h2[i];
+        }
+    };
+    (void)write_ckpt;
+    if constexpr (CKW) {
+        if (w.t0 == 0) write_ckpt(0);   // the initial state
+    }
+
     int stage = 0;          // stage of tile `it`
     uint32_t parity = 0;    // mbarrier phase parity of tile `it`
     if (ntiles > 0) {
@@ -719,6 +746,9 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
 
     for (int it = 0; it < ntiles && !aborted; ++it) {
         const long long tt0 = w.t0 + (long long)it * TT;
+        // the first t + 1 (1 .. kBwdTile) with tt0 + t + 1 a multiple of kBwdTile
+        const int ck0 = kBwdTile - (int)(tt0 % kBwdTile);
+        (void)ck0;
         const int nv = (int)min((long long)TT, w.t1 - tt0);   // steps of this unit in the tile
         // with per-entry lengths, the steps of the tile past them get y = 0
         // (without, steps past the sequence are not stored at all)
@@ -771,23 +801,28 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                 float pt;
                 if (t + 1 < TT) {
                     load_bc<NT>(bbuf[nxt], bct + (t + 1) * (NP / 2));
-                    pt = fused_step<NT, ACC, ZOH, STATE_ONLY>(h2, abuf[cur], abuf[nxt], a2, zk, dtn,
-                                                              dt, du, bbuf[cur]);
+                    pt = fused_step<NT, ACC, ZOH, !OUT>(h2, abuf[cur], abuf[nxt], a2, zk, dtn,
+                                                        dt, du, bbuf[cur]);
                 } else {
-                    pt = state_step<NT, ACC, ZOH, STATE_ONLY>(h2, abuf[cur], a2, zk, dt, du,
-                                                              bbuf[cur]);
+                    pt = state_step<NT, ACC, ZOH, !OUT>(h2, abuf[cur], a2, zk, dt, du, bbuf[cur]);
                 }
                 if constexpr (STATE_ONLY) {
                     dsum += dt;
-                } else {
+                } else if constexpr (OUT) {
                     if (mine[t / HT])
                         own[t % HT] = pt;
                     else
                         pseg[t / HT][t * CH] = pt;
                 }
+                if constexpr (CKW) {
+                    // after step t the state is the one before step tt0 + t + 1:
+                    // a checkpoint when that is a multiple of kBwdTile
+                    if (t + 1 == ck0 || t + 1 == ck0 + kBwdTile || t + 1 == ck0 + 2 * kBwdTile)
+                        write_ckpt(tt0 + t + 1);
+                }
             }
         }
-        if (!STATE_ONLY && tma && tid == 0) bulk_wait_read_0();   // y tile free again
+        if (OUT && tma && tid == 0) bulk_wait_read_0();   // y tile free again
         __syncthreads();   // partial sums complete; every read of du_s done
 
         // next tile's data, then (3) the outputs of this tile together with
@@ -801,7 +836,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
             const long long tn0 = tt0 + TT;
             phase1(smem + Lay::stage(next_stage), (int)max(-1LL, min((long long)TT, t_end - tn0)));
         }
-        if constexpr (!STATE_ONLY) {
+        if constexpr (OUT) {
             // the other slices' partials of this slice's steps t = hh*HT + i:
             // slice r = (hh + k) % SPLIT keeps them at row t (r > hh) or t - HT
             const float* pk[SPLIT > 1 ? SPLIT - 1 : 1];
@@ -842,7 +877,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
         // stage consumed, y tile complete, next tile's du_s ready
         aborted = __syncthreads_or(to);
 
-        if (!STATE_ONLY) {
+        if (OUT) {
             if (tma) {
                 if (tid == 0) {
                     tma_store_3d(&a.m_y, smem_u32(yt), (int)tt0, w.d0, w.b);
@@ -878,7 +913,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
             for (int it = max(0, issued - stages); it < issued; ++it)
                 (void)mbar_wait_bounded(smem_u32(&bars[it % stages]), (uint32_t)((it / stages) & 1));
         }
-        if (!STATE_ONLY && tid == 0) bulk_wait_all();
+        if (OUT && tid == 0) bulk_wait_all();
         __syncthreads();
         if (aborted) return;
     }
@@ -899,7 +934,7 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                 const float an = j ? a2[i].y : a2[i].x;
                 MAMBA_ST(a.ws_P, idx, ws_extent, ACC ? expf(an * dsum) : ex2_approx(an * dsum));
                 MAMBA_ST(a.ws_h, idx, ws_extent, hv);
-            } else if (a.final_state && w.t1 == L_) {
+            } else if (OUT && a.final_state && w.t1 == L_) {
                 MAMBA_ST(a.final_state, row * N + n, (long long)a.batch * dim * N, hv);
             }
         }
@@ -1276,7 +1311,10 @@ cudaError_t launch_scan(const ScanArgs& a, int grid, int smem, cudaStream_t st) 
 template <typename T, bool STATE_ONLY, int NT, int S, int MODE>
 cudaError_t dispatch_flags(bool sp, bool hz, const ScanArgs& a, int grid, int smem,
                            cudaStream_t st) {
-    if constexpr (STATE_ONLY) {
+    if constexpr (MODE == kModeCkpt && !STATE_ONLY) {   // no outputs: no gate
+        return sp ? launch_scan<T, NT, S, false, true, false, MODE>(a, grid, smem, st)
+                  : launch_scan<T, NT, S, false, false, false, MODE>(a, grid, smem, st);
+    } else if constexpr (STATE_ONLY) {
         return sp ? launch_scan<T, NT, S, true, true, false, MODE>(a, grid, smem, st)
                   : launch_scan<T, NT, S, true, false, false, MODE>(a, grid, smem, st);
     } else {
@@ -1293,6 +1331,12 @@ cudaError_t dispatch_mode(int mode, bool sp, bool hz, const ScanArgs& a, int gri
                           cudaStream_t st) {
     if (mode == kModeExtZoh)
         return dispatch_flags<T, STATE_ONLY, NT, S, kModeExtZoh>(sp, hz, a, grid, smem, st);
+    if (mode == kModeCkpt) {   // its summary pass is the extended mode's
+        if constexpr (STATE_ONLY)
+            return dispatch_flags<T, STATE_ONLY, NT, S, kModeExt>(sp, hz, a, grid, smem, st);
+        else
+            return dispatch_flags<T, STATE_ONLY, NT, S, kModeCkpt>(sp, hz, a, grid, smem, st);
+    }
     if (mode == kModeExt)
         return dispatch_flags<T, STATE_ONLY, NT, S, kModeExt>(sp, hz, a, grid, smem, st);
     return dispatch_flags<T, STATE_ONLY, NT, S, kModePlain>(sp, hz, a, grid, smem, st);
@@ -1647,13 +1691,14 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
                            const float* dt_bias, const float* A, const void* B, const void* C,
                            const float* D_skip, const void* z, int softplus, bool zoh,
                            const float* h0, const int32_t* seqlens, void* y,
-                           float* final_state, cudaStream_t stream, bool no_alloc) {
+                           float* final_state, cudaStream_t stream, bool no_alloc,
+                           float* ckpt = nullptr, int ck_tiles = 0) {
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
     if (batch < 1 || dim < 1 || dstate < 1 || dstate > kMaxN || seqlen < 0) return MAMBA_ERR_SHAPE;
     if (batch > INT32_MAX / 2 || dim > (1ll << 40) || seqlen > (1ll << 40) ||
         (double)batch * dim * (double)(seqlen > 0 ? seqlen : 1) > 4.0e18)
         return MAMBA_ERR_SHAPE;
-    if (!A || (seqlen > 0 && (!u || !delta || !B || !C || !y))) return MAMBA_ERR_NULL;
+    if (!A || (seqlen > 0 && (!u || !delta || !B || !C || (!y && !ckpt)))) return MAMBA_ERR_NULL;
     const int es = esize(io_dtype);
     const size_t big = (size_t)(batch * dim * seqlen) * es;
     const size_t bcb = (size_t)(batch * dstate * seqlen) * es;
@@ -1713,7 +1758,7 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
         tma = encode_map(&a.m_u, u, es, bf, seqlen, dim, batch, tt, pl.ch, sw) &&
               encode_map(&a.m_dl, delta, es, bf, seqlen, dim, batch, tt, pl.ch, sw) &&
               (!z || encode_map(&a.m_z, z, es, bf, seqlen, dim, batch, tt, pl.ch, sw)) &&
-              encode_map(&a.m_y, y, es, bf, seqlen, dim, batch, tt, pl.ch, sw);
+              (!y || encode_map(&a.m_y, y, es, bf, seqlen, dim, batch, tt, pl.ch, sw));
         if (!tma) pl = make_plan(dev, io_dtype, batch, dim, (int)dstate, seqlen, false, !no_alloc, tn);
     }
     const bool chunked = pl.n_full < pl.n_groups && pl.nchunks > 1;
@@ -1754,6 +1799,7 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     a.u = u; a.delta = delta; a.z = z;
     a.dt_bias = dt_bias; a.A = A; a.D_skip = D_skip; a.y = y; a.final_state = final_state;
     a.h0 = h0; a.seqlens = seqlens;
+    a.ckpt = ckpt; a.ck_tiles = ck_tiles;
     a.dim = dim; a.seqlen = seqlen; a.chunk_len = pl.chunk_len;
     a.batch = (int)batch; a.dstate = (int)dstate;
     a.use_tma = tma ? 1 : 0; a.stages = pl.stages;
@@ -1767,7 +1813,8 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
                        (int)dstate, pl.np, acc ? 1.0f : kLn2, stream);
     const bool bf = io_dtype == MAMBA_BF16;
     const bool hz = z != nullptr;
-    const int mode = zoh ? kModeExtZoh : ((h0 || seqlens) ? kModeExt : kModePlain);
+    const int mode = ckpt ? kModeCkpt
+                          : (zoh ? kModeExtZoh : ((h0 || seqlens) ? kModeExt : kModePlain));
     auto summary_and_carry = [&](cudaStream_t st) -> cudaError_t {
         const int grid1 = (pl.n_groups - pl.n_full) * (pl.nchunks - 1);
         cudaError_t r =
@@ -1930,3 +1977,15 @@ int mamba_state_update_ex(int64_t batch, int64_t dim, int64_t dstate, mamba_dtyp
 }
 
 }  // extern "C"
+
+namespace mamba {
+int scan_checkpoints(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io_dtype,
+                     const void* u, const void* delta, const float* dt_bias, const float* A,
+                     const void* B, const void* C, int softplus, const float* initial_state,
+                     float* ckpt, int ck_tiles, cudaStream_t stream) {
+    if (!ckpt || ck_tiles != (int)((seqlen + kBwdTile - 1) / kBwdTile)) return MAMBA_ERR_SHAPE;
+    return scan_fwd_common(batch, dim, dstate, seqlen, io_dtype, u, delta, dt_bias, A, B, C,
+                           nullptr, nullptr, softplus, false, initial_state, nullptr, nullptr,
+                           nullptr, stream, false, ckpt, ck_tiles);
+}
+}  // namespace mamba

@@ -4,10 +4,9 @@
 // recomputes it instead of reading it back (page "Mamba: linear-time
 // sequence modeling with selective state spaces", "What they did").  Here:
 //
-//   1. checkpoint pass: one lane per channel, the N state entries split over
-//      two warps (their recurrences are independent), runs the forward
-//      recurrence and stores the state before every tile of kBwdTile steps
-//      (B x D x ceil(L / kBwdTile) x N fp32);
+//   1. checkpoint pass: the forward scan kernel in its checkpoint mode (no
+//      outputs) runs the recurrence and stores the state before every tile
+//      of kBwdTile steps (B x D x ceil(L / kBwdTile) x N fp32);
 //   2. reverse pass: one two-warp CTA per 32 channels, each warp holding half
 //      of the entries.  Per tile, last to first, the tile's inputs are staged
 //      in shared memory, each warp recomputes its entries' states from the
@@ -34,9 +33,8 @@
 namespace mamba {
 namespace {
 
-constexpr int kBwdTile = 12;        // steps between checkpoints = reverse tile (42 KB of
-                                    // shared memory per two-warp CTA at dstate 16: five per SM)
-constexpr int kCkptThreads = 128;   // checkpoint pass: four independent warps per CTA
+// kBwdTile (scan_common.cuh, 12) steps between checkpoints = the reverse tile
+// (42 KB of shared memory per two-warp CTA at dstate 16: five per SM)
 constexpr int kReduceThreads = 256;
 
 struct BwdArgs {
@@ -131,12 +129,14 @@ __device__ __forceinline__ float sigmoid_f(float s) {
     if constexpr (ACC) return 1.0f / (1.0f + expf(-s));
     else return __fdividef(1.0f, 1.0f + ex2_approx(-s * kLog2e));
 }
-// Abar = exp(Delta * A).  dtl is Delta / ln 2, formed once per step, so the
-// fast path needs one multiply and one ex2 per state entry.
+// Abar = exp(Delta * A) of a pair of entries.  dtl2 holds Delta / ln 2 (as
+// Delta * log2(e)) in both halves, formed once per step, so the fast path
+// needs one packed multiply and two ex2 per pair.
 template <bool ACC>
-__device__ __forceinline__ float abar_of(float dt, float dtl, float a) {
-    if constexpr (ACC) return expf(dt * a);
-    else return ex2_approx(dtl * a);
+__device__ __forceinline__ float2 abar2_of(float dt, const float2& dtl2, const float2& a) {
+    if constexpr (ACC) return make_float2(expf(dt * a.x), expf(dt * a.y));
+    const float2 arg = __fmul2_rn(dtl2, a);
+    return make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
 }
 
 // Warp unit of both passes: 32 consecutive channels of one batch entry.
@@ -156,101 +156,10 @@ __device__ __forceinline__ WarpUnit warp_unit(const BwdArgs& a, long long w) {
     return u;
 }
 
-// State entries of a unit are split over kBwdSplit warps in the reverse pass
-// and ckpt_split<NP>() warps in the checkpoint pass (their recurrences are
-// independent); warp w of a unit holds entries [w * NPW, (w + 1) * NPW).
-// Measured on B300, four warps per unit make the checkpoint pass slower
-// (0.50 -> 0.58 ms on the Mamba-2.8B layer), so both use two.
+// The state entries of a unit are split over kBwdSplit warps in the reverse
+// pass (their recurrences are independent); warp w of a unit holds entries
+// [w * NPW, (w + 1) * NPW).
 constexpr int kBwdSplit = 2;
-template <int NP>
-__host__ __device__ constexpr int ckpt_split() {
-    return 2;
-}
-
-template <typename T, int NP, bool SP>
-__global__ void __launch_bounds__(kCkptThreads)
-bwd_checkpoint_kernel(const BwdArgs a) {
-    constexpr bool ACC = IO<T>::kAccurate;
-    constexpr int CS = ckpt_split<NP>();
-    constexpr int NPW = NP / CS;
-    // the tile's B/C rows of this warp's state entries, per warp of the CTA
-    __shared__ float4 ck_bc[kCkptThreads / 32][kBwdTile * (NPW / 2)];
-    const long long gw = ((long long)blockIdx.x * kCkptThreads + threadIdx.x) >> 5;
-    if (gw >= (long long)a.batch * a.groups * CS) return;   // whole warps leave together
-    const int half = (int)(gw % CS);
-    const WarpUnit q = warp_unit(a, gw / CS);
-    const int N = a.N, n0 = half * NPW;
-    const long long L = a.L;
-    float4* sb = ck_bc[threadIdx.x >> 5];
-    float h[NPW], Ar[NPW];
-#pragma unroll
-    for (int n = 0; n < NPW; ++n) {
-        const bool on = q.ok && n0 + n < N;
-        Ar[n] = on ? a.A[q.d * N + n0 + n] : 0.0f;
-        h[n] = (on && a.h0) ? a.h0[q.row * N + n0 + n] : 0.0f;
-    }
-    const float bias = (q.ok && a.dt_bias) ? a.dt_bias[q.d] : 0.0f;
-    const T* ur = static_cast<const T*>(a.u) + q.row * L;
-    const T* dl = static_cast<const T*>(a.delta) + q.row * L;
-    const float4* bcb = a.bc + (long long)q.b * L * (NP / 2) + n0 / 2;
-    float2* ck = reinterpret_cast<float2*>(a.ckpt + q.row * a.ntiles * NP + n0);
-    // tile k + 1's loads are issued before tile k's recurrence (registers:
-    // u, delta and this lane's share of the B/C rows)
-    constexpr int kRowsPerLane = (kBwdTile * (NPW / 2) + 31) / 32;
-    float uvs[kBwdTile], dvs[kBwdTile];
-    float4 bcr[kRowsPerLane];
-    auto fetch = [&](int kk) {
-        const long long t0 = (long long)kk * kBwdTile;
-        const int nv = (int)min((long long)kBwdTile, L - t0);
-        load_tile_row<T>(ur, t0, nv, a.vec8 != 0, q.ok, uvs);
-        load_tile_row<T>(dl, t0, nv, a.vec8 != 0, q.ok, dvs);
-#pragma unroll
-        for (int r = 0; r < kRowsPerLane; ++r) {
-            const int e = r * 32 + q.lane;
-            const int i = e / (NPW / 2);
-            bcr[r] = (e < kBwdTile * (NPW / 2) && i < nv)
-                         ? bcb[(t0 + i) * (NP / 2) + (e % (NPW / 2))]
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    };
-    if (a.ntiles > 0) fetch(0);
-    for (int k = 0; k < a.ntiles; ++k) {
-        if (q.ok) {
-#pragma unroll
-            for (int j = 0; j < NPW / 2; ++j) ck[k * (NP / 2) + j] = make_float2(h[2 * j], h[2 * j + 1]);
-        }
-        const long long t0 = (long long)k * kBwdTile;
-        const int nv = (int)min((long long)kBwdTile, L - t0);
-        float uc[kBwdTile], dc[kBwdTile];
-#pragma unroll
-        for (int i = 0; i < kBwdTile; ++i) {
-            uc[i] = uvs[i];
-            dc[i] = dvs[i];
-        }
-#pragma unroll
-        for (int r = 0; r < kRowsPerLane; ++r) {
-            const int e = r * 32 + q.lane;
-            if (e < kBwdTile * (NPW / 2)) sb[e] = bcr[r];
-        }
-        if (k + 1 < a.ntiles) fetch(k + 1);
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < kBwdTile; ++i) {
-            if (i < nv) {
-                const float dt = delta_nat<ACC, SP>(dc[i] + bias);
-                const float dtl = dt * kLog2e;
-                const float du = dt * uc[i];
-#pragma unroll
-                for (int j = 0; j < NPW / 2; ++j) {
-                    const float4 p = sb[i * (NPW / 2) + j];
-                    h[2 * j] = fmaf(abar_of<ACC>(dt, dtl, Ar[2 * j]), h[2 * j], du * p.x);
-                    h[2 * j + 1] = fmaf(abar_of<ACC>(dt, dtl, Ar[2 * j + 1]), h[2 * j + 1], du * p.y);
-                }
-            }
-        }
-        __syncwarp();   // the rows are rewritten for the next tile
-    }
-}
 
 // Sum v over the 32 lanes of the warp, NV values at once: at each of the
 // first log2(NV) levels a lane keeps half of its values and sends the other
@@ -313,7 +222,9 @@ bwd_kernel(const BwdArgs a) {
     constexpr int NPW = NP / kBwdSplit;
     extern __shared__ __align__(16) float bwd_smem[];
     const int warp = threadIdx.x >> 5;
-    float* hist = bwd_smem + warp * (kBwdTile * NPW * 32);
+    // the warp's recomputed states, as float2 pairs of entries: pair j of
+    // step i at hist2[(i * NPW / 2 + j) * 32 + lane]
+    float2* hist2 = reinterpret_cast<float2*>(bwd_smem + warp * (kBwdTile * NPW * 32));
     float* rows = bwd_smem + kBwdTile * NP * 32;
     float* parts = rows + kSRows * kBwdTile * 32;
     float4* sbc = reinterpret_cast<float4*>(parts + kBwdSplit * kPRows * kBwdTile * 32);
@@ -325,13 +236,23 @@ bwd_kernel(const BwdArgs a) {
         return parts[((w * kPRows + r) * kBwdTile + i) * 32 + lane];
     };
 
-    float Ar[NPW], dh[NPW], dA[NPW], hs[NPW];
+    // this warp's entries in pairs: A, dJ/dh, the dA partial sums, and the
+    // state at the start of the current tile (from its checkpoint)
+    constexpr int NPP = NPW / 2;
+    float2 A2[NPP], dh2[NPP], dA2[NPP], hs2[NPP];
 #pragma unroll
-    for (int n = 0; n < NPW; ++n) {
-        const bool on = q.ok && n0 + n < N;
-        Ar[n] = on ? a.A[q.d * N + n0 + n] : 0.0f;
-        dh[n] = (on && a.dfinal) ? a.dfinal[q.row * N + n0 + n] : 0.0f;
-        dA[n] = 0.0f;
+    for (int j = 0; j < NPP; ++j) {
+        float av[2], dv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int n = n0 + 2 * j + e;
+            const bool on = q.ok && n < N;
+            av[e] = on ? a.A[q.d * N + n] : 0.0f;
+            dv[e] = (on && a.dfinal) ? a.dfinal[q.row * N + n] : 0.0f;
+        }
+        A2[j] = make_float2(av[0], av[1]);
+        dh2[j] = make_float2(dv[0], dv[1]);
+        dA2[j] = make_float2(0.0f, 0.0f);
     }
     const float bias = (q.ok && a.dt_bias) ? a.dt_bias[q.d] : 0.0f;
     const float dsk = (q.ok && a.D_skip) ? a.D_skip[q.d] : 0.0f;
@@ -413,43 +334,41 @@ bwd_kernel(const BwdArgs a) {
             if (e < kBwdTile * (NP / 2)) sbc[e] = bcr[r];
         }
 #pragma unroll
-        for (int j = 0; j < NPW / 2; ++j) {
-            hs[2 * j] = ckr[j].x;
-            hs[2 * j + 1] = ckr[j].y;
-        }
+        for (int j = 0; j < NPP; ++j) hs2[j] = ckr[j];
         if (k > 0) fetch(k - 1);
         __syncthreads();
-        // (b) recompute this warp's states and its part of C.h (+ D u)
+        // (b) recompute this warp's states and its part of C.h (+ D u), two
+        //     entries at a time with packed arithmetic
         {
-            float h[NPW];
+            float2 h2[NPP];
 #pragma unroll
-            for (int n = 0; n < NPW; ++n) h[n] = hs[n];
+            for (int j = 0; j < NPP; ++j) h2[j] = hs2[j];
 #pragma unroll
             for (int i = 0; i < kBwdTile; ++i) {
                 if (i >= nv) continue;
                 const float uv = S(kSU, i), dt = S(kSDT, i);
-                const float dtl = dt * kLog2e;
-                const float du = dt * uv;
-                float acc = warp == 0 ? dsk * uv : 0.0f;
+                const float2 dtl2 = make_float2(dt * kLog2e, dt * kLog2e);
+                const float2 du2 = make_float2(dt * uv, dt * uv);
+                float2 acc2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-                for (int j = 0; j < NPW / 2; ++j) {
+                for (int j = 0; j < NPP; ++j) {
                     const float4 p = sbc[i * (NP / 2) + n0 / 2 + j];
-                    h[2 * j] = fmaf(abar_of<ACC>(dt, dtl, Ar[2 * j]), h[2 * j], du * p.x);
-                    h[2 * j + 1] = fmaf(abar_of<ACC>(dt, dtl, Ar[2 * j + 1]), h[2 * j + 1], du * p.y);
-                    acc = fmaf(p.z, h[2 * j], acc);
-                    acc = fmaf(p.w, h[2 * j + 1], acc);
-                    hist[(i * NPW + 2 * j) * 32 + lane] = h[2 * j];
-                    hist[(i * NPW + 2 * j + 1) * 32 + lane] = h[2 * j + 1];
+                    const float2 ab = abar2_of<ACC>(dt, dtl2, A2[j]);
+                    h2[j] = __ffma2_rn(ab, h2[j], __fmul2_rn(du2, make_float2(p.x, p.y)));
+                    acc2 = __ffma2_rn(make_float2(p.z, p.w), h2[j], acc2);
+                    hist2[(i * NPP + j) * 32 + lane] = h2[j];
                 }
-                P(warp, kPY, i) = acc;
+                P(warp, kPY, i) = (warp == 0 ? dsk * uv : 0.0f) + (acc2.x + acc2.y);
             }
         }
         __syncwarp();
-        // (c) backwards through the tile for this warp's entries; h_t of
-        //     step i is h_{t-1} of step i + 1, so each state is read once
-        float hn[NPW];
+        // (c) backwards through the tile for this warp's entries, two entries
+        //     at a time; h_t of step i is h_{t-1} of step i + 1, so each state
+        //     is read once
+        float2 hn2[NPP];
 #pragma unroll
-        for (int n = 0; n < NPW; ++n) hn[n] = nv > 0 ? hist[((nv - 1) * NPW + n) * 32 + lane] : 0.0f;
+        for (int j = 0; j < NPP; ++j)
+            hn2[j] = nv > 0 ? hist2[((nv - 1) * NPP + j) * 32 + lane] : make_float2(0.0f, 0.0f);
         // (kept rolled: the unrolled tile's code overflows the instruction
         // cache; measured on B300 6% slower)
 #pragma unroll 1
@@ -457,32 +376,35 @@ bwd_kernel(const BwdArgs a) {
             if (i >= nv) continue;
             const long long t = t0 + i;
             const float uv = S(kSU, i), dt = S(kSDT, i), g = S(kSG, i);
-            const float dtl = dt * kLog2e;
-            float dus[2] = {warp == 0 ? g * dsk : 0.0f, 0.0f}, dds[2] = {0.0f, 0.0f};
+            const float2 g2 = make_float2(g, g), dt2 = make_float2(dt, dt), uv2 = make_float2(uv, uv);
+            const float2 dtl2 = make_float2(dt * kLog2e, dt * kLog2e);
+            float2 dus2 = make_float2(0.0f, 0.0f), dds2 = make_float2(0.0f, 0.0f);
             float pb[NPW], pc[NPW];
+            // the states after step i - 1 (at i = 0 the checkpoint, hs2; the
+            // row read is clamped so that every load stays in the history)
+            const float2* hprev = hist2 + ((i > 0 ? i - 1 : 0) * NPP) * 32 + lane;
 #pragma unroll
-            for (int j = 0; j < NPW / 2; ++j) {
+            for (int j = 0; j < NPP; ++j) {
                 const float4 p = sbc[i * (NP / 2) + n0 / 2 + j];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int n = 2 * j + e;
-                    const float Bn = e ? p.y : p.x, Cn = e ? p.w : p.z;
-                    const float ht = hn[n];
-                    const float hp = i > 0 ? hist[((i - 1) * NPW + n) * 32 + lane] : hs[n];
-                    hn[n] = hp;
-                    const float abar = abar_of<ACC>(dt, dtl, Ar[n]);
-                    dh[n] = fmaf(g, Cn, dh[n]);
-                    pc[n] = g * ht;
-                    const float dhd = dh[n] * dt;
-                    pb[n] = dhd * uv;
-                    dus[e] = fmaf(dhd, Bn, dus[e]);
-                    dds[e] = fmaf(dh[n], fmaf(Ar[n] * abar, hp, Bn * uv), dds[e]);
-                    dA[n] = fmaf(dhd * abar, hp, dA[n]);
-                    dh[n] *= abar;
-                }
+                const float2 B2 = make_float2(p.x, p.y), C2 = make_float2(p.z, p.w);
+                const float2 ht = hn2[j];
+                const float2 hp = i > 0 ? hprev[j * 32] : hs2[j];
+                hn2[j] = hp;
+                const float2 ab = abar2_of<ACC>(dt, dtl2, A2[j]);
+                dh2[j] = __ffma2_rn(g2, C2, dh2[j]);
+                const float2 pcv = __fmul2_rn(g2, ht);
+                const float2 dhd = __fmul2_rn(dh2[j], dt2);
+                const float2 pbv = __fmul2_rn(dhd, uv2);
+                pc[2 * j] = pcv.x; pc[2 * j + 1] = pcv.y;
+                pb[2 * j] = pbv.x; pb[2 * j + 1] = pbv.y;
+                dus2 = __ffma2_rn(dhd, B2, dus2);
+                const float2 tin = __ffma2_rn(__fmul2_rn(A2[j], ab), hp, __fmul2_rn(B2, uv2));
+                dds2 = __ffma2_rn(dh2[j], tin, dds2);
+                dA2[j] = __ffma2_rn(__fmul2_rn(dhd, ab), hp, dA2[j]);
+                dh2[j] = __fmul2_rn(dh2[j], ab);
             }
-            P(warp, kPDU, i) = dus[0] + dus[1];
-            P(warp, kPDD, i) = dds[0] + dds[1];
+            P(warp, kPDU, i) = (warp == 0 ? g * dsk : 0.0f) + (dus2.x + dus2.y);
+            P(warp, kPDD, i) = dds2.x + dds2.y;
             const float sb = warp_sum_transpose<NPW>(pb, lane);
             const float sc = warp_sum_transpose<NPW>(pc, lane);
             if (writer) {
@@ -530,9 +452,13 @@ bwd_kernel(const BwdArgs a) {
     }
     if (q.ok) {
 #pragma unroll
-        for (int n = 0; n < NPW; ++n) {
-            a.pA[q.row * NP + n0 + n] = dA[n];
-            if (a.dh0 && n0 + n < N) a.dh0[q.row * N + n0 + n] = dh[n];
+        for (int j = 0; j < NPP; ++j) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int n = n0 + 2 * j + e;
+                a.pA[q.row * NP + n] = e ? dA2[j].y : dA2[j].x;
+                if (a.dh0 && n < N) a.dh0[q.row * N + n] = e ? dh2[j].y : dh2[j].x;
+            }
         }
         if (warp == 0) {
             a.pD[q.row] = dD;
@@ -590,14 +516,7 @@ bwd_reduce_params_kernel(const float* __restrict__ pA, const float* __restrict__
 template <typename T, int NP, bool SP>
 cudaError_t launch_bwd(const BwdArgs& a, bool hz, cudaStream_t st) {
     const long long units = (long long)a.batch * a.groups;
-    {
-        ProfScope prof(kKindBwdCheckpoint, st);
-        const long long threads = units * ckpt_split<NP>() * 32;
-        const unsigned grid = (unsigned)((threads + kCkptThreads - 1) / kCkptThreads);
-        bwd_checkpoint_kernel<T, NP, SP><<<grid, kCkptThreads, 0, st>>>(a);
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
     const int smem = bwd_smem_floats<NP>() * (int)sizeof(float);
     auto k = hz ? bwd_kernel<T, NP, SP, true> : bwd_kernel<T, NP, SP, false>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -722,6 +641,17 @@ int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, m
     for (const void* q : {u, delta, z, dy, (const void*)du, (const void*)ddelta, (const void*)dz})
         if (q && !aligned(q, 8)) a.vec8 = 0;
 
+    // checkpoints: the forward kernel's checkpoint mode (its own B/C table and
+    // plan, from the same pool on the same stream)
+    {
+        ProfScope prof(kKindBwdCheckpoint, stream);
+        rc = scan_checkpoints(batch, dim, dstate, seqlen, io_dtype, u, delta, dt_bias, A, B, C,
+                              sp ? 1 : 0, initial_state, a.ckpt, ntiles, stream);
+    }
+    if (rc != MAMBA_OK) {
+        cudaFreeAsync(scratch, stream);
+        return rc;
+    }
     cudaError_t e = launch_pack_bc(io_dtype, B, C, const_cast<float4*>(a.bc), batch, seqlen,
                                    (int)dstate, np, 1.0f, stream);
     if (e == cudaSuccess)

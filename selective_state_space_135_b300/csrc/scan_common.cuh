@@ -18,6 +18,9 @@
 namespace mamba {
 
 constexpr int kMaxN = 16;   // largest dstate
+// Steps between the state checkpoints the backward pass recomputes from
+// (its reverse tile); the forward kernel's checkpoint mode writes them.
+constexpr int kBwdTile = 12;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
@@ -193,6 +196,15 @@ struct ProfScope {
 int sm_count(int dev);
 // The library's stream-ordered pool of the device (MAMBA_OK or an error).
 int get_pool(int dev, cudaMemPool_t* out);
+// The forward scan in its checkpoint mode (mamba_scan.cu): the Euler scan
+// from initial_state (or zero) with no outputs, writing the state before
+// every step that is a multiple of kBwdTile into ckpt[(row * ck_tiles + k) *
+// np + n] (np = dstate padded to 4, 8 or 16; ck_tiles = ceil(seqlen /
+// kBwdTile)).  Scratch from the stream-ordered pool.  Returns a status.
+int scan_checkpoints(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io_dtype,
+                     const void* u, const void* delta, const float* dt_bias, const float* A,
+                     const void* B, const void* C, int softplus, const float* initial_state,
+                     float* ckpt, int ck_tiles, cudaStream_t stream);
 // B and C (batch, N, L) in io_dtype -> fp32 rows of NP/2 float4 (s*B pair,
 // C pair) per (batch, step), entries n >= N zero.
 cudaError_t launch_pack_bc(int io_dtype, const void* B, const void* C, float4* out,
