@@ -20,7 +20,9 @@
 //      with ddelta = dDelta * sigmoid(s) under softplus.  B and C are shared
 //      by all channels of a batch entry, so dB and dC are sums over d: the
 //      warp sums its 32 channels with a transposing butterfly of shuffles
-//      (one shuffle per value) and writes one partial per 32 channels;
+//      (one shuffle per value), parks the sums of step t in its own pairs of
+//      the tile's B/C row t once read, and the CTA writes the tile's rows of
+//      partials (one per 32 channels) as whole 16-byte stores;
 //   3. reduction passes add the partials in a fixed order (deterministic
 //      results, no atomics): dB, dC over channel groups, dA, D_skip and
 //      dt_bias gradients over the batch.
@@ -156,15 +158,28 @@ __device__ __forceinline__ WarpUnit warp_unit(const BwdArgs& a, long long w) {
     return u;
 }
 
-// The state entries of a unit are split over kBwdSplit warps in the reverse
-// pass (their recurrences are independent); warp w of a unit holds entries
-// [w * NPW, (w + 1) * NPW).
-constexpr int kBwdSplit = 2;
+// The state entries of a unit are split over bwd_split<NP>() warps in the
+// reverse pass (their recurrences are independent); warp w of a unit holds
+// entries [w * NPW, (w + 1) * NPW).  (Four warps of four entries at dstate
+// 16 measured slower on B300: the per-step work outside the entries' own
+// arithmetic is paid per warp, and the larger CTAs fit fewer to an SM.)
+template <int NP>
+__host__ __device__ constexpr int bwd_split() {
+    return 2;
+}
 
-// Sum v over the 32 lanes of the warp, NV values at once: at each of the
+// Sum v over the 32 lanes of the warp, NV values at once.  At each of the
 // first log2(NV) levels a lane keeps half of its values and sends the other
-// half to its partner, so every value costs one shuffle in all.  On return
-// every lane holds the full sum of v[n] for n = bwd_lane_entry<NV>(lane).
+// half to its partner (lane ^ m), so every value costs one shuffle in all;
+// then the last partial sums are added over the remaining lanes.  On return
+// every lane holds the full sum of the entry bwd_lane_entry<NV>(lane).
+//
+// So that a lane need not choose, level by level, which half it keeps, its
+// entries sit in its registers in a lane-dependent order: slot s of lane l
+// holds entry s ^ bwd_slot_xor<NV>(l), the entry bits of every level but the
+// last.  At each of those levels the kept half is then slots [0, half) on
+// every lane; only the last level (entries 2k and 2k + 1, which stay
+// together as a packed pair) selects.
 template <int NV>
 __host__ __device__ constexpr int bwd_levels() {
     return NV == 16 ? 4 : (NV == 8 ? 3 : (NV == 4 ? 2 : 1));
@@ -178,74 +193,83 @@ __device__ __forceinline__ int bwd_lane_entry(int lane) {
     return n;
 }
 template <int NV>
-__device__ __forceinline__ float warp_sum_transpose(float (&v)[NV], int lane) {
+__device__ __forceinline__ int bwd_slot_xor(int lane) {
+    return bwd_lane_entry<NV>(lane) & ~1;
+}
+template <int NV>
+__device__ __forceinline__ float warp_sum_lanes(float (&v)[NV]) {
     constexpr int LV = bwd_levels<NV>();
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int lev = 0; lev < LV; ++lev) {
+    for (int lev = 0; lev < LV - 1; ++lev) {
         const int m = 16 >> lev;
-        const bool upper = (lane & m) != 0;
+        const int half = NV >> (lev + 1);
 #pragma unroll
-        for (int i = 0; i < NV / 2; ++i) {
-            const int half = NV >> (lev + 1);
-            if (i < half) {
-                const float send = upper ? v[i] : v[i + half];
-                const float keep = upper ? v[i + half] : v[i];
-                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-            }
-        }
+        for (int i = 0; i < NV / 2; ++i)
+            if (i < half) v[i] += __shfl_xor_sync(0xffffffffu, v[i + half], m);
     }
-    float s = v[0];
+    // last level: slots 0 and 1 hold entries e and e + 1 (e even)
+    const int m = 16 >> (LV - 1);
+    const bool upper = (lane & m) != 0;
+    float s = (upper ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, upper ? v[0] : v[1], m);
 #pragma unroll
-    for (int m = 16 >> LV; m >= 1; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+    for (int mm = m >> 1; mm >= 1; mm >>= 1) s += __shfl_xor_sync(0xffffffffu, s, mm);
     return s;
 }
 
-// Shared memory of one CTA (kBwdSplit warps, one unit), per tile:
-//   hist  [warp][kBwdTile][NPW][32]   the warp's states h_t (after step t)
-//   rows  [kSRows][kBwdTile][32]      per step and lane: g = dy silu(z), u,
-//                                     Delta, sigmoid(s), dy silu'(z)
-//   parts [warp][3][kBwdTile][32]     the warp's partial sums over its
-//                                     entries: C.h, du, dDelta
-//   bc    [kBwdTile][NP / 2] float4   the tile's packed B/C rows
-enum { kSG = 0, kSU = 1, kSDT = 2, kSSIG = 3, kSZF = 4, kSRows = 5 };
-enum { kPY = 0, kPDU = 1, kPDD = 2, kPRows = 3 };
+// Shared memory of one CTA (bwd_split<NP>() warps, one unit), per tile:
+//   hist  [warp][kBwdTile][NPW / 2][32] float2  the warp's states h_t (after
+//                                     step t), in the lane's register order
+//   srow  [kBwdTile][2][32] float2    per step and lane: (u, Delta) and
+//                                     (g = dy silu(z), sigmoid(s))
+//   szf   [kBwdTile][32]              per step and lane: dy silu'(z)
+//   party [warp][kBwdTile][32]        the warp's partial sum of C.h
+//   partd [warp][kBwdTile][32] float2 the warp's partial sums of du, dDelta
+//   sbc   [kBwdTile][NP / 2] float4   the tile's packed B/C rows; in the
+//                                     reverse walk each warp overwrites its
+//                                     own pairs of row t, once read, with
+//                                     the step's dB and dC sums (same layout)
 template <int NP>
 __host__ __device__ constexpr int bwd_smem_floats() {
-    return kBwdTile * NP * 32 + kSRows * kBwdTile * 32 + kBwdSplit * kPRows * kBwdTile * 32 +
+    return kBwdTile * NP * 32 + 5 * kBwdTile * 32 + bwd_split<NP>() * 3 * kBwdTile * 32 +
            kBwdTile * (NP / 2) * 4;
 }
 
+// Registers are allocated per warp on one SM sub-partition (16384 each):
+// at most 168 per thread leave room for three warps per sub-partition, so
+// five of these two-warp CTAs (the shared-memory limit) fit on an SM; at 190
+// only four did, and 640 CTAs took two waves on 148 SMs.  Asking for six
+// CTAs per SM caps ptxas at 168.
 template <typename T, int NP, bool SP, bool HZ>
-__global__ void __launch_bounds__(32 * kBwdSplit)
+__global__ void __launch_bounds__(32 * bwd_split<NP>(), 6)
 bwd_kernel(const BwdArgs a) {
     constexpr bool ACC = IO<T>::kAccurate;
-    constexpr int NPW = NP / kBwdSplit;
+    constexpr int SPL = bwd_split<NP>();
+    constexpr int NPW = NP / SPL;
+    constexpr int NPP = NPW / 2;
     extern __shared__ __align__(16) float bwd_smem[];
     const int warp = threadIdx.x >> 5;
-    // the warp's recomputed states, as float2 pairs of entries: pair j of
-    // step i at hist2[(i * NPW / 2 + j) * 32 + lane]
     float2* hist2 = reinterpret_cast<float2*>(bwd_smem + warp * (kBwdTile * NPW * 32));
-    float* rows = bwd_smem + kBwdTile * NP * 32;
-    float* parts = rows + kSRows * kBwdTile * 32;
-    float4* sbc = reinterpret_cast<float4*>(parts + kBwdSplit * kPRows * kBwdTile * 32);
+    float2* srow = reinterpret_cast<float2*>(bwd_smem + kBwdTile * NP * 32);
+    float* szf = reinterpret_cast<float*>(srow + kBwdTile * 2 * 32);
+    float* party = szf + kBwdTile * 32;
+    float2* partd = reinterpret_cast<float2*>(party + SPL * kBwdTile * 32);
+    float4* sbc = reinterpret_cast<float4*>(partd + SPL * kBwdTile * 32);
     const WarpUnit q = warp_unit(a, blockIdx.x);
     const int lane = q.lane, N = a.N, n0 = warp * NPW;
     const long long L = a.L;
-    auto S = [&](int r, int i) -> float& { return rows[(r * kBwdTile + i) * 32 + lane]; };
-    auto P = [&](int w, int r, int i) -> float& {
-        return parts[((w * kPRows + r) * kBwdTile + i) * 32 + lane];
-    };
 
     // this warp's entries in pairs: A, dJ/dh, the dA partial sums, and the
-    // state at the start of the current tile (from its checkpoint)
-    constexpr int NPP = NPW / 2;
+    // state at the start of the current tile (from its checkpoint).  Register
+    // pair j of this lane holds the entry pair j ^ pj (see warp_sum_lanes).
+    const int pj = bwd_slot_xor<NPW>(lane) >> 1;
     float2 A2[NPP], dh2[NPP], dA2[NPP], hs2[NPP];
 #pragma unroll
     for (int j = 0; j < NPP; ++j) {
         float av[2], dv[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int n = n0 + 2 * j + e;
+            const int n = n0 + 2 * (j ^ pj) + e;
             const bool on = q.ok && n < N;
             av[e] = on ? a.A[q.d * N + n] : 0.0f;
             dv[e] = (on && a.dfinal) ? a.dfinal[q.row * N + n] : 0.0f;
@@ -266,8 +290,11 @@ bwd_kernel(const BwdArgs a) {
     T* dzr = HZ ? static_cast<T*>(a.dz) + q.row * L : nullptr;
     const float4* bcb = a.bc + (long long)q.b * L * (NP / 2);
     const float2* ck = reinterpret_cast<const float2*>(a.ckpt + q.row * a.ntiles * NP + n0);
-    const int my_n = n0 + bwd_lane_entry<NPW>(lane);
+    // after the butterfly this lane holds the sums of entry n0 + le; the first
+    // lane of each group that shares an entry stores them into the B/C row
+    const int le = bwd_lane_entry<NPW>(lane);
     const bool writer = (lane & ((16 >> bwd_levels<NPW>()) * 2 - 1)) == 0;
+    float* sum_at = reinterpret_cast<float*>(sbc + n0 / 2 + (le >> 1)) + (le & 1);
     float* pBg = a.pB + ((long long)q.grp * a.batch + q.b) * L * NP;
     float* pCg = a.pC + ((long long)q.grp * a.batch + q.b) * L * NP;
     const bool vec = a.vec8 != 0;
@@ -275,31 +302,31 @@ bwd_kernel(const BwdArgs a) {
     // Tile k - 1's global loads are issued before tile k's work: per warp two
     // input rows (warp 0: u, delta; warp 1: dy, z), each thread's share of
     // the B/C rows, and the warp's checkpoint, held in registers.
-    constexpr int kRowsPerThread = (kBwdTile * (NP / 2) + 32 * kBwdSplit - 1) / (32 * kBwdSplit);
+    constexpr int kRowsPerThread = (kBwdTile * (NP / 2) + 32 * SPL - 1) / (32 * SPL);
     float r1[kBwdTile], r2[kBwdTile];
     float4 bcr[kRowsPerThread];
-    float2 ckr[NPW / 2];
+    float2 ckr[NPP];
     auto fetch = [&](int kk) {
         const long long t0 = (long long)kk * kBwdTile;
         const int nv = (int)min((long long)kBwdTile, L - t0);
         if (warp == 0) {
             load_tile_row<T>(ur, t0, nv, vec, q.ok, r1);
             load_tile_row<T>(dl, t0, nv, vec, q.ok, r2);
-        } else {
+        } else if (warp == 1) {
             load_tile_row<T>(dyr, t0, nv, vec, q.ok, r1);
             if constexpr (HZ) load_tile_row<T>(zr, t0, nv, vec, q.ok, r2);
         }
 #pragma unroll
         for (int r = 0; r < kRowsPerThread; ++r) {
-            const int e = r * 32 * kBwdSplit + threadIdx.x;
+            const int e = r * 32 * SPL + threadIdx.x;
             const int i = e / (NP / 2);
             bcr[r] = (e < kBwdTile * (NP / 2) && i < nv)
                          ? bcb[(t0 + i) * (NP / 2) + (e % (NP / 2))]
                          : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int j = 0; j < NPW / 2; ++j)
-            ckr[j] = q.ok ? ck[kk * (NP / 2) + j] : make_float2(0.f, 0.f);
+        for (int j = 0; j < NPP; ++j)
+            ckr[j] = q.ok ? ck[kk * (NP / 2) + (j ^ pj)] : make_float2(0.f, 0.f);
     };
     if (a.ntiles > 0) fetch(a.ntiles - 1);
 
@@ -307,30 +334,34 @@ bwd_kernel(const BwdArgs a) {
         const long long t0 = (long long)k * kBwdTile;
         const int nv = (int)min((long long)kBwdTile, L - t0);
         // (a) the tile's per-step inputs, B/C rows and checkpoint from the
-        //     registers into shared memory, then the next loads
+        //     registers into shared memory, then the next loads.  Steps
+        //     i >= nv of a last, short tile get u = 0, Delta = 0 and zero
+        //     B/C rows: they leave the state as it is.
         if (warp == 0) {
 #pragma unroll
             for (int i = 0; i < kBwdTile; ++i) {
                 const float sarg = r2[i] + bias;
-                S(kSU, i) = r1[i];
-                S(kSDT, i) = (q.ok && i < nv) ? delta_nat<ACC, SP>(sarg) : 0.0f;
-                S(kSSIG, i) = SP ? sigmoid_f<ACC>(sarg) : 1.0f;
+                srow[(2 * i) * 32 + lane] =
+                    make_float2(r1[i], (q.ok && i < nv) ? delta_nat<ACC, SP>(sarg) : 0.0f);
+                reinterpret_cast<float*>(srow + (2 * i + 1) * 32 + lane)[1] =
+                    SP ? sigmoid_f<ACC>(sarg) : 1.0f;
             }
-        } else {
+        } else if (warp == 1) {
 #pragma unroll
             for (int i = 0; i < kBwdTile; ++i) {
+                float* sr = reinterpret_cast<float*>(srow + (2 * i + 1) * 32 + lane);
                 if constexpr (HZ) {   // the gate's factors do not depend on the state
                     const float zv = r2[i], sz = sigmoid_f<ACC>(zv);
-                    S(kSG, i) = r1[i] * zv * sz;
-                    S(kSZF, i) = r1[i] * sz * fmaf(zv, 1.0f - sz, 1.0f);
+                    sr[0] = r1[i] * zv * sz;
+                    szf[i * 32 + lane] = r1[i] * sz * fmaf(zv, 1.0f - sz, 1.0f);
                 } else {
-                    S(kSG, i) = r1[i];
+                    sr[0] = r1[i];
                 }
             }
         }
 #pragma unroll
         for (int r = 0; r < kRowsPerThread; ++r) {
-            const int e = r * 32 * kBwdSplit + threadIdx.x;
+            const int e = r * 32 * SPL + threadIdx.x;
             if (e < kBwdTile * (NP / 2)) sbc[e] = bcr[r];
         }
 #pragma unroll
@@ -345,37 +376,37 @@ bwd_kernel(const BwdArgs a) {
             for (int j = 0; j < NPP; ++j) h2[j] = hs2[j];
 #pragma unroll
             for (int i = 0; i < kBwdTile; ++i) {
-                if (i >= nv) continue;
-                const float uv = S(kSU, i), dt = S(kSDT, i);
+                const float2 ud = srow[(2 * i) * 32 + lane];
+                const float uv = ud.x, dt = ud.y;
                 const float2 dtl2 = make_float2(dt * kLog2e, dt * kLog2e);
                 const float2 du2 = make_float2(dt * uv, dt * uv);
+                const float4* brow = sbc + i * (NP / 2) + n0 / 2;
                 float2 acc2 = make_float2(0.0f, 0.0f);
 #pragma unroll
                 for (int j = 0; j < NPP; ++j) {
-                    const float4 p = sbc[i * (NP / 2) + n0 / 2 + j];
+                    const float4 p = brow[j ^ pj];
                     const float2 ab = abar2_of<ACC>(dt, dtl2, A2[j]);
                     h2[j] = __ffma2_rn(ab, h2[j], __fmul2_rn(du2, make_float2(p.x, p.y)));
                     acc2 = __ffma2_rn(make_float2(p.z, p.w), h2[j], acc2);
                     hist2[(i * NPP + j) * 32 + lane] = h2[j];
                 }
-                P(warp, kPY, i) = (warp == 0 ? dsk * uv : 0.0f) + (acc2.x + acc2.y);
+                party[(warp * kBwdTile + i) * 32 + lane] =
+                    (warp == 0 ? dsk * uv : 0.0f) + (acc2.x + acc2.y);
             }
         }
         __syncwarp();
         // (c) backwards through the tile for this warp's entries, two entries
         //     at a time; h_t of step i is h_{t-1} of step i + 1, so each state
-        //     is read once
+        //     is read once.  (Kept rolled: the unrolled tile's code overflows
+        //     the instruction cache; measured on B300 6% slower.)
         float2 hn2[NPP];
 #pragma unroll
         for (int j = 0; j < NPP; ++j)
             hn2[j] = nv > 0 ? hist2[((nv - 1) * NPP + j) * 32 + lane] : make_float2(0.0f, 0.0f);
-        // (kept rolled: the unrolled tile's code overflows the instruction
-        // cache; measured on B300 6% slower)
 #pragma unroll 1
-        for (int i = kBwdTile - 1; i >= 0; --i) {
-            if (i >= nv) continue;
-            const long long t = t0 + i;
-            const float uv = S(kSU, i), dt = S(kSDT, i), g = S(kSG, i);
+        for (int i = nv - 1; i >= 0; --i) {
+            const float2 ud = srow[(2 * i) * 32 + lane];
+            const float uv = ud.x, dt = ud.y, g = srow[(2 * i + 1) * 32 + lane].x;
             const float2 g2 = make_float2(g, g), dt2 = make_float2(dt, dt), uv2 = make_float2(uv, uv);
             const float2 dtl2 = make_float2(dt * kLog2e, dt * kLog2e);
             float2 dus2 = make_float2(0.0f, 0.0f), dds2 = make_float2(0.0f, 0.0f);
@@ -383,9 +414,10 @@ bwd_kernel(const BwdArgs a) {
             // the states after step i - 1 (at i = 0 the checkpoint, hs2; the
             // row read is clamped so that every load stays in the history)
             const float2* hprev = hist2 + ((i > 0 ? i - 1 : 0) * NPP) * 32 + lane;
+            const float4* brow = sbc + i * (NP / 2) + n0 / 2;
 #pragma unroll
             for (int j = 0; j < NPP; ++j) {
-                const float4 p = sbc[i * (NP / 2) + n0 / 2 + j];
+                const float4 p = brow[j ^ pj];
                 const float2 B2 = make_float2(p.x, p.y), C2 = make_float2(p.z, p.w);
                 const float2 ht = hn2[j];
                 const float2 hp = i > 0 ? hprev[j * 32] : hs2[j];
@@ -403,50 +435,64 @@ bwd_kernel(const BwdArgs a) {
                 dA2[j] = __ffma2_rn(__fmul2_rn(dhd, ab), hp, dA2[j]);
                 dh2[j] = __fmul2_rn(dh2[j], ab);
             }
-            P(warp, kPDU, i) = (warp == 0 ? g * dsk : 0.0f) + (dus2.x + dus2.y);
-            P(warp, kPDD, i) = dds2.x + dds2.y;
-            const float sb = warp_sum_transpose<NPW>(pb, lane);
-            const float sc = warp_sum_transpose<NPW>(pc, lane);
+            partd[(warp * kBwdTile + i) * 32 + lane] =
+                make_float2((warp == 0 ? g * dsk : 0.0f) + (dus2.x + dus2.y), dds2.x + dds2.y);
+            const float sb = warp_sum_lanes<NPW>(pb);
+            const float sc = warp_sum_lanes<NPW>(pc);
+            __syncwarp();   // every lane has read its pairs of row i
             if (writer) {
-                pBg[t * NP + my_n] = sb;
-                pCg[t * NP + my_n] = sc;
+                sum_at[i * NP * 2] = sb;
+                sum_at[i * NP * 2 + 2] = sc;
             }
         }
         __syncthreads();
         // (d) the tile's outputs, one lane per row: warp 0 du and ddelta,
-        //     warp 1 dz; partial sums added in warp order
+        //     warp 1 dz; partial sums added in warp order.  The dB and dC
+        //     sums of the tile go out as whole rows of 4 entries.
         if (warp == 0) {
             float o[kBwdTile], od[kBwdTile];
 #pragma unroll
             for (int i = 0; i < kBwdTile; ++i) {
                 float su = 0.0f, sd = 0.0f;
 #pragma unroll
-                for (int w = 0; w < kBwdSplit; ++w) {
-                    su += P(w, kPDU, i);
-                    sd += P(w, kPDD, i);
+                for (int w = 0; w < SPL; ++w) {
+                    const float2 pd = partd[(w * kBwdTile + i) * 32 + lane];
+                    su += pd.x;
+                    sd += pd.y;
                 }
-                const bool on = i < nv;
+                const float2 ud = srow[(2 * i) * 32 + lane], gs = srow[(2 * i + 1) * 32 + lane];
                 o[i] = su;
-                od[i] = sd * S(kSSIG, i);
-                if (on) {
+                od[i] = sd * gs.y;
+                if (i < nv) {
                     dbias += od[i];
-                    dD = fmaf(S(kSG, i), S(kSU, i), dD);
+                    dD = fmaf(gs.x, ud.x, dD);
                 }
             }
             if (q.ok) {
                 store_tile_row<T>(dur, t0, nv, vec, o);
                 store_tile_row<T>(ddr, t0, nv, vec, od);
             }
-        } else if constexpr (HZ) {
+        } else if (HZ && warp == 1) {
             float o[kBwdTile];
 #pragma unroll
             for (int i = 0; i < kBwdTile; ++i) {
                 float sy = 0.0f;
 #pragma unroll
-                for (int w = 0; w < kBwdSplit; ++w) sy += P(w, kPY, i);
-                o[i] = S(kSZF, i) * sy;   // dz = dy (C.h + D u) silu'(z)
+                for (int w = 0; w < SPL; ++w) sy += party[(w * kBwdTile + i) * 32 + lane];
+                o[i] = szf[i * 32 + lane] * sy;   // dz = dy (C.h + D u) silu'(z)
             }
             if (q.ok) store_tile_row<T>(dzr, t0, nv, vec, o);
+        }
+        {
+            constexpr int kQuads = NP / 4;   // 4-entry quads per step
+            for (int e = threadIdx.x; e < nv * kQuads; e += 32 * SPL) {
+                const int i = e / kQuads, c = e % kQuads;
+                const float4 f0 = sbc[i * (NP / 2) + 2 * c];
+                const float4 f1 = sbc[i * (NP / 2) + 2 * c + 1];
+                const long long off = (t0 + i) * NP + 4 * c;
+                *reinterpret_cast<float4*>(pBg + off) = make_float4(f0.x, f0.y, f1.x, f1.y);
+                *reinterpret_cast<float4*>(pCg + off) = make_float4(f0.z, f0.w, f1.z, f1.w);
+            }
         }
         __syncthreads();   // shared memory is rewritten by the next tile
     }
@@ -455,7 +501,7 @@ bwd_kernel(const BwdArgs a) {
         for (int j = 0; j < NPP; ++j) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                const int n = n0 + 2 * j + e;
+                const int n = n0 + 2 * (j ^ pj) + e;
                 a.pA[q.row * NP + n] = e ? dA2[j].y : dA2[j].x;
                 if (a.dh0 && n < N) a.dh0[q.row * N + n] = e ? dh2[j].y : dh2[j].x;
             }
@@ -523,7 +569,7 @@ cudaError_t launch_bwd(const BwdArgs& a, bool hz, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     {
         ProfScope prof(kKindBwd, st);
-        k<<<(unsigned)units, 32 * kBwdSplit, smem, st>>>(a);
+        k<<<(unsigned)units, 32 * bwd_split<NP>(), smem, st>>>(a);
     }
     return cudaGetLastError();
 }
