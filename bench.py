@@ -551,28 +551,54 @@ def bwd_leg(shape, ins, dev, stream, mm, steps=10, warmup=3):
     """The backward pass on the same workload: gradients of every input from
     a random dy, with the final-state gradient off.  Device-resident inputs
     and outputs, CUDA events on the launching stream; per-kind device times
-    from the library's launch timing."""
+    from the library's launch timing.  Also the training pair: the forward
+    that keeps the checkpoints (mamba_scan_fwd_train) and the backward from
+    them (mamba_scan_bwd_ckpt), each timed alone, against the plain forward
+    and backward."""
     import torch
     g = torch.Generator(device=dev).manual_seed(11)
     dy = torch.randn(ins[0].shape, device=dev, generator=g).to(ins[0].dtype)
     out = mm.mamba_scan_bwd(*ins, dy, stream=stream)
-    for _ in range(warmup):
-        mm.mamba_scan_bwd(*ins, dy, out=out, stream=stream)
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    mm.mamba_profile_begin()
-    e0.record(stream)
-    for _ in range(steps):
-        mm.mamba_scan_bwd(*ins, dy, out=out, stream=stream)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    prof = mm.mamba_profile_end()
-    ms = e0.elapsed_time(e1) / steps
+
+    def timed(fn, n, prof=False):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if prof:
+            mm.mamba_profile_begin()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        kinds = mm.mamba_profile_end() if prof else None
+        return e0.elapsed_time(e1) / n, kinds
+
+    ms, prof = timed(lambda: mm.mamba_scan_bwd(*ins, dy, out=out, stream=stream), steps, True)
     updates = shape.batch * shape.dim * shape.seqlen * shape.dstate
-    return {"ms_per_step": ms, "value": shape.elems / (ms * 1e-3), "unit": UNIT, "steps": steps,
-            "state_updates_per_s": updates / (ms * 1e-3),
-            "launch_ms_by_kind": {k: v[0] / v[1] for k, v in prof.items() if v[1]},
-            "note": "checkpoint pass + reverse pass (recomputes each 12-step tile) + reductions"}
+    res = {"ms_per_step": ms, "value": shape.elems / (ms * 1e-3), "unit": UNIT, "steps": steps,
+           "state_updates_per_s": updates / (ms * 1e-3),
+           "launch_ms_by_kind": {k: v[0] / v[1] for k, v in prof.items() if v[1]},
+           "note": "checkpoint pass + reverse pass (recomputes each 12-step tile) + reductions; "
+                   "the checkpoint pass's own scan, chunk-summary and carry launches are also "
+                   "listed under their kinds"}
+    y = torch.empty_like(ins[0])
+    ck = torch.empty(mm.checkpoint_shape(shape.batch, shape.dim, shape.dstate, shape.seqlen),
+                     dtype=torch.float32, device=dev)
+    fwd_ms, _ = timed(lambda: mm.mamba_scan_fwd(*ins, True, y=y, stream=stream), steps)
+    train_ms, _ = timed(lambda: mm.mamba_scan_fwd_train(*ins, True, y=y, checkpoints=ck,
+                                                        stream=stream), steps)
+    bwd_ck_ms, prof2 = timed(lambda: mm.mamba_scan_bwd_ckpt(*ins, dy, ck, out=out, stream=stream),
+                             steps, True)
+    res["from_checkpoints"] = {
+        "fwd_train_ms": train_ms, "bwd_ckpt_ms": bwd_ck_ms,
+        "train_step_ms": train_ms + bwd_ck_ms, "fwd_plus_bwd_ms": fwd_ms + ms,
+        "fwd_ms": fwd_ms, "checkpoint_bytes": ck.numel() * 4,
+        "bwd_ckpt_launch_ms_by_kind": {k: v[0] / v[1] for k, v in prof2.items() if v[1]},
+        "note": "mamba_scan_fwd_train keeps the state every 12 steps; mamba_scan_bwd_ckpt "
+                "starts from them (same gradients, bit for bit)"}
+    return res
 
 
 def conv_leg(shape, x, dev, stream, mm, width=4, steps=50, warmup=5):

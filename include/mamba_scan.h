@@ -30,6 +30,9 @@
  *   mamba_scan_fwd_noalloc  mamba_scan_fwd with fixed scratch, no allocation
  *   mamba_state_update(_ex) one generation step on a caller-held state
  *   mamba_scan_bwd          gradients of every scan input (state recomputed)
+ *   mamba_scan_fwd_train    the forward of a training step: outputs plus the
+ *                           state checkpoints mamba_scan_bwd_ckpt reads
+ *   mamba_scan_bwd_ckpt     mamba_scan_bwd from those checkpoints
  *   mamba_conv1d_fwd        the causal convolution in front of the scan
  *   mamba_conv1d_update     its generation step
  *   plus status strings, the device error word and its self-test, tuning
@@ -276,6 +279,53 @@ int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
                    void *du, void *ddelta, float *dA, float *dB, float *dC,
                    float *dD_skip, void *dz, float *ddt_bias,
                    float *d_initial_state, cudaStream_t stream);
+
+/*
+ * A training step's pair: the forward keeps the state checkpoints that
+ * mamba_scan_bwd would otherwise recompute in its first pass, and the
+ * backward starts from them (the recomputation of each 12-step tile inside
+ * the reverse pass is unchanged; page "Mamba: linear-time sequence modeling
+ * with selective state spaces", "What they did").
+ *
+ * mamba_scan_checkpoint_bytes: the size of the checkpoint buffer,
+ *   batch * dim * ceil(seqlen / 12) * P * 4 bytes with P = dstate padded to
+ *   4, 8 or 16 (fp32 states, [batch][ceil(seqlen / 12)][dim][P]); -1 for an
+ *   invalid shape.  (For batch 4, dim 5120, dstate 16, seqlen 2048: 224 MB,
+ *   2.7 times one bf16 (batch, dim, seqlen) tensor.)
+ *
+ * mamba_scan_fwd_train: y and final_state exactly as mamba_scan_fwd_ex with
+ *   the same inputs and initial_state (Euler; flags: MAMBA_FLAG_SOFTPLUS
+ *   only, other bits -> MAMBA_ERR_FLAGS; no per-entry lengths), and writes
+ *   checkpoints (16-byte aligned, caller-owned, required when seqlen > 0):
+ *   the state before step 12k for every k < ceil(seqlen / 12), the initial
+ *   state (or zero) at k = 0.  Scratch as mamba_scan_fwd.  checkpoints must
+ *   not overlap any input or output (MAMBA_ERR_ALIAS).
+ *
+ * mamba_scan_bwd_ckpt: mamba_scan_bwd with the checkpoint pass replaced by
+ *   `checkpoints` from mamba_scan_fwd_train on the same inputs (the initial
+ *   state is in them, so there is no initial_state argument).  Results are
+ *   bit for bit those of mamba_scan_bwd.  Checkpoints from other inputs give
+ *   the gradients of a different forward; nothing checks this.  Scratch:
+ *   the partials of mamba_scan_bwd, no checkpoints.
+ */
+int64_t mamba_scan_checkpoint_bytes(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen);
+int mamba_scan_fwd_train(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                         mamba_dtype_t io_dtype,
+                         const void *u, const void *delta, const float *dt_bias,
+                         const float *A, const void *B, const void *C,
+                         const float *D_skip, const void *z, int flags,
+                         const float *initial_state, void *y, float *final_state,
+                         float *checkpoints, cudaStream_t stream);
+int mamba_scan_bwd_ckpt(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                        mamba_dtype_t io_dtype,
+                        const void *u, const void *delta, const float *dt_bias,
+                        const float *A, const void *B, const void *C,
+                        const float *D_skip, const void *z, int flags,
+                        const float *checkpoints, const void *dy,
+                        const float *d_final_state,
+                        void *du, void *ddelta, float *dA, float *dB, float *dC,
+                        float *dD_skip, void *dz, float *ddt_bias,
+                        float *d_initial_state, cudaStream_t stream);
 
 /*
  * Causal depthwise convolution with optional SiLU: the short convolution in

@@ -17,6 +17,7 @@ from ._lib import (  # noqa: F401
     MAMBA_FLAG_SOFTPLUS,
     MAMBA_FLAG_ZOH,
     MambaError,
+    checkpoint_shape,
     lib_path,
     load,
     mamba_conv1d_fwd,
@@ -27,9 +28,12 @@ from ._lib import (  # noqa: F401
     mamba_probe_pipe_rate,
     mamba_profile_end,
     mamba_scan_bwd,
+    mamba_scan_bwd_ckpt,
+    mamba_scan_checkpoint_bytes,
     mamba_scan_fwd,
     mamba_scan_fwd_ex,
     mamba_scan_fwd_noalloc,
+    mamba_scan_fwd_train,
     mamba_scan_set_tuning,
     mamba_selftest_bounds,
     mamba_selftest_wait_timeout,

@@ -23,7 +23,8 @@ EXPORTS = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_ex", "mam
            "mamba_state_update_ex", "mamba_status_string", "mamba_device_status",
            "mamba_selftest_wait_timeout", "mamba_version", "mamba_scan_set_tuning",
            "mamba_profile_begin", "mamba_profile_end", "mamba_probe_pipe_rate",
-           "mamba_debug_build", "mamba_selftest_bounds")
+           "mamba_debug_build", "mamba_selftest_bounds", "mamba_scan_checkpoint_bytes",
+           "mamba_scan_fwd_train", "mamba_scan_bwd_ckpt")
 
 # flags of the extended entry points
 MAMBA_FLAG_SOFTPLUS = 1
@@ -74,6 +75,13 @@ def load():
         lib.mamba_scan_bwd.argtypes = [i64, i64, i64, i64, i32] + [vp] * 8 + [i32] + [vp] * 3 \
             + [vp] * 9 + [vp]
         lib.mamba_scan_bwd.restype = i32
+        lib.mamba_scan_bwd_ckpt.argtypes = lib.mamba_scan_bwd.argtypes   # checkpoints for h0
+        lib.mamba_scan_bwd_ckpt.restype = i32
+        lib.mamba_scan_checkpoint_bytes.argtypes = [i64, i64, i64, i64]
+        lib.mamba_scan_checkpoint_bytes.restype = i64
+        lib.mamba_scan_fwd_train.argtypes = [i64, i64, i64, i64, i32] + [vp] * 8 + [i32] \
+            + [vp] * 4 + [vp]
+        lib.mamba_scan_fwd_train.restype = i32
         lib.mamba_conv1d_fwd.argtypes = [i64, i64, i64, i32, i32, vp, vp, vp, vp, i32, vp, vp, vp]
         lib.mamba_conv1d_fwd.restype = i32
         lib.mamba_conv1d_update.argtypes = [i64, i64, i32, i32, vp, vp, vp, vp, i32, vp, vp]
@@ -257,6 +265,79 @@ def mamba_scan_bwd(u, delta, dt_bias, A, B, C, D_skip, z, dy, softplus: bool = T
     (None without z), dA, dB, dC, dD_skip, ddt_bias and, when asked,
     d_initial_state.  dy has u's shape and dtype; d_final_state (batch, dim,
     N) fp32 is optional.  `out` may supply any of the output tensors."""
+    batch, dim, _ = u.shape
+    h0 = _ptr(initial_state, "initial_state", _torch().float32, (batch, dim, A.shape[1]),
+              u.device)
+    return _bwd_call("mamba_scan_bwd", h0, u, delta, dt_bias, A, B, C, D_skip, z, dy, softplus,
+                     d_final_state, want_initial_state_grad, out, stream)
+
+
+def mamba_scan_checkpoint_bytes(batch: int, dim: int, dstate: int, seqlen: int) -> int:
+    """Bytes of the state checkpoints of mamba_scan_fwd_train (-1: bad shape)."""
+    return int(load().mamba_scan_checkpoint_bytes(batch, dim, dstate, seqlen))
+
+
+def checkpoint_shape(batch: int, dim: int, dstate: int, seqlen: int) -> tuple:
+    """(batch, ceil(seqlen / 12), dim, dstate padded to 4, 8 or 16), fp32."""
+    pad = 4 if dstate <= 4 else (8 if dstate <= 8 else 16)
+    return (batch, (seqlen + 11) // 12, dim, pad)
+
+
+def mamba_scan_fwd_train(u, delta, dt_bias, A, B, C, D_skip, z, softplus: bool = True,
+                         initial_state=None, y=None, final_state=None, checkpoints=None,
+                         stream=None):
+    """The forward of a training step: y (and final_state) as mamba_scan_fwd_ex
+    from initial_state, plus the state checkpoints that mamba_scan_bwd_ckpt
+    reads (allocated if None, shape checkpoint_shape(...)).  Returns
+    (y, checkpoints)."""
+    torch = _torch()
+    lib = load()
+    batch, dim, L = u.shape
+    N = A.shape[1]
+    dev = u.device
+    io = _io_dtype(u)
+    if y is None:
+        y = torch.empty_like(u)
+    cks = checkpoint_shape(batch, dim, N, L)
+    if checkpoints is None:
+        checkpoints = torch.empty(cks, dtype=torch.float32, device=dev)
+    args = (
+        _ptr(u, "u", u.dtype, (batch, dim, L), dev),
+        _ptr(delta, "delta", u.dtype, (batch, dim, L), dev),
+        _ptr(dt_bias, "dt_bias", torch.float32, (dim,), dev),
+        _ptr(A, "A", torch.float32, (dim, N), dev),
+        _ptr(B, "B", u.dtype, (batch, N, L), dev),
+        _ptr(C, "C", u.dtype, (batch, N, L), dev),
+        _ptr(D_skip, "D_skip", torch.float32, (dim,), dev),
+        _ptr(z, "z", u.dtype, (batch, dim, L), dev),
+    )
+    hp = _ptr(initial_state, "initial_state", torch.float32, (batch, dim, N), dev)
+    yp = _ptr(y, "y", u.dtype, (batch, dim, L), dev)
+    fp = _ptr(final_state, "final_state", torch.float32, (batch, dim, N), dev)
+    cp = _ptr(checkpoints, "checkpoints", torch.float32, cks, dev)
+    with torch.cuda.device(dev):
+        st = _stream_handle(stream, dev)
+        rc = lib.mamba_scan_fwd_train(batch, dim, N, L, io, *args,
+                                      scan_flags(softplus), hp, yp, fp, cp, st)
+    if rc != 0:
+        raise MambaError(rc, "mamba_scan_fwd_train")
+    return y, checkpoints
+
+
+def mamba_scan_bwd_ckpt(u, delta, dt_bias, A, B, C, D_skip, z, dy, checkpoints,
+                        softplus: bool = True, d_final_state=None,
+                        want_initial_state_grad: bool = False, out=None, stream=None) -> dict:
+    """mamba_scan_bwd from the checkpoints of mamba_scan_fwd_train on the same
+    inputs (the initial state is inside them).  Same results, bit for bit."""
+    batch, dim, L = u.shape
+    cp = _ptr(checkpoints, "checkpoints", _torch().float32,
+              checkpoint_shape(batch, dim, A.shape[1], L), u.device)
+    return _bwd_call("mamba_scan_bwd_ckpt", cp, u, delta, dt_bias, A, B, C, D_skip, z, dy,
+                     softplus, d_final_state, want_initial_state_grad, out, stream)
+
+
+def _bwd_call(fn_name, state_ptr, u, delta, dt_bias, A, B, C, D_skip, z, dy, softplus,
+              d_final_state, want_initial_state_grad, out, stream) -> dict:
     torch = _torch()
     lib = load()
     batch, dim, L = u.shape
@@ -285,7 +366,6 @@ def mamba_scan_bwd(u, delta, dt_bias, A, B, C, D_skip, z, dy, softplus: bool = T
         _ptr(D_skip, "D_skip", f32, (dim,), dev),
         _ptr(z, "z", u.dtype, (batch, dim, L), dev),
     )
-    h0 = _ptr(initial_state, "initial_state", f32, (batch, dim, N), dev)
     dyp = _ptr(dy, "dy", u.dtype, (batch, dim, L), dev)
     dfp = _ptr(d_final_state, "d_final_state", f32, (batch, dim, N), dev)
     shapes = dict(du=((batch, dim, L), u.dtype), ddelta=((batch, dim, L), u.dtype),
@@ -295,12 +375,12 @@ def mamba_scan_bwd(u, delta, dt_bias, A, B, C, D_skip, z, dy, softplus: bool = T
     op = {k: _ptr(o[k], k, shapes[k][1], shapes[k][0], dev) for k in shapes}
     with torch.cuda.device(dev):
         st = _stream_handle(stream, dev)
-        rc = lib.mamba_scan_bwd(batch, dim, N, L, io, *ins, int(bool(softplus)), h0, dyp, dfp,
-                                op["du"], op["ddelta"], op["dA"], op["dB"], op["dC"],
-                                op["dD_skip"], op["dz"], op["ddt_bias"], op["d_initial_state"],
-                                st)
+        rc = getattr(lib, fn_name)(batch, dim, N, L, io, *ins, int(bool(softplus)), state_ptr,
+                                   dyp, dfp, op["du"], op["ddelta"], op["dA"], op["dB"],
+                                   op["dC"], op["dD_skip"], op["dz"], op["ddt_bias"],
+                                   op["d_initial_state"], st)
     if rc != 0:
-        raise MambaError(rc, "mamba_scan_bwd")
+        raise MambaError(rc, fn_name)
     return o
 
 

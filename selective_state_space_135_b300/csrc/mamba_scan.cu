@@ -272,8 +272,8 @@ struct ScanArgs {
     float* ws_h;  // chunk end states, then carried-in states (same layout)
     const float* h0;       // initial state (batch, dim, N), or null for zero
     const int* seqlens;    // per batch entry: steps in use, or null for all
-    float* ckpt;           // checkpoint mode: [row][ck_tiles][NP], the state before
-                           // every step that is a multiple of kBwdTile
+    float* ckpt;           // checkpoint modes: [batch][ck_tiles][dim][NP], the state
+                           // before every step that is a multiple of kBwdTile
     int ck_tiles;
     long long dim;
     long long seqlen;
@@ -503,8 +503,9 @@ __device__ __forceinline__ void load_bc(float4 (&bc)[NT / 2], const float4* row)
 // term).  The plain mode is compiled without the extensions: their per-tile
 // bookkeeping costs about 2% on B300.
 // kModeCkpt: the Euler scan from an initial state with no outputs, writing
-// state checkpoints for the backward pass.
-enum { kModePlain = 0, kModeExt = 1, kModeExtZoh = 2, kModeCkpt = 3 };
+// state checkpoints for the backward pass; kModeTrain: the same scan with
+// its outputs and the checkpoints (a training forward).
+enum { kModePlain = 0, kModeExt = 1, kModeExtZoh = 2, kModeCkpt = 3, kModeTrain = 4 };
 template <typename T, int NT, int SPLIT, bool STATE_ONLY, bool SOFTPLUS, bool HAS_Z, int MODE>
 __global__ void __launch_bounds__(32 * kScanWarps, kScanMinBlocks)
 scan_kernel(const __grid_constant__ ScanArgs a) {
@@ -517,11 +518,12 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     constexpr int kNPair = NT / 2;
     constexpr bool CKPT = MODE == kModeCkpt;
     constexpr bool OUT = !STATE_ONLY && !CKPT;   // y (and the partial sums it needs)
-    constexpr bool CKW = CKPT && !STATE_ONLY;    // writes checkpoints
+    constexpr bool CKW = (CKPT || MODE == kModeTrain) && !STATE_ONLY;   // writes checkpoints
     constexpr bool has_z = OUT && HAS_Z;
     constexpr bool EXT = MODE != kModePlain;
     constexpr bool ZOH = MODE == kModeExtZoh;
     static_assert(NT % 2 == 0 && NP <= kMaxN, "bad state size");
+    static_assert(TT <= 32, "the checkpoint schedule of a tile is a 32-bit mask");
     static_assert(CK::G == G && QC * G == HT && QC >= 1, "a slice's steps are whole 16-byte chunks");
 
     // Offset the __shared__ array itself (not a pointer rebuilt from an
@@ -717,21 +719,34 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
         }
     };
 
-    // checkpoint mode: this warp's NT entries of the state before step `step`
-    // (a multiple of kBwdTile) into ckpt[(row * ck_tiles + step / kBwdTile) * NP + hh * NT]
+    // checkpoint modes: this warp's NT entries of the state before step
+    // `step` (a multiple of kBwdTile) into
+    // ckpt[((b * ck_tiles + step / kBwdTile) * dim + d) * NP + hh * NT]
+    // (adjacent channels adjacent, so a warp's stores share sectors).  The
+    // unit writes its checkpoints in step order: ck_at is the element index
+    // of the next one, advanced by dim * NP per write.  A unit from step 0
+    // writes checkpoint 0 (the initial state) first; a unit from t0 > 0
+    // writes those after its steps, from t0 / kBwdTile + 1 on (the one at
+    // t0 itself, if any, is the end state of the unit before it).
+    long long ck_at = 0;
+    if constexpr (CKW) {
+        const long long k0 = w.t0 == 0 ? 0 : w.t0 / kBwdTile + 1;
+        ck_at = (((long long)w.b * a.ck_tiles + k0) * dim + d) * NP + hh * NT;
+    }
     auto write_ckpt = [&](long long step) {
-        if (!chan_ok || step >= L_) return;
-        const long long k = step / kBwdTile;
-        const long long base = (row * a.ck_tiles + k) * NP + hh * NT;
-        const long long ext = (long long)a.batch * dim * a.ck_tiles * NP;
-        (void)ext;
-        if (MAMBA_IN(base, ext) && MAMBA_IN(base + NT - 1, ext)) {
-            float2* p2 = reinterpret_cast<float2*>(a.ckpt + base);
+        if (chan_ok && step < L_) {
+            const long long ext = (long long)a.batch * dim * a.ck_tiles * NP;
+            (void)ext;
+            if (MAMBA_IN(ck_at, ext) && MAMBA_IN(ck_at + NT - 1, ext)) {
+                float2* p2 = reinterpret_cast<float2*>(a.ckpt + ck_at);
 #pragma unroll
-            for (int i = 0; i < kNPair; ++i) p2[i] = h2[i];
+                for (int i = 0; i < kNPair; ++i) p2[i] = h2[i];
+            }
         }
+        ck_at += dim * NP;
     };
     (void)write_ckpt;
+    (void)ck_at;
     if constexpr (CKW) {
         if (w.t0 == 0) write_ckpt(0);   // the initial state
     }
@@ -746,9 +761,13 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
 
     for (int it = 0; it < ntiles && !aborted; ++it) {
         const long long tt0 = w.t0 + (long long)it * TT;
-        // the first t + 1 (1 .. kBwdTile) with tt0 + t + 1 a multiple of kBwdTile
-        const int ck0 = kBwdTile - (int)(tt0 % kBwdTile);
-        (void)ck0;
+        // bit t: tt0 + t + 1 is a multiple of kBwdTile (a checkpoint after step t)
+        uint32_t ckmask = 0;
+        if constexpr (CKW) {
+            for (int t1 = kBwdTile - (int)(tt0 % kBwdTile); t1 <= TT; t1 += kBwdTile)
+                ckmask |= 1u << (t1 - 1);
+        }
+        (void)ckmask;
         const int nv = (int)min((long long)TT, w.t1 - tt0);   // steps of this unit in the tile
         // with per-entry lengths, the steps of the tile past them get y = 0
         // (without, steps past the sequence are not stored at all)
@@ -815,10 +834,8 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
                         pseg[t / HT][t * CH] = pt;
                 }
                 if constexpr (CKW) {
-                    // after step t the state is the one before step tt0 + t + 1:
-                    // a checkpoint when that is a multiple of kBwdTile
-                    if (t + 1 == ck0 || t + 1 == ck0 + kBwdTile || t + 1 == ck0 + 2 * kBwdTile)
-                        write_ckpt(tt0 + t + 1);
+                    // after step t the state is the one before step tt0 + t + 1
+                    if (ckmask & (1u << t)) write_ckpt(tt0 + t + 1);
                 }
             }
         }
@@ -1331,11 +1348,13 @@ cudaError_t dispatch_mode(int mode, bool sp, bool hz, const ScanArgs& a, int gri
                           cudaStream_t st) {
     if (mode == kModeExtZoh)
         return dispatch_flags<T, STATE_ONLY, NT, S, kModeExtZoh>(sp, hz, a, grid, smem, st);
-    if (mode == kModeCkpt) {   // its summary pass is the extended mode's
+    if (mode == kModeCkpt || mode == kModeTrain) {   // summary pass: the extended mode's
         if constexpr (STATE_ONLY)
             return dispatch_flags<T, STATE_ONLY, NT, S, kModeExt>(sp, hz, a, grid, smem, st);
-        else
+        else if (mode == kModeCkpt)
             return dispatch_flags<T, STATE_ONLY, NT, S, kModeCkpt>(sp, hz, a, grid, smem, st);
+        else
+            return dispatch_flags<T, STATE_ONLY, NT, S, kModeTrain>(sp, hz, a, grid, smem, st);
     }
     if (mode == kModeExt)
         return dispatch_flags<T, STATE_ONLY, NT, S, kModeExt>(sp, hz, a, grid, smem, st);
@@ -1545,7 +1564,7 @@ int noalloc_scratch(void** out) {
 
 // Bytes of packed B/C rows per (batch entry, step): 2 * padded state * fp32.
 long long packed_row_bytes(int64_t dstate) {
-    return 2LL * (dstate <= 4 ? 4 : (dstate <= 8 ? 8 : 16)) * (long long)sizeof(float);
+    return 2LL * padded_state(dstate) * (long long)sizeof(float);
 }
 
 }  // namespace mamba
@@ -1718,6 +1737,13 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
             if (overlaps(final_state, fsb, ins[i], insz[i])) return MAMBA_ERR_ALIAS;
         }
         if (overlaps(y, big, final_state, fsb)) return MAMBA_ERR_ALIAS;
+        if (ckpt) {
+            const size_t ckb = (size_t)(batch * dim) * ck_tiles * padded_state(dstate) * 4;
+            for (int i = 0; i < 10; ++i)
+                if (overlaps(ckpt, ckb, ins[i], insz[i])) return MAMBA_ERR_ALIAS;
+            if (overlaps(ckpt, ckb, y, big) || overlaps(ckpt, ckb, final_state, fsb))
+                return MAMBA_ERR_ALIAS;
+        }
     }
     if (seqlen == 0) {
         if (final_state) {
@@ -1813,7 +1839,7 @@ static int scan_fwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t s
                        (int)dstate, pl.np, acc ? 1.0f : kLn2, stream);
     const bool bf = io_dtype == MAMBA_BF16;
     const bool hz = z != nullptr;
-    const int mode = ckpt ? kModeCkpt
+    const int mode = ckpt ? (y ? kModeTrain : kModeCkpt)
                           : (zoh ? kModeExtZoh : ((h0 || seqlens) ? kModeExt : kModePlain));
     auto summary_and_carry = [&](cudaStream_t st) -> cudaError_t {
         const int grid1 = (pl.n_groups - pl.n_full) * (pl.nchunks - 1);
@@ -1884,6 +1910,29 @@ int mamba_scan_fwd_noalloc(int64_t batch, int64_t dim, int64_t dstate, int64_t s
     return scan_fwd_common(batch, dim, dstate, seqlen, io_dtype, u, delta, dt_bias, A, B, C,
                            D_skip, z, softplus, false, nullptr, nullptr, y, final_state, stream,
                            true);
+}
+
+int64_t mamba_scan_checkpoint_bytes(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen) {
+    if (batch < 1 || dim < 1 || dstate < 1 || dstate > kMaxN || seqlen < 0) return -1;
+    if ((double)batch * dim * (double)checkpoint_tiles(seqlen) * padded_state(dstate) * 4.0 > 4.0e18)
+        return -1;
+    return batch * dim * checkpoint_tiles(seqlen) * padded_state(dstate) * (int64_t)sizeof(float);
+}
+
+int mamba_scan_fwd_train(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                         mamba_dtype_t io_dtype, const void* u, const void* delta,
+                         const float* dt_bias, const float* A, const void* B, const void* C,
+                         const float* D_skip, const void* z, int flags,
+                         const float* initial_state, void* y, float* final_state,
+                         float* checkpoints, cudaStream_t stream) {
+    if (flags & ~MAMBA_FLAG_SOFTPLUS) return MAMBA_ERR_FLAGS;
+    if (seqlen > 0 && (!y || !checkpoints)) return MAMBA_ERR_NULL;
+    if (checkpoints && !aligned(checkpoints, 16)) return MAMBA_ERR_ALIGN;
+    if (seqlen < 0 || checkpoint_tiles(seqlen) > INT32_MAX) return MAMBA_ERR_SHAPE;
+    return scan_fwd_common(batch, dim, dstate, seqlen, io_dtype, u, delta, dt_bias, A, B, C,
+                           D_skip, z, (flags & MAMBA_FLAG_SOFTPLUS) ? 1 : 0, false, initial_state,
+                           nullptr, y, final_state, stream, false, seqlen > 0 ? checkpoints : nullptr,
+                           (int)checkpoint_tiles(seqlen));
 }
 
 int mamba_scan_fwd_ex(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, mamba_dtype_t io_dtype,
@@ -1983,7 +2032,7 @@ int scan_checkpoints(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
                      const void* u, const void* delta, const float* dt_bias, const float* A,
                      const void* B, const void* C, int softplus, const float* initial_state,
                      float* ckpt, int ck_tiles, cudaStream_t stream) {
-    if (!ckpt || ck_tiles != (int)((seqlen + kBwdTile - 1) / kBwdTile)) return MAMBA_ERR_SHAPE;
+    if (!ckpt || ck_tiles != (int)checkpoint_tiles(seqlen)) return MAMBA_ERR_SHAPE;
     return scan_fwd_common(batch, dim, dstate, seqlen, io_dtype, u, delta, dt_bias, A, B, C,
                            nullptr, nullptr, softplus, false, initial_state, nullptr, nullptr,
                            nullptr, stream, false, ckpt, ck_tiles);

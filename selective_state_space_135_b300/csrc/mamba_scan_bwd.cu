@@ -50,7 +50,7 @@ struct BwdArgs {
     const float* D_skip;
     const float* h0;      // initial state or null
     const float* dfinal;  // dJ / d final state or null
-    float* ckpt;          // [row][ntiles][NP]: state before each tile
+    float* ckpt;          // [batch][ntiles][dim][NP]: state before each tile
     void* du;
     void* ddelta;
     void* dz;
@@ -289,7 +289,9 @@ bwd_kernel(const BwdArgs a) {
     T* ddr = static_cast<T*>(a.ddelta) + q.row * L;
     T* dzr = HZ ? static_cast<T*>(a.dz) + q.row * L : nullptr;
     const float4* bcb = a.bc + (long long)q.b * L * (NP / 2);
-    const float2* ck = reinterpret_cast<const float2*>(a.ckpt + q.row * a.ntiles * NP + n0);
+    // checkpoint of tile kk: pair j at ck[kk * dim * NP / 2 + j]
+    const float2* ck = reinterpret_cast<const float2*>(
+        a.ckpt + ((long long)q.b * a.ntiles * a.dim + q.d) * NP + n0);
     // after the butterfly this lane holds the sums of entry n0 + le; the first
     // lane of each group that shares an entry stores them into the B/C row
     const int le = bwd_lane_entry<NPW>(lane);
@@ -326,7 +328,7 @@ bwd_kernel(const BwdArgs a) {
         }
 #pragma unroll
         for (int j = 0; j < NPP; ++j)
-            ckr[j] = q.ok ? ck[kk * (NP / 2) + (j ^ pj)] : make_float2(0.f, 0.f);
+            ckr[j] = q.ok ? ck[(long long)kk * a.dim * (NP / 2) + (j ^ pj)] : make_float2(0.f, 0.f);
     };
     if (a.ntiles > 0) fetch(a.ntiles - 1);
 
@@ -588,14 +590,17 @@ cudaError_t dispatch_bwd(int np, bool sp, bool hz, const BwdArgs& a, cudaStream_
 
 using namespace mamba;
 
-extern "C" {
+namespace {
 
-int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, mamba_dtype_t io_dtype,
-                   const void* u, const void* delta, const float* dt_bias, const float* A,
-                   const void* B, const void* C, const float* D_skip, const void* z, int flags,
-                   const float* initial_state, const void* dy, const float* d_final_state,
-                   void* du, void* ddelta, float* dA, float* dB, float* dC, float* dD_skip,
-                   void* dz, float* ddt_bias, float* d_initial_state, cudaStream_t stream) {
+// Both backward entry points.  ckpt_in: the checkpoints of a training
+// forward (then the checkpoint pass is skipped), or null.
+int bwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io_dtype,
+               const void* u, const void* delta, const float* dt_bias, const float* A,
+               const void* B, const void* C, const float* D_skip, const void* z, int flags,
+               const float* initial_state, const float* ckpt_in, const void* dy,
+               const float* d_final_state, void* du, void* ddelta, float* dA, float* dB,
+               float* dC, float* dD_skip, void* dz, float* ddt_bias, float* d_initial_state,
+               cudaStream_t stream) {
     if (flags & ~MAMBA_FLAG_SOFTPLUS) return MAMBA_ERR_FLAGS;
     if (io_dtype != MAMBA_F32 && io_dtype != MAMBA_BF16) return MAMBA_ERR_DTYPE;
     if (batch < 1 || dim < 1 || dstate < 1 || dstate > kMaxN || seqlen < 0) return MAMBA_ERR_SHAPE;
@@ -606,6 +611,7 @@ int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, m
     if (seqlen > 0 && (!u || !delta || !B || !C || !dy || !du || !ddelta || !dB || !dC))
         return MAMBA_ERR_NULL;
     if (z && seqlen > 0 && !dz) return MAMBA_ERR_NULL;
+    if (seqlen > 0 && checkpoint_tiles(seqlen) > INT32_MAX) return MAMBA_ERR_SHAPE;
     const int es = esize(io_dtype);
     const size_t big = (size_t)(batch * dim * seqlen) * es;
     const size_t bcb = (size_t)(batch * dstate * seqlen) * es;
@@ -620,14 +626,16 @@ int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, m
                           (const void*)dB, (const void*)dC, (const void*)dD_skip,
                           (const void*)ddt_bias, (const void*)d_initial_state})
         if (q && !aligned(q, 4)) return MAMBA_ERR_ALIGN;
+    if (ckpt_in && !aligned(ckpt_in, 16)) return MAMBA_ERR_ALIGN;
     {
+        const size_t ckb = (size_t)(batch * dim) * checkpoint_tiles(seqlen) * padded_state(dstate) * 4;
         const void* ins[] = {u, delta, z, dy, B, C, dt_bias, A, D_skip, initial_state,
-                             d_final_state};
-        const size_t insz[] = {big, big, big, big, bcb, bcb, vb, ab, vb, stb, stb};
+                             d_final_state, ckpt_in};
+        const size_t insz[] = {big, big, big, big, bcb, bcb, vb, ab, vb, stb, stb, ckb};
         void* outs[] = {du, ddelta, dz, dA, dB, dC, dD_skip, ddt_bias, d_initial_state};
         const size_t outsz[] = {big, big, big, ab, bcf, bcf, vb, vb, stb};
         for (int o = 0; o < 9; ++o) {
-            for (int i = 0; i < 11; ++i)
+            for (int i = 0; i < 12; ++i)
                 if (overlaps(outs[o], outsz[o], ins[i], insz[i])) return MAMBA_ERR_ALIAS;
             for (int p = o + 1; p < 9; ++p)
                 if (overlaps(outs[o], outsz[o], outs[p], outsz[p])) return MAMBA_ERR_ALIAS;
@@ -648,12 +656,12 @@ int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, m
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MAMBA_ERR_CUDA;
-    const int np = dstate <= 4 ? 4 : (dstate <= 8 ? 8 : 16);
+    const int np = padded_state(dstate);
     const int groups = (int)((dim + 31) / 32);
-    const int ntiles = (int)((seqlen + kBwdTile - 1) / kBwdTile);
+    const int ntiles = (int)checkpoint_tiles(seqlen);
     const size_t rows = (size_t)(batch * dim);
     const size_t sz_bc = (size_t)batch * seqlen * (np / 2) * sizeof(float4);
-    const size_t sz_ck = rows * ntiles * np * sizeof(float);
+    const size_t sz_ck = ckpt_in ? 0 : rows * ntiles * np * sizeof(float);
     const size_t sz_p = (size_t)groups * batch * seqlen * np * sizeof(float);
     const size_t sz_a = rows * np * sizeof(float);
     const size_t sz_r = rows * sizeof(float);
@@ -671,7 +679,8 @@ int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, m
     BwdArgs a;
     std::memset(&a, 0, sizeof(a));
     a.bc = reinterpret_cast<const float4*>(p); p += up(sz_bc);
-    a.ckpt = reinterpret_cast<float*>(p); p += up(sz_ck);
+    a.ckpt = ckpt_in ? const_cast<float*>(ckpt_in) : reinterpret_cast<float*>(p);
+    p += up(sz_ck);
     a.pB = reinterpret_cast<float*>(p); p += up(sz_p);
     a.pC = reinterpret_cast<float*>(p); p += up(sz_p);
     a.pA = reinterpret_cast<float*>(p); p += up(sz_a);
@@ -687,9 +696,9 @@ int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, m
     for (const void* q : {u, delta, z, dy, (const void*)du, (const void*)ddelta, (const void*)dz})
         if (q && !aligned(q, 8)) a.vec8 = 0;
 
-    // checkpoints: the forward kernel's checkpoint mode (its own B/C table and
-    // plan, from the same pool on the same stream)
-    {
+    // checkpoints (unless given): the forward kernel's checkpoint mode (its
+    // own B/C table and plan, from the same pool on the same stream)
+    if (!ckpt_in) {
         ProfScope prof(kKindBwdCheckpoint, stream);
         rc = scan_checkpoints(batch, dim, dstate, seqlen, io_dtype, u, delta, dt_bias, A, B, C,
                               sp ? 1 : 0, initial_state, a.ckpt, ntiles, stream);
@@ -720,6 +729,34 @@ int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, m
     }
     cudaFreeAsync(scratch, stream);
     return e == cudaSuccess ? MAMBA_OK : MAMBA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, mamba_dtype_t io_dtype,
+                   const void* u, const void* delta, const float* dt_bias, const float* A,
+                   const void* B, const void* C, const float* D_skip, const void* z, int flags,
+                   const float* initial_state, const void* dy, const float* d_final_state,
+                   void* du, void* ddelta, float* dA, float* dB, float* dC, float* dD_skip,
+                   void* dz, float* ddt_bias, float* d_initial_state, cudaStream_t stream) {
+    return bwd_common(batch, dim, dstate, seqlen, io_dtype, u, delta, dt_bias, A, B, C, D_skip,
+                      z, flags, initial_state, nullptr, dy, d_final_state, du, ddelta, dA, dB,
+                      dC, dD_skip, dz, ddt_bias, d_initial_state, stream);
+}
+
+int mamba_scan_bwd_ckpt(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
+                        mamba_dtype_t io_dtype, const void* u, const void* delta,
+                        const float* dt_bias, const float* A, const void* B, const void* C,
+                        const float* D_skip, const void* z, int flags, const float* checkpoints,
+                        const void* dy, const float* d_final_state, void* du, void* ddelta,
+                        float* dA, float* dB, float* dC, float* dD_skip, void* dz,
+                        float* ddt_bias, float* d_initial_state, cudaStream_t stream) {
+    if (seqlen > 0 && !checkpoints) return MAMBA_ERR_NULL;
+    return bwd_common(batch, dim, dstate, seqlen, io_dtype, u, delta, dt_bias, A, B, C, D_skip,
+                      z, flags, nullptr, checkpoints, dy, d_final_state, du, ddelta, dA, dB,
+                      dC, dD_skip, dz, ddt_bias, d_initial_state, stream);
 }
 
 }  // extern "C"

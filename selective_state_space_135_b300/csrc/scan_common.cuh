@@ -164,6 +164,10 @@ static inline int take_debug_word() {
 // ---------------------------------------------------------------------------
 
 inline int esize(int dt) { return dt == MAMBA_BF16 ? 2 : 4; }
+// dstate padded to the state sizes the kernels are built for: 4, 8 or 16
+inline int padded_state(int64_t dstate) { return dstate <= 4 ? 4 : (dstate <= 8 ? 8 : 16); }
+// state checkpoints of a sequence: one before every kBwdTile steps
+inline int64_t checkpoint_tiles(int64_t seqlen) { return (seqlen + kBwdTile - 1) / kBwdTile; }
 
 // The debug word of the convolution's translation unit (mamba_conv.cu).
 int conv_take_debug_word();
@@ -198,9 +202,10 @@ int sm_count(int dev);
 int get_pool(int dev, cudaMemPool_t* out);
 // The forward scan in its checkpoint mode (mamba_scan.cu): the Euler scan
 // from initial_state (or zero) with no outputs, writing the state before
-// every step that is a multiple of kBwdTile into ckpt[(row * ck_tiles + k) *
-// np + n] (np = dstate padded to 4, 8 or 16; ck_tiles = ceil(seqlen /
-// kBwdTile)).  Scratch from the stream-ordered pool.  Returns a status.
+// every step that is a multiple of kBwdTile into ckpt[((b * ck_tiles + k) *
+// dim + d) * np + n] (np = dstate padded to 4, 8 or 16; ck_tiles =
+// ceil(seqlen / kBwdTile)).  Scratch from the stream-ordered pool.  Returns
+// a status.
 int scan_checkpoints(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io_dtype,
                      const void* u, const void* delta, const float* dt_bias, const float* A,
                      const void* B, const void* C, int softplus, const float* initial_state,

@@ -305,3 +305,56 @@ def test_header_is_plain_c(tmp_path):
            str(src), "-o", str(exe), lib, f"-Wl,-rpath,{os.path.dirname(lib)}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_checkpoint_bytes(lib):
+    # batch * dim * ceil(seqlen / 12) * padded dstate * 4 bytes
+    assert lib.mamba_scan_checkpoint_bytes(2, 16, 4, 64) == 2 * 16 * 6 * 4 * 4
+    assert lib.mamba_scan_checkpoint_bytes(1, 3, 5, 12) == 1 * 3 * 1 * 8 * 4
+    assert lib.mamba_scan_checkpoint_bytes(1, 3, 16, 13) == 1 * 3 * 2 * 16 * 4
+    assert lib.mamba_scan_checkpoint_bytes(1, 3, 16, 0) == 0
+    assert lib.mamba_scan_checkpoint_bytes(1, 3, 17, 10) == -1
+    assert lib.mamba_scan_checkpoint_bytes(0, 3, 4, 10) == -1
+    for b, d, n, l in ((2, 16, 4, 64), (1, 3, 5, 12), (3, 7, 16, 25)):
+        shp = _lib.checkpoint_shape(b, d, n, l)
+        assert lib.mamba_scan_checkpoint_bytes(b, d, n, l) == 4 * shp[0] * shp[1] * shp[2] * shp[3]
+
+
+def train_call(lib, flags=SOFTPLUS, extra=None, **over):
+    names = ("u", "delta", "dtb", "A", "B", "C", "Dk", "z", "h0", "y", "fin", "ckpt")
+    v = {k: addr(i, (extra or {}).get(k, 0)) for i, k in enumerate(names, 1)}
+    v.update(over)
+    return lib.mamba_scan_fwd_train(2, 16, 16, 64, 1, v["u"], v["delta"], v["dtb"], v["A"],
+                                    v["B"], v["C"], v["Dk"], v["z"], flags, v["h0"], v["y"],
+                                    v["fin"], v["ckpt"], None)
+
+
+def test_scan_fwd_train_validation(lib):
+    # every case is rejected on the host, before any CUDA call
+    assert train_call(lib, flags=ZOH) == EFLAGS
+    assert train_call(lib, flags=SOFTPLUS | NOALLOC) == EFLAGS
+    for k in ("u", "delta", "A", "B", "C", "y", "ckpt"):
+        assert train_call(lib, **{k: None}) == ENULL, k
+    assert train_call(lib, extra={"ckpt": 8}) == EALIGN     # checkpoints need 16 bytes
+    assert train_call(lib, ckpt=addr(1)) == EALIAS          # on top of u
+    assert train_call(lib, ckpt=addr(10)) == EALIAS         # on top of y
+    assert train_call(lib, ckpt=addr(11)) == EALIAS         # on top of final_state
+
+
+def test_scan_bwd_ckpt_validation(lib):
+    def call(**over):
+        names = ("u", "delta", "dtb", "A", "B", "C", "Dk", "z", "ckpt", "dy", "dfin", "du",
+                 "ddelta", "dA", "dB", "dC", "dD", "dz", "dbias", "dh0")
+        flags = over.pop("flags", SOFTPLUS)
+        extra = over.pop("extra", {})
+        v = {k: addr(i, extra.get(k, 0)) for i, k in enumerate(names, 1)}
+        v.update(over)
+        return lib.mamba_scan_bwd_ckpt(2, 16, 16, 64, 1, *(v[k] for k in names[:8]), flags,
+                                       *(v[k] for k in names[8:]), None)
+    assert call(flags=ZOH) == EFLAGS
+    assert call(ckpt=None) == ENULL
+    for k in ("u", "dy", "du", "dB"):
+        assert call(**{k: None}) == ENULL, k
+    assert call(extra={"ckpt": 4}) == EALIGN
+    assert call(du=addr(9)) == EALIAS                 # du on top of the checkpoints
+    assert call(dh0=addr(9)) == EALIAS                # d_initial_state on top of them
