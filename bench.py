@@ -43,6 +43,9 @@ METRIC = "scan throughput (B*L*D elems/s)"
 UNIT = "elems/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "scan_traffic.json")
+# the output of `python bench.py --pipe-rates` on a B300 (measured per-SM
+# rates of the scan's arithmetic), the source of the measured ceiling
+PIPE_RATES_FILE = os.path.join(ROOT, "profiles", "pipe_rates.json")
 KERNEL_SRC = os.path.join(ROOT, "selective_state_space_135_b300", "csrc", "mamba_scan.cu")
 # Per-SM unit counts of B300 (sm_103): 128 fp32 lanes (one fp32 multiply or
 # FMA per lane per clock, packed f32x2 included) and 32 ex2 results per clock
@@ -264,6 +267,16 @@ PIPE_KINDS = {0: "ex2", 1: "lg2", 2: "tanh", 3: "ffma2 (lane-ops)", 4: "ffma",
               5: "scan state update (2 ex2 + 4 packed ops per 2 updates)"}
 
 
+def load_pipe_ceiling():
+    """State updates per clock per SM that the scan's core arithmetic reaches
+    alone on B300 (committed measurement), or None."""
+    try:
+        with open(PIPE_RATES_FILE) as f:
+            return float(json.load(f)["scan_core_ceiling"]["state_updates_per_clk_sm"])
+    except Exception:
+        return None
+
+
 def run_pipe_rates():
     """Sustained per-SM rates, in lane operations per SM clock, of each kind
     of arithmetic the scan uses, with 1 to 8 warps per SM sub-partition and
@@ -392,6 +405,7 @@ def run_ours(args, shape):
     updates = shape.batch * shape.dim * shape.seqlen * shape.dstate
     alu_peak = min(FP32_LANES_PER_SM / FP32_OPS_PER_UPDATE, EX2_PER_CLK_SM) * N_SM * smax * 1e6
     alu_achieved = updates / (k_ms * 1e-3)
+    ceiling = load_pipe_ceiling()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     hbm_achieved = shape.io_bytes() / (k_ms * 1e-3) / 1e9
     traffic = load_traffic(shape.name)
@@ -405,6 +419,13 @@ def run_ours(args, shape):
                        f"{FP32_OPS_PER_UPDATE} ops, {EX2_PER_CLK_SM} ex2) per clock x "
                        f"{smax:.0f} MHz ({peak_src} sm_max)",
         "work_per_launch": f"{updates:.4g} state updates (B*D*L*N)",
+        "measured_ceiling": None if ceiling is None else {
+            "achieved": alu_achieved / 1e12,
+            "peak": ceiling * N_SM * smax * 1e6 / 1e12, "unit": "T state-updates/s",
+            "frac": alu_achieved / (ceiling * N_SM * smax * 1e6),
+            "peak_source": f"{ceiling:.2f} state updates per clock per SM (the state update's "
+                           f"2 ex2 + 4 packed fp32 ops, measured alone: profiles/pipe_rates.json)"
+                           f" x {N_SM} SMs x {smax:.0f} MHz"},
         "hbm": {"achieved": hbm_achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": hbm_achieved / hbm_peak, "peak_source": peak_src,
                 "algorithmic_bytes_per_launch": shape.io_bytes(),
