@@ -515,21 +515,50 @@ bwd_kernel(const BwdArgs a) {
     }
 }
 
-// dB[b][n][t] (or dC) = sum over channel groups of the partials, in group order.
+// dB[b][n][t] and dC[b][n][t] = sums over channel groups of the partials
+// (blockIdx.y: 0 for dB, 1 for dC).  A block takes kReduceThreads / S
+// consecutive partial elements; each of its S parts of threads adds the
+// groups [groups * s / S, groups * (s + 1) / S) in group order, and the part
+// sums are added in part order: a fixed order, so the result is
+// deterministic.  S = 4 when there are many groups (the 2.8B layer's 160),
+// else 1.
+template <int S>
 __global__ void __launch_bounds__(kReduceThreads)
-bwd_reduce_bc_kernel(const float* __restrict__ part, float* __restrict__ out, int groups,
-                     int batch, long long L, int N, int NP) {
+bwd_reduce_bc_kernel(const float* __restrict__ pB, const float* __restrict__ pC,
+                     float* __restrict__ dB, float* __restrict__ dC, int groups, int batch,
+                     long long L, int N, int NP) {
+    constexpr int kOuts = kReduceThreads / S;
+    __shared__ float part_sum[S][kOuts];
+    const float* part = blockIdx.y ? pC : pB;
+    float* out = blockIdx.y ? dC : dB;
     const long long total = (long long)batch * L * NP;
-    const long long stride = total;
-    for (long long i = (long long)blockIdx.x * kReduceThreads + threadIdx.x; i < total;
-         i += (long long)gridDim.x * kReduceThreads) {
-        const int n = (int)(i % NP);
-        if (n >= N) continue;
-        const long long bt = i / NP;           // b * L + t
-        const long long b = bt / L, t = bt - b * L;
+    const int q = threadIdx.x / kOuts, o = threadIdx.x % kOuts;
+    const int g0 = (int)((long long)groups * q / S), g1 = (int)((long long)groups * (q + 1) / S);
+    for (long long base = (long long)blockIdx.x * kOuts; base < total;
+         base += (long long)gridDim.x * kOuts) {
+        const long long i = base + o;
         float s = 0.0f;
-        for (int g = 0; g < groups; ++g) s += part[g * stride + i];
-        out[(b * N + n) * L + t] = s;
+        if (i < total) {
+#pragma unroll 8
+            for (int g = g0; g < g1; ++g) s += part[g * total + i];
+        }
+        if constexpr (S > 1) {
+            part_sum[q][o] = s;
+            __syncthreads();
+            if (q == 0) {
+#pragma unroll
+                for (int k = 1; k < S; ++k) s += part_sum[k][o];
+            }
+            __syncthreads();
+        }
+        if (q == 0 && i < total) {
+            const int n = (int)(i % NP);
+            if (n < N) {
+                const long long bt = i / NP;   // b * L + t
+                const long long b = bt / L, t = bt - b * L;
+                out[(b * N + n) * L + t] = s;
+            }
+        }
     }
 }
 
@@ -716,11 +745,14 @@ int bwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int i
         ProfScope prof(kKindBwdReduce, stream);
         const int cap = 16 * sm_count(dev);
         const long long nbc = (long long)batch * seqlen * np;
-        const int g1 = (int)std::max<long long>(1, std::min<long long>((nbc + kReduceThreads - 1) / kReduceThreads, cap));
-        bwd_reduce_bc_kernel<<<g1, kReduceThreads, 0, stream>>>(a.pB, dB, groups, (int)batch,
-                                                                seqlen, (int)dstate, np);
-        bwd_reduce_bc_kernel<<<g1, kReduceThreads, 0, stream>>>(a.pC, dC, groups, (int)batch,
-                                                                seqlen, (int)dstate, np);
+        const int outs = groups >= 96 ? kReduceThreads / 4 : kReduceThreads;
+        const int g1 = (int)std::max<long long>(1, std::min<long long>((nbc + outs - 1) / outs, cap));
+        if (groups >= 96)
+            bwd_reduce_bc_kernel<4><<<dim3(g1, 2), kReduceThreads, 0, stream>>>(
+                a.pB, a.pC, dB, dC, groups, (int)batch, seqlen, (int)dstate, np);
+        else
+            bwd_reduce_bc_kernel<1><<<dim3(g1, 2), kReduceThreads, 0, stream>>>(
+                a.pB, a.pC, dB, dC, groups, (int)batch, seqlen, (int)dstate, np);
         const long long npar = dim * np;
         const int g2 = (int)std::max<long long>(1, std::min<long long>((npar + kReduceThreads - 1) / kReduceThreads, cap));
         bwd_reduce_params_kernel<<<g2, kReduceThreads, 0, stream>>>(

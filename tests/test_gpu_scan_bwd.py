@@ -4,7 +4,7 @@ reverse-mode gradient, through the C ABI.
 Every gradient (du, ddelta, dz, dA, dB, dC, dD_skip, ddt_bias, the initial
 state's) is compared element by element on the same seeded inputs: fp32 and
 bf16 I/O, dstate 4, 5 and 16, channel counts that leave a partial group of
-32, lengths that leave a partial 16-step tile, every nullable input absent
+32 (up to 97 groups), lengths that leave a partial 16-step tile, every nullable input absent
 or present, softplus on and off, an initial state and a final-state
 gradient.  Tolerances: fp32 I/O max |err| <= 1e-4 max(1, rms(ref)) (fp32
 accumulation over the sequence and the channels); bf16 I/O as the forward
@@ -84,6 +84,9 @@ SHAPES = [
     (synth.BF16, 2, 70, 16, 200),
     (synth.BF16, 1, 64, 8, 100),
     (synth.BF16, 2, 128, 16, 1024),
+    # 97 groups of 32 channels (the last partial): the dB / dC reduction
+    # splits its sum over groups into four parts from 96 groups on
+    (synth.BF16, 1, 3104, 16, 100),
 ]
 
 

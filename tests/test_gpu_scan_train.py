@@ -143,3 +143,28 @@ def test_train_pair_zero_length():
     torch.cuda.synchronize()
     assert ck.numel() == 0 and torch.equal(fin, h0)
     assert bool((g["dA"] == 0).all()) and torch.equal(g["d_initial_state"], dfin)
+
+
+@pytest.mark.slow
+def test_train_pair_bitwise_on_the_130m_layer():
+    """The Mamba-130M layer workload (B8 D1536 N16 L2048 bf16, 384 units of 32
+    channels, the backward's full wave): the training pair against the plain
+    calls, bit for bit, every output and gradient."""
+    import selective_state_space_135_b300 as mm
+    torch = torch_mod()
+    inp = synth.scan_inputs(synth.M130)
+    args = _dev(inp)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    dy = torch.randn(args[0].shape, device="cuda", generator=g).to(args[0].dtype)
+    dfin = torch.randn((8, 1536, 16), device="cuda", generator=g)
+    fin_t = torch.empty((8, 1536, 16), device="cuda")
+    fin = torch.empty_like(fin_t)
+    y_t, ck = mm.mamba_scan_fwd_train(*args, final_state=fin_t)
+    y = mm.mamba_scan_fwd(*args, final_state=fin)
+    g_ck = mm.mamba_scan_bwd_ckpt(*args, dy, ck, d_final_state=dfin, want_initial_state_grad=True)
+    g_pl = mm.mamba_scan_bwd(*args, dy, d_final_state=dfin, want_initial_state_grad=True)
+    torch.cuda.synchronize()
+    assert mm.mamba_device_status() == 0
+    assert torch.equal(y_t, y) and torch.equal(fin_t, fin)
+    for k, v in g_pl.items():
+        assert torch.equal(g_ck[k], v), k
