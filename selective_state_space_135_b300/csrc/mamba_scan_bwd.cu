@@ -405,12 +405,30 @@ bwd_kernel(const BwdArgs a) {
 #pragma unroll
         for (int j = 0; j < NPP; ++j)
             hn2[j] = nv > 0 ? hist2[((nv - 1) * NPP + j) * 32 + lane] : make_float2(0.0f, 0.0f);
+        // Software-pipelined by one step: the step's (u, Delta, g) and Abar
+        // are loaded and formed in the iteration before, so that the
+        // shared-load and ex2 latency at the head of a step overlaps the
+        // previous step's arithmetic and butterflies.
+        float uvn = 0.0f, dtn = 0.0f, gn = 0.0f;
+        float2 abn[NPP];
+        auto head = [&](int i) {
+            const float2 ud = srow[(2 * i) * 32 + lane];
+            uvn = ud.x;
+            dtn = ud.y;
+            gn = srow[(2 * i + 1) * 32 + lane].x;
+            const float2 dtl2 = make_float2(dtn * kLog2e, dtn * kLog2e);
+#pragma unroll
+            for (int j = 0; j < NPP; ++j) abn[j] = abar2_of<ACC>(dtn, dtl2, A2[j]);
+        };
+        head(nv > 0 ? nv - 1 : 0);
 #pragma unroll 1
         for (int i = nv - 1; i >= 0; --i) {
-            const float2 ud = srow[(2 * i) * 32 + lane];
-            const float uv = ud.x, dt = ud.y, g = srow[(2 * i + 1) * 32 + lane].x;
+            const float uv = uvn, dt = dtn, g = gn;
+            float2 ab2[NPP];
+#pragma unroll
+            for (int j = 0; j < NPP; ++j) ab2[j] = abn[j];
+            head(i > 0 ? i - 1 : 0);
             const float2 g2 = make_float2(g, g), dt2 = make_float2(dt, dt), uv2 = make_float2(uv, uv);
-            const float2 dtl2 = make_float2(dt * kLog2e, dt * kLog2e);
             float2 dus2 = make_float2(0.0f, 0.0f), dds2 = make_float2(0.0f, 0.0f);
             float pb[NPW], pc[NPW];
             // the states after step i - 1 (at i = 0 the checkpoint, hs2; the
@@ -424,7 +442,7 @@ bwd_kernel(const BwdArgs a) {
                 const float2 ht = hn2[j];
                 const float2 hp = i > 0 ? hprev[j * 32] : hs2[j];
                 hn2[j] = hp;
-                const float2 ab = abar2_of<ACC>(dt, dtl2, A2[j]);
+                const float2 ab = ab2[j];
                 dh2[j] = __ffma2_rn(g2, C2, dh2[j]);
                 const float2 pcv = __fmul2_rn(g2, ht);
                 const float2 dhd = __fmul2_rn(dh2[j], dt2);
