@@ -289,8 +289,9 @@ int mamba_scan_bwd(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen,
  *
  * mamba_scan_checkpoint_bytes: the size of the checkpoint buffer,
  *   batch * dim * ceil(seqlen / 12) * P * 4 bytes with P = dstate padded to
- *   4, 8 or 16 (fp32 states, [batch][ceil(seqlen / 12)][dim][P]); -1 for an
- *   invalid shape.  (For batch 4, dim 5120, dstate 16, seqlen 2048: 224 MB,
+ *   4, 8 or 16 (fp32 states, [batch][ceil(seqlen / 12)][P / 4][dim][4]:
+ *   entry n of channel d at ((k * P / 4 + n / 4) * dim + d) * 4 + n % 4 within
+ *   a batch entry); -1 for an invalid shape.  (For batch 4, dim 5120, dstate 16, seqlen 2048: 224 MB,
  *   2.7 times one bf16 (batch, dim, seqlen) tensor.)
  *
  * mamba_scan_fwd_train: y and final_state exactly as mamba_scan_fwd_ex with

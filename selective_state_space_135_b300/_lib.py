@@ -278,9 +278,10 @@ def mamba_scan_checkpoint_bytes(batch: int, dim: int, dstate: int, seqlen: int) 
 
 
 def checkpoint_shape(batch: int, dim: int, dstate: int, seqlen: int) -> tuple:
-    """(batch, ceil(seqlen / 12), dim, dstate padded to 4, 8 or 16), fp32."""
+    """(batch, ceil(seqlen / 12), P / 4, dim, 4) fp32 with P = dstate padded to
+    4, 8 or 16: entries in quads of four, channel-major within a quad."""
     pad = 4 if dstate <= 4 else (8 if dstate <= 8 else 16)
-    return (batch, (seqlen + 11) // 12, dim, pad)
+    return (batch, (seqlen + 11) // 12, pad // 4, dim, 4)
 
 
 def mamba_scan_fwd_train(u, delta, dt_bias, A, B, C, D_skip, z, softplus: bool = True,

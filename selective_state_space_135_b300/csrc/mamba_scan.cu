@@ -272,8 +272,8 @@ struct ScanArgs {
     float* ws_h;  // chunk end states, then carried-in states (same layout)
     const float* h0;       // initial state (batch, dim, N), or null for zero
     const int* seqlens;    // per batch entry: steps in use, or null for all
-    float* ckpt;           // checkpoint modes: [batch][ck_tiles][dim][NP], the state
-                           // before every step that is a multiple of kBwdTile
+    float* ckpt;           // checkpoint modes: [batch][ck_tiles][NP / 4][dim][4], the
+                           // state before every step that is a multiple of kBwdTile
     int ck_tiles;
     long long dim;
     long long seqlen;
@@ -720,30 +720,41 @@ scan_kernel(const __grid_constant__ ScanArgs a) {
     };
 
     // checkpoint modes: this warp's NT entries of the state before step
-    // `step` (a multiple of kBwdTile) into
-    // ckpt[((b * ck_tiles + step / kBwdTile) * dim + d) * NP + hh * NT]
-    // (adjacent channels adjacent, so a warp's stores share sectors).  The
-    // unit writes its checkpoints in step order: ck_at is the element index
-    // of the next one, advanced by dim * NP per write.  A unit from step 0
-    // writes checkpoint 0 (the initial state) first; a unit from t0 > 0
-    // writes those after its steps, from t0 / kBwdTile + 1 on (the one at
-    // t0 itself, if any, is the end state of the unit before it).
+    // `step` (a multiple of kBwdTile) into the quad-major layout
+    // ckpt[(((b * ck_tiles + step / kBwdTile) * NP / 4 + n / 4) * dim + d) * 4 + n % 4]
+    // (entries in quads of four, adjacent channels adjacent: a warp's store
+    // of a quad is 512 contiguous bytes).  The unit writes its checkpoints in
+    // step order: ck_at is the element index of the next one's first entry,
+    // advanced by NP * dim per write.  A unit from step 0 writes checkpoint 0
+    // (the initial state) first; a unit from t0 > 0 writes those after its
+    // steps, from t0 / kBwdTile + 1 on (the one at t0 itself, if any, is the
+    // end state of the unit before it).
     long long ck_at = 0;
     if constexpr (CKW) {
         const long long k0 = w.t0 == 0 ? 0 : w.t0 / kBwdTile + 1;
-        ck_at = (((long long)w.b * a.ck_tiles + k0) * dim + d) * NP + hh * NT;
+        const int n_first = hh * NT;
+        ck_at = ((((long long)w.b * a.ck_tiles + k0) * (NP / 4) + n_first / 4) * dim + d) * 4 +
+                n_first % 4;
     }
     auto write_ckpt = [&](long long step) {
         if (chan_ok && step < L_) {
             const long long ext = (long long)a.batch * dim * a.ck_tiles * NP;
             (void)ext;
-            if (MAMBA_IN(ck_at, ext) && MAMBA_IN(ck_at + NT - 1, ext)) {
-                float2* p2 = reinterpret_cast<float2*>(a.ckpt + ck_at);
+            if constexpr (NT >= 4) {   // whole quads: one 16-byte store each
 #pragma unroll
-                for (int i = 0; i < kNPair; ++i) p2[i] = h2[i];
+                for (int qd = 0; qd < NT / 4; ++qd) {
+                    const long long at = ck_at + (long long)qd * dim * 4;
+                    if (MAMBA_IN(at, ext) && MAMBA_IN(at + 3, ext))
+                        *reinterpret_cast<float4*>(a.ckpt + at) =
+                            make_float4(h2[2 * qd].x, h2[2 * qd].y, h2[2 * qd + 1].x,
+                                        h2[2 * qd + 1].y);
+                }
+            } else {   // one pair, half a quad
+                if (MAMBA_IN(ck_at, ext) && MAMBA_IN(ck_at + 1, ext))
+                    *reinterpret_cast<float2*>(a.ckpt + ck_at) = h2[0];
             }
         }
-        ck_at += dim * NP;
+        ck_at += (long long)NP * dim;
     };
     (void)write_ckpt;
     (void)ck_at;

@@ -50,7 +50,7 @@ struct BwdArgs {
     const float* D_skip;
     const float* h0;      // initial state or null
     const float* dfinal;  // dJ / d final state or null
-    float* ckpt;          // [batch][ntiles][dim][NP]: state before each tile
+    float* ckpt;          // [batch][ntiles][NP / 4][dim][4]: state before each tile
     void* du;
     void* ddelta;
     void* dz;
@@ -289,9 +289,11 @@ bwd_kernel(const BwdArgs a) {
     T* ddr = static_cast<T*>(a.ddelta) + q.row * L;
     T* dzr = HZ ? static_cast<T*>(a.dz) + q.row * L : nullptr;
     const float4* bcb = a.bc + (long long)q.b * L * (NP / 2);
-    // checkpoint of tile kk: pair j at ck[kk * dim * NP / 2 + j]
-    const float2* ck = reinterpret_cast<const float2*>(
-        a.ckpt + ((long long)q.b * a.ntiles * a.dim + q.d) * NP + n0);
+    // checkpoints (quad-major: entry n of tile kk at ((kk * NP / 4 + n / 4) *
+    // dim + d) * 4 + n % 4 from the batch entry's base): this lane's register
+    // pair j (entries n = n0 + 2 (j ^ pj) and n + 1) of tile kk is at
+    // ck + kk * NP * dim + (n / 4) * dim * 4 + n % 4
+    const float* ck = a.ckpt + (long long)q.b * a.ntiles * NP * a.dim + q.d * 4;
     // after the butterfly this lane holds the sums of entry n0 + le; the first
     // lane of each group that shares an entry stores them into the B/C row
     const int le = bwd_lane_entry<NPW>(lane);
@@ -327,8 +329,12 @@ bwd_kernel(const BwdArgs a) {
                          : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int j = 0; j < NPP; ++j)
-            ckr[j] = q.ok ? ck[(long long)kk * a.dim * (NP / 2) + (j ^ pj)] : make_float2(0.f, 0.f);
+        for (int j = 0; j < NPP; ++j) {
+            const int n = n0 + 2 * (j ^ pj);
+            ckr[j] = q.ok ? *reinterpret_cast<const float2*>(
+                                ck + ((long long)kk * NP + (n & ~3)) * a.dim + (n & 3))
+                          : make_float2(0.f, 0.f);
+        }
     };
     if (a.ntiles > 0) fetch(a.ntiles - 1);
 

@@ -202,10 +202,10 @@ int sm_count(int dev);
 int get_pool(int dev, cudaMemPool_t* out);
 // The forward scan in its checkpoint mode (mamba_scan.cu): the Euler scan
 // from initial_state (or zero) with no outputs, writing the state before
-// every step that is a multiple of kBwdTile into ckpt[((b * ck_tiles + k) *
-// dim + d) * np + n] (np = dstate padded to 4, 8 or 16; ck_tiles =
-// ceil(seqlen / kBwdTile)).  Scratch from the stream-ordered pool.  Returns
-// a status.
+// every step that is a multiple of kBwdTile into ckpt[(((b * ck_tiles + k) *
+// np / 4 + n / 4) * dim + d) * 4 + n % 4] (np = dstate padded to 4, 8 or
+// 16; ck_tiles = ceil(seqlen / kBwdTile)).  Scratch from the stream-ordered
+// pool.  Returns a status.
 int scan_checkpoints(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int io_dtype,
                      const void* u, const void* delta, const float* dt_bias, const float* A,
                      const void* B, const void* C, int softplus, const float* initial_state,

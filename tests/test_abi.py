@@ -5,6 +5,8 @@ the host before touching the device."""
 import os
 import re
 
+import numpy as np
+
 import pytest
 
 import selective_state_space_135_b300 as mm
@@ -317,7 +319,7 @@ def test_checkpoint_bytes(lib):
     assert lib.mamba_scan_checkpoint_bytes(0, 3, 4, 10) == -1
     for b, d, n, l in ((2, 16, 4, 64), (1, 3, 5, 12), (3, 7, 16, 25)):
         shp = _lib.checkpoint_shape(b, d, n, l)
-        assert lib.mamba_scan_checkpoint_bytes(b, d, n, l) == 4 * shp[0] * shp[1] * shp[2] * shp[3]
+        assert lib.mamba_scan_checkpoint_bytes(b, d, n, l) == 4 * int(np.prod(shp))
 
 
 def train_call(lib, flags=SOFTPLUS, extra=None, **over):

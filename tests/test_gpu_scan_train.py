@@ -90,7 +90,9 @@ def test_train_pair_matches_the_plain_calls(dtype, batch, dim, n, l, chunks, h0,
     # the checkpoints: shape, zero padding of the state, the initial state at
     # k = 0, the oracle's state after 12 k steps for a few later k
     assert tuple(ck.shape) == mm.checkpoint_shape(batch, dim, n, l)
-    c = ck.cpu().numpy().astype(np.float64)
+    # (batch, tile, quad, dim, 4) -> (batch, tile, dim, padded state)
+    c = ck.permute(0, 1, 3, 2, 4).reshape(batch, ck.shape[1], dim, -1).cpu().numpy()
+    c = c.astype(np.float64)
     assert np.all(c[..., n:] == 0.0)
     want0 = inp["h0"] if h0 else np.zeros((batch, dim, n), np.float32)
     assert np.array_equal(c[:, 0, :, :n], want0.astype(np.float64))
