@@ -427,26 +427,27 @@ bwd_kernel(const BwdArgs a) {
             for (int j = 0; j < NPP; ++j) abn[j] = abar2_of<ACC>(dtn, dtl2, A2[j]);
         };
         head(nv > 0 ? nv - 1 : 0);
-#pragma unroll 1
-        for (int i = nv - 1; i >= 0; --i) {
+        // One step of the walk; the last one (i = 0) is peeled off so that
+        // the loop's steps read h_{t-1} from the history without a select
+        // (at i = 0 it is the checkpoint, hs2) and prefetch without a clamp.
+        auto step = [&](int i, auto last) {
+            constexpr bool LAST = decltype(last)::value;
             const float uv = uvn, dt = dtn, g = gn;
             float2 ab2[NPP];
 #pragma unroll
             for (int j = 0; j < NPP; ++j) ab2[j] = abn[j];
-            head(i > 0 ? i - 1 : 0);
+            if constexpr (!LAST) head(i - 1);
             const float2 g2 = make_float2(g, g), dt2 = make_float2(dt, dt), uv2 = make_float2(uv, uv);
             float2 dus2 = make_float2(0.0f, 0.0f), dds2 = make_float2(0.0f, 0.0f);
             float pb[NPW], pc[NPW];
-            // the states after step i - 1 (at i = 0 the checkpoint, hs2; the
-            // row read is clamped so that every load stays in the history)
-            const float2* hprev = hist2 + ((i > 0 ? i - 1 : 0) * NPP) * 32 + lane;
+            const float2* hprev = hist2 + ((LAST ? 0 : i - 1) * NPP) * 32 + lane;
             const float4* brow = sbc + i * (NP / 2) + n0 / 2;
 #pragma unroll
             for (int j = 0; j < NPP; ++j) {
                 const float4 p = brow[j ^ pj];
                 const float2 B2 = make_float2(p.x, p.y), C2 = make_float2(p.z, p.w);
                 const float2 ht = hn2[j];
-                const float2 hp = i > 0 ? hprev[j * 32] : hs2[j];
+                const float2 hp = LAST ? hs2[j] : hprev[j * 32];
                 hn2[j] = hp;
                 const float2 ab = ab2[j];
                 dh2[j] = __ffma2_rn(g2, C2, dh2[j]);
@@ -470,7 +471,10 @@ bwd_kernel(const BwdArgs a) {
                 sum_at[i * NP * 2] = sb;
                 sum_at[i * NP * 2 + 2] = sc;
             }
-        }
+        };
+#pragma unroll 1
+        for (int i = nv - 1; i >= 1; --i) step(i, std::false_type{});
+        if (nv > 0) step(0, std::true_type{});
         __syncthreads();
         // (d) the tile's outputs, one lane per row: warp 0 du and ddelta,
         //     warp 1 dz; partial sums added in warp order.  The dB and dC
