@@ -1637,9 +1637,10 @@ int mamba_device_status(cudaStream_t stream) {
             return MAMBA_ERR_CUDA;
     }
     // the index checks of debug builds (always zero in release builds)
-    const int dbg_scan = take_debug_word(), dbg_conv = conv_take_debug_word();
-    if (dbg_scan < 0 || dbg_conv < 0) return MAMBA_ERR_CUDA;
-    const int dbg = dbg_scan ? dbg_scan : dbg_conv;
+    const int dbg_scan = take_debug_word(), dbg_conv = conv_take_debug_word(),
+              dbg_bwd = bwd_take_debug_word();
+    if (dbg_scan < 0 || dbg_conv < 0 || dbg_bwd < 0) return MAMBA_ERR_CUDA;
+    const int dbg = dbg_scan ? dbg_scan : (dbg_conv ? dbg_conv : dbg_bwd);
     if (dbg) g_debug_last_line.store(dbg & ~kDebugBoundsFlag);
     if (v) return MAMBA_ERR_TIMEOUT;
     if (dbg) return MAMBA_ERR_BOUNDS;

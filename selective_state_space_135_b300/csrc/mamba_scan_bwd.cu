@@ -69,10 +69,19 @@ struct BwdArgs {
 // boundary: 8-byte accesses for a full tile of an aligned row (the tile
 // start is 8-byte aligned: kBwdTile elements are 24 or 48 bytes), scalar
 // accesses otherwise.
+// (row_at, ext: the row's element offset in its tensor and the tensor's
+// extent, for the index checks of debug builds)
 template <typename T>
 __device__ __forceinline__ void load_tile_row(const T* row, long long t0, int nv, bool vec,
-                                              bool on, float (&v)[kBwdTile]) {
-    if (on && vec && nv == kBwdTile) {
+                                              bool on, float (&v)[kBwdTile], long long row_at,
+                                              long long ext) {
+    (void)row_at;
+    (void)ext;
+    if (on && vec && nv == kBwdTile &&
+        (!MAMBA_IN(row_at + t0, ext) || !MAMBA_IN(row_at + t0 + kBwdTile - 1, ext))) {
+#pragma unroll
+        for (int i = 0; i < kBwdTile; ++i) v[i] = 0.0f;
+    } else if (on && vec && nv == kBwdTile) {
         const uint2* p = reinterpret_cast<const uint2*>(row + t0);
         constexpr int kPer = 8 / (int)sizeof(T);
 #pragma unroll
@@ -90,13 +99,20 @@ __device__ __forceinline__ void load_tile_row(const T* row, long long t0, int nv
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < kBwdTile; ++i) v[i] = (on && i < nv) ? IO<T>::to_f(row[t0 + i]) : 0.0f;
+        for (int i = 0; i < kBwdTile; ++i)
+            v[i] = (on && i < nv && MAMBA_IN(row_at + t0 + i, ext)) ? IO<T>::to_f(row[t0 + i]) : 0.0f;
     }
 }
 template <typename T>
 __device__ __forceinline__ void store_tile_row(T* row, long long t0, int nv, bool vec,
-                                               const float (&v)[kBwdTile]) {
-    if (vec && nv == kBwdTile) {
+                                               const float (&v)[kBwdTile], long long row_at,
+                                               long long ext) {
+    (void)row_at;
+    (void)ext;
+    if (vec && nv == kBwdTile &&
+        (!MAMBA_IN(row_at + t0, ext) || !MAMBA_IN(row_at + t0 + kBwdTile - 1, ext))) {
+        return;
+    } else if (vec && nv == kBwdTile) {
         uint2* p = reinterpret_cast<uint2*>(row + t0);
         constexpr int kPer = 8 / (int)sizeof(T);
 #pragma unroll
@@ -116,7 +132,7 @@ __device__ __forceinline__ void store_tile_row(T* row, long long t0, int nv, boo
     } else {
 #pragma unroll
         for (int i = 0; i < kBwdTile; ++i)
-            if (i < nv) row[t0 + i] = IO<T>::from_f(v[i]);
+            if (i < nv && MAMBA_IN(row_at + t0 + i, ext)) row[t0 + i] = IO<T>::from_f(v[i]);
     }
 }
 
@@ -258,6 +274,15 @@ bwd_kernel(const BwdArgs a) {
     const WarpUnit q = warp_unit(a, blockIdx.x);
     const int lane = q.lane, N = a.N, n0 = warp * NPW;
     const long long L = a.L;
+    // extents for the index checks of debug builds
+    const long long rows = (long long)a.batch * a.dim;   // (b, d) rows
+    const long long big = rows * L;                      // u, delta, z, dy and their gradients
+    const long long pext = (long long)a.groups * a.batch * L * NP;
+    const long long ckext = (long long)a.batch * a.ntiles * NP * a.dim;
+    (void)rows;
+    (void)big;
+    (void)pext;
+    (void)ckext;
 
     // this warp's entries in pairs: A, dJ/dh, the dA partial sums, and the
     // state at the start of the current tile (from its checkpoint).  Register
@@ -271,15 +296,15 @@ bwd_kernel(const BwdArgs a) {
         for (int e = 0; e < 2; ++e) {
             const int n = n0 + 2 * (j ^ pj) + e;
             const bool on = q.ok && n < N;
-            av[e] = on ? a.A[q.d * N + n] : 0.0f;
-            dv[e] = (on && a.dfinal) ? a.dfinal[q.row * N + n] : 0.0f;
+            av[e] = on ? MAMBA_LD(a.A, q.d * N + n, a.dim * N) : 0.0f;
+            dv[e] = (on && a.dfinal) ? MAMBA_LD(a.dfinal, q.row * N + n, rows * N) : 0.0f;
         }
         A2[j] = make_float2(av[0], av[1]);
         dh2[j] = make_float2(dv[0], dv[1]);
         dA2[j] = make_float2(0.0f, 0.0f);
     }
-    const float bias = (q.ok && a.dt_bias) ? a.dt_bias[q.d] : 0.0f;
-    const float dsk = (q.ok && a.D_skip) ? a.D_skip[q.d] : 0.0f;
+    const float bias = (q.ok && a.dt_bias) ? MAMBA_LD(a.dt_bias, q.d, a.dim) : 0.0f;
+    const float dsk = (q.ok && a.D_skip) ? MAMBA_LD(a.D_skip, q.d, a.dim) : 0.0f;
     float dD = 0.0f, dbias = 0.0f;
     const T* ur = static_cast<const T*>(a.u) + q.row * L;
     const T* dl = static_cast<const T*>(a.delta) + q.row * L;
@@ -288,7 +313,6 @@ bwd_kernel(const BwdArgs a) {
     T* dur = static_cast<T*>(a.du) + q.row * L;
     T* ddr = static_cast<T*>(a.ddelta) + q.row * L;
     T* dzr = HZ ? static_cast<T*>(a.dz) + q.row * L : nullptr;
-    const float4* bcb = a.bc + (long long)q.b * L * (NP / 2);
     // checkpoints (quad-major: entry n of tile kk at ((kk * NP / 4 + n / 4) *
     // dim + d) * 4 + n % 4 from the batch entry's base): this lane's register
     // pair j (entries n = n0 + 2 (j ^ pj) and n + 1) of tile kk is at
@@ -314,26 +338,30 @@ bwd_kernel(const BwdArgs a) {
         const long long t0 = (long long)kk * kBwdTile;
         const int nv = (int)min((long long)kBwdTile, L - t0);
         if (warp == 0) {
-            load_tile_row<T>(ur, t0, nv, vec, q.ok, r1);
-            load_tile_row<T>(dl, t0, nv, vec, q.ok, r2);
+            load_tile_row<T>(ur, t0, nv, vec, q.ok, r1, q.row * L, big);
+            load_tile_row<T>(dl, t0, nv, vec, q.ok, r2, q.row * L, big);
         } else if (warp == 1) {
-            load_tile_row<T>(dyr, t0, nv, vec, q.ok, r1);
-            if constexpr (HZ) load_tile_row<T>(zr, t0, nv, vec, q.ok, r2);
+            load_tile_row<T>(dyr, t0, nv, vec, q.ok, r1, q.row * L, big);
+            if constexpr (HZ) load_tile_row<T>(zr, t0, nv, vec, q.ok, r2, q.row * L, big);
         }
 #pragma unroll
         for (int r = 0; r < kRowsPerThread; ++r) {
             const int e = r * 32 * SPL + threadIdx.x;
             const int i = e / (NP / 2);
             bcr[r] = (e < kBwdTile * (NP / 2) && i < nv)
-                         ? bcb[(t0 + i) * (NP / 2) + (e % (NP / 2))]
+                         ? MAMBA_LD(a.bc, (q.b * L + t0 + i) * (NP / 2) + (e % (NP / 2)),
+                                    (long long)a.batch * L * (NP / 2))
                          : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int j = 0; j < NPP; ++j) {
             const int n = n0 + 2 * (j ^ pj);
-            ckr[j] = q.ok ? *reinterpret_cast<const float2*>(
-                                ck + ((long long)kk * NP + (n & ~3)) * a.dim + (n & 3))
-                          : make_float2(0.f, 0.f);
+            const long long at = ((long long)kk * NP + (n & ~3)) * a.dim + (n & 3);
+            const long long at_all = (long long)q.b * a.ntiles * NP * a.dim + q.d * 4 + at;
+            (void)at_all;
+            ckr[j] = (q.ok && MAMBA_IN(at_all, ckext) && MAMBA_IN(at_all + 1, ckext))
+                         ? *reinterpret_cast<const float2*>(ck + at)
+                         : make_float2(0.f, 0.f);
         }
     };
     if (a.ntiles > 0) fetch(a.ntiles - 1);
@@ -499,8 +527,8 @@ bwd_kernel(const BwdArgs a) {
                 }
             }
             if (q.ok) {
-                store_tile_row<T>(dur, t0, nv, vec, o);
-                store_tile_row<T>(ddr, t0, nv, vec, od);
+                store_tile_row<T>(dur, t0, nv, vec, o, q.row * L, big);
+                store_tile_row<T>(ddr, t0, nv, vec, od, q.row * L, big);
             }
         } else if (HZ && warp == 1) {
             float o[kBwdTile];
@@ -511,7 +539,7 @@ bwd_kernel(const BwdArgs a) {
                 for (int w = 0; w < SPL; ++w) sy += party[(w * kBwdTile + i) * 32 + lane];
                 o[i] = szf[i * 32 + lane] * sy;   // dz = dy (C.h + D u) silu'(z)
             }
-            if (q.ok) store_tile_row<T>(dzr, t0, nv, vec, o);
+            if (q.ok) store_tile_row<T>(dzr, t0, nv, vec, o, q.row * L, big);
         }
         {
             constexpr int kQuads = NP / 4;   // 4-entry quads per step
@@ -520,8 +548,12 @@ bwd_kernel(const BwdArgs a) {
                 const float4 f0 = sbc[i * (NP / 2) + 2 * c];
                 const float4 f1 = sbc[i * (NP / 2) + 2 * c + 1];
                 const long long off = (t0 + i) * NP + 4 * c;
-                *reinterpret_cast<float4*>(pBg + off) = make_float4(f0.x, f0.y, f1.x, f1.y);
-                *reinterpret_cast<float4*>(pCg + off) = make_float4(f0.z, f0.w, f1.z, f1.w);
+                const long long at = ((long long)q.grp * a.batch + q.b) * L * NP + off;
+                (void)at;
+                if (MAMBA_IN(at, pext) && MAMBA_IN(at + 3, pext)) {
+                    *reinterpret_cast<float4*>(pBg + off) = make_float4(f0.x, f0.y, f1.x, f1.y);
+                    *reinterpret_cast<float4*>(pCg + off) = make_float4(f0.z, f0.w, f1.z, f1.w);
+                }
             }
         }
         __syncthreads();   // shared memory is rewritten by the next tile
@@ -532,13 +564,13 @@ bwd_kernel(const BwdArgs a) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int n = n0 + 2 * (j ^ pj) + e;
-                a.pA[q.row * NP + n] = e ? dA2[j].y : dA2[j].x;
-                if (a.dh0 && n < N) a.dh0[q.row * N + n] = e ? dh2[j].y : dh2[j].x;
+                MAMBA_ST(a.pA, q.row * NP + n, rows * NP, e ? dA2[j].y : dA2[j].x);
+                if (a.dh0 && n < N) MAMBA_ST(a.dh0, q.row * N + n, rows * N, e ? dh2[j].y : dh2[j].x);
             }
         }
         if (warp == 0) {
-            a.pD[q.row] = dD;
-            a.pbias[q.row] = dbias;
+            MAMBA_ST(a.pD, q.row, rows, dD);
+            MAMBA_ST(a.pbias, q.row, rows, dbias);
         }
     }
 }
@@ -568,7 +600,7 @@ bwd_reduce_bc_kernel(const float* __restrict__ pB, const float* __restrict__ pC,
         float s = 0.0f;
         if (i < total) {
 #pragma unroll 8
-            for (int g = g0; g < g1; ++g) s += part[g * total + i];
+            for (int g = g0; g < g1; ++g) s += MAMBA_LD(part, g * total + i, groups * total);
         }
         if constexpr (S > 1) {
             part_sum[q][o] = s;
@@ -584,7 +616,7 @@ bwd_reduce_bc_kernel(const float* __restrict__ pB, const float* __restrict__ pC,
             if (n < N) {
                 const long long bt = i / NP;   // b * L + t
                 const long long b = bt / L, t = bt - b * L;
-                out[(b * N + n) * L + t] = s;
+                MAMBA_ST(out, (b * N + n) * L + t, (long long)batch * N * L, s);
             }
         }
     }
@@ -603,17 +635,18 @@ bwd_reduce_params_kernel(const float* __restrict__ pA, const float* __restrict__
         const int n = (int)(i % NP);
         if (n < N) {
             float s = 0.0f;
-            for (int b = 0; b < batch; ++b) s += pA[((long long)b * dim + d) * NP + n];
-            dA[d * N + n] = s;
+            for (int b = 0; b < batch; ++b)
+                s += MAMBA_LD(pA, ((long long)b * dim + d) * NP + n, batch * dim * NP);
+            MAMBA_ST(dA, d * N + n, dim * N, s);
         }
         if (n == 0) {
             float sd = 0.0f, sb = 0.0f;
             for (int b = 0; b < batch; ++b) {
-                sd += pD[(long long)b * dim + d];
-                sb += pbias[(long long)b * dim + d];
+                sd += MAMBA_LD(pD, (long long)b * dim + d, batch * dim);
+                sb += MAMBA_LD(pbias, (long long)b * dim + d, batch * dim);
             }
-            if (dD) dD[d] = sd;
-            if (dbias) dbias[d] = sb;
+            if (dD) MAMBA_ST(dD, d, dim, sd);
+            if (dbias) MAMBA_ST(dbias, d, dim, sb);
         }
     }
 }
@@ -643,6 +676,10 @@ cudaError_t dispatch_bwd(int np, bool sp, bool hz, const BwdArgs& a, cudaStream_
 }
 
 }  // namespace
+
+// The debug word of this translation unit (the index checks of debug builds).
+int bwd_take_debug_word() { return take_debug_word(); }
+
 }  // namespace mamba
 
 using namespace mamba;

@@ -169,8 +169,10 @@ inline int padded_state(int64_t dstate) { return dstate <= 4 ? 4 : (dstate <= 8 
 // state checkpoints of a sequence: one before every kBwdTile steps
 inline int64_t checkpoint_tiles(int64_t seqlen) { return (seqlen + kBwdTile - 1) / kBwdTile; }
 
-// The debug word of the convolution's translation unit (mamba_conv.cu).
+// The debug words of the convolution's and the backward pass's translation
+// units (mamba_conv.cu, mamba_scan_bwd.cu).
 int conv_take_debug_word();
+int bwd_take_debug_word();
 
 inline bool aligned(const void* p, size_t a) {
     return (reinterpret_cast<uintptr_t>(p) % a) == 0;

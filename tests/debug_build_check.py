@@ -1,9 +1,10 @@
 """Run by tests/test_gpu_debug_build.py in a fresh process with
 MAMBA_SCAN_LIBRARY=debug: drives the library built with -DMAMBA_DEBUG
 (index checks on every global access) through the odd scan shapes, the
-generation step and the convolution, checks each against the fp64 oracle,
-and checks that no index check failed.  Also runs the index-check self-test,
-which must be reported as MAMBA_ERR_BOUNDS with its source line."""
+generation step, the convolution, the backward pass and the training pair,
+checks each against the fp64 oracle, and checks that no index check failed.
+Also runs the index-check self-test, which must be reported as
+MAMBA_ERR_BOUNDS with its source line."""
 
 import os
 import sys
@@ -86,6 +87,41 @@ def main():
         ref = oracle.conv1d(synth.widen(xb, synth.BF16), wt.cpu().numpy().astype(np.float64),
                             silu=True)[0]
         assert_close(to_f64(out), ref, synth.BF16)
+    # the backward pass (ragged tile, partial channel group, dstate 5 and 16,
+    # 97 channel groups for the four-part reduction) and the training pair
+    for dtype, batch, dim, n, l in ((synth.F32, 2, 33, 5, 70), (synth.BF16, 2, 70, 16, 200),
+                                    (synth.BF16, 1, 3104, 16, 40)):
+        shp = synth.ScanShape("debug bwd", batch, dim, n, l, dtype=dtype, seed=23)
+        inp = synth.scan_inputs(shp)
+        gg = np.random.default_rng(24)
+        dyh = synth.store(gg.standard_normal((batch, dim, l)).astype(np.float32), dtype)
+        h0 = (0.5 * gg.standard_normal((batch, dim, n))).astype(np.float32)
+        dfin = gg.standard_normal((batch, dim, n)).astype(np.float32)
+        args = (to_dev(inp["u"], dtype), to_dev(inp["delta"], dtype), f32_dev(inp["dt_bias"]),
+                f32_dev(inp["A"]), to_dev(inp["B"], dtype), to_dev(inp["C"], dtype),
+                f32_dev(inp["D_skip"]), to_dev(inp["z"], dtype))
+        dy = to_dev(dyh, dtype)
+        g1 = mm.mamba_scan_bwd(*args, dy, initial_state=f32_dev(h0), d_final_state=f32_dev(dfin),
+                               want_initial_state_grad=True)
+        _, ck = mm.mamba_scan_fwd_train(*args, initial_state=f32_dev(h0))
+        g2 = mm.mamba_scan_bwd_ckpt(*args, dy, ck, d_final_state=f32_dev(dfin),
+                                    want_initial_state_grad=True)
+        torch.cuda.synchronize()
+        assert mm.mamba_device_status() == 0, (dim, n, l, mm.mamba_debug_build())
+        for k, v in g1.items():
+            assert v is None or torch.equal(g2[k], v), k
+        w = oracle.scan_inputs_f64(inp)
+        ref = oracle.scan_bwd(w["u"], w["delta"], w["A"], w["B"], w["C"], synth.widen(dyh, dtype),
+                              dt_bias=w["dt_bias"], D_skip=w["D_skip"], z=w["z"], h0=h0,
+                              dfinal=dfin)
+        for gk, rk in (("du", "du"), ("dB", "dB"), ("dC", "dC"), ("dA", "dA"),
+                       ("d_initial_state", "dh0")):
+            got, want = to_f64(g1[gk]), ref[rk]
+            if dtype == synth.F32:
+                scale = max(1.0, float(np.sqrt(np.mean(want * want))))
+                assert np.max(np.abs(got - want)) <= 1e-4 * scale, gk
+            else:
+                assert_close(got, want, dtype, gk, bf16_output=gk == "du")
     # the self-test: a check one past the end is reported, with its line
     mm.mamba_selftest_bounds()
     assert mm.mamba_device_status() == BOUNDS

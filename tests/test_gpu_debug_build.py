@@ -1,12 +1,12 @@
 """The debug build (libmamba_scan_debug.so, compiled with -DMAMBA_DEBUG):
-every global load and store of the scan, generation-step, packing, carry
-and convolution kernels checks its index against its buffer's extent and,
+every global load and store of the scan, generation-step, packing, carry,
+convolution and backward kernels checks its index against its buffer's extent and,
 instead of faulting, skips the access and reports MAMBA_ERR_BOUNDS through
 mamba_device_status.  The check runs in a fresh process that loads the debug
 library (MAMBA_SCAN_LIBRARY=debug): the odd scan shapes of the parity tests
 (tensor-map and element-wise paths, ragged tails), a chunked plan, the
-extended modes, both generation-step kernels and the convolution must match
-the oracle with no failed check, and the index-check self-test must be
+extended modes, both generation-step kernels, the convolution, the backward
+pass and the training pair must match the oracle with no failed check, and the index-check self-test must be
 reported with its source line."""
 
 import os
