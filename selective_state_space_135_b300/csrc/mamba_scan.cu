@@ -1087,90 +1087,113 @@ state_update_kernel(const StepArgs a) {
 
 // Vectorised generation step for dstate == 16.  Two lanes per (b, d) row,
 // lane q holding state entries [8q, 8q + 8) as two float4.  A block covers
-// 32 channels x 4 batch entries, so the rows of one batch entry are
-// contiguous in memory (coalesced state access) and each A row is read by
-// four rows of the block (L1 hits).  B and C of a row's half are one 16-byte
-// (bf16) or two 16-byte (fp32) loads.  Fast path as in the scan: Delta is
-// kept in log2 units and Abar = ex2(Delta' * A).
-constexpr int kStepDims = 32, kStepBatches = 4;   // block = 32 x 4 rows x 2 lanes
+// 32 channels x 8 batch entries, two rows per thread (batch entries bi and
+// bi + 4 of the block): every load of both rows is issued before either is
+// computed, so each thread keeps 64 bytes of state in flight.  The rows of
+// one batch entry are contiguous in memory (coalesced state access) and a
+// thread reads its channel's A row once for both.  B and C of a row's half
+// are one 16-byte (bf16) or two 16-byte (fp32) loads.  Fast path as in the
+// scan: Delta is kept in log2 units and Abar = ex2(Delta' * A).
+constexpr int kStepDims = 32, kStepBatches = 4, kStepRows = 2;   // block = 32 x 4 x 2 lanes
 template <typename T, bool SP, bool ZOH>
-__global__ void __launch_bounds__(2 * kStepDims * kStepBatches)
+__global__ void __launch_bounds__(2 * kStepDims * kStepBatches, 3)
 state_update16_kernel(const StepArgs a) {
     constexpr bool ACC = IO<T>::kAccurate;
-    constexpr int N = 16, H = 8;
+    constexpr int N = 16, H = 8, R = kStepRows;
     const int tid = threadIdx.x;
     const int q = tid & 1;
     const int di = (tid >> 1) % kStepDims, bi = (tid >> 1) / kStepDims;
     const long long d = (long long)blockIdx.x * kStepDims + di;
-    const long long b = (long long)blockIdx.y * kStepBatches + bi;
     const long long batch = a.rows / a.dim;
-    const bool ok = d < a.dim && b < batch;
-    float acc = 0.0f, xv = 0.0f, zv = 0.0f, dsk = 0.0f;
     // extents for the index checks of debug builds
     const long long nrow = a.rows, nbn = batch * N, ndn = a.dim * N, nst = a.rows * N;
     (void)nrow; (void)nbn; (void)ndn; (void)nst;
-    // the 8-entry vector accesses of this lane's half of the row
-    const bool vok = !ok || (MAMBA_IN(b * N + H * q, nbn) && MAMBA_IN(b * N + H * q + H - 1, nbn) &&
-                             MAMBA_IN(d * N + H * q, ndn) && MAMBA_IN(d * N + H * q + H - 1, ndn) &&
-                             MAMBA_IN((b * a.dim + d) * N + H * q, nst) &&
-                             MAMBA_IN((b * a.dim + d) * N + H * q + H - 1, nst));
-    if (ok && vok) {
-        const long long row = b * a.dim + d;
-        xv = IO<T>::to_f(MAMBA_LD(static_cast<const T*>(a.x), row, nrow));
-        const float dv = IO<T>::to_f(MAMBA_LD(static_cast<const T*>(a.delta), row, nrow));
-        const float bias = a.dt_bias ? MAMBA_LD(a.dt_bias, d, a.dim) : 0.0f;
-        if (a.z) zv = IO<T>::to_f(MAMBA_LD(static_cast<const T*>(a.z), row, nrow));
-        dsk = a.D_skip ? MAMBA_LD(a.D_skip, d, a.dim) : 0.0f;
-        // Delta (log2 units on the fast path), Delta (natural units), Delta*u
-        float dt, dtn, du;
-        if constexpr (ACC) {
-            const float sarg = dv + bias;
-            dt = SP ? softplus_f<true>(sarg) : sarg;
-            dtn = dt;
-        } else {
-            const float tl = fmaf(dv, kLog2e, bias * kLog2e);
-            dt = SP ? softplus_log2_fast(tl) : tl;
-            dtn = dt * kLn2;
-        }
-        du = dtn * xv;
-        float Bv[H], Cv[H], Av[H];
-        const T* Bb = static_cast<const T*>(a.B) + b * N + H * q;
-        const T* Cb = static_cast<const T*>(a.C) + b * N + H * q;
-        if constexpr (sizeof(T) == 2) {
-            IO<T>::unpack(*reinterpret_cast<const uint4*>(Bb), Bv);
-            IO<T>::unpack(*reinterpret_cast<const uint4*>(Cb), Cv);
-        } else {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                IO<T>::unpack(reinterpret_cast<const uint4*>(Bb)[k], Bv + 4 * k);
-                IO<T>::unpack(reinterpret_cast<const uint4*>(Cb)[k], Cv + 4 * k);
-            }
-        }
+    const bool dok = d < a.dim && MAMBA_IN(d * N + H * q, ndn) && MAMBA_IN(d * N + H * q + H - 1, ndn);
+    float Av[H];
+    float bias = 0.0f, dsk = 0.0f;
+    if (dok) {
         const float4* Ad = reinterpret_cast<const float4*>(a.A + d * N + H * q);
-        float4* hp = reinterpret_cast<float4*>(a.state + row * N + H * q);
         const float4 a0 = Ad[0], a1 = Ad[1];
-        float4 h0 = hp[0], h1 = hp[1];
         Av[0] = a0.x; Av[1] = a0.y; Av[2] = a0.z; Av[3] = a0.w;
         Av[4] = a1.x; Av[5] = a1.y; Av[6] = a1.z; Av[7] = a1.w;
-        float hs[H] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-        float acc1 = 0.0f;
-#pragma unroll
-        for (int k = 0; k < H; ++k) {
-            const float dA = ACC ? expf(dt * Av[k]) : ex2_approx(dt * Av[k]);
-            const float bin = ZOH ? zoh_weight<ACC>(dA, dtn, Av[k]) * xv : du;
-            hs[k] = fmaf(dA, hs[k], bin * Bv[k]);
-            if (k & 1) acc1 = fmaf(Cv[k], hs[k], acc1);
-            else acc = fmaf(Cv[k], hs[k], acc);
-        }
-        acc += acc1;
-        hp[0] = make_float4(hs[0], hs[1], hs[2], hs[3]);
-        hp[1] = make_float4(hs[4], hs[5], hs[6], hs[7]);
+        bias = a.dt_bias ? MAMBA_LD(a.dt_bias, d, a.dim) : 0.0f;
+        dsk = a.D_skip ? MAMBA_LD(a.D_skip, d, a.dim) : 0.0f;
     }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    if (ok && q == 0) {
-        float o = acc + dsk * xv;
-        if (a.z) o *= silu_f<ACC>(zv);
-        MAMBA_ST(static_cast<T*>(a.y), b * a.dim + d, nrow, IO<T>::from_f(o));
+    // (1) every load of both rows
+    bool ok[R];
+    long long brow[R];
+    // B and C stay packed (bf16: one uint4 per half row) until the update
+    constexpr int kBC = sizeof(T) == 2 ? 1 : 2;
+    float xv[R], dv[R], zv[R], hs[R][H];
+    uint4 Braw[R][kBC], Craw[R][kBC];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const long long b = ((long long)blockIdx.y * R + r) * kStepBatches + bi;
+        brow[r] = b;
+        const long long row = b * a.dim + d;
+        ok[r] = dok && b < batch && MAMBA_IN(b * N + H * q, nbn) && MAMBA_IN(b * N + H * q + H - 1, nbn) &&
+                MAMBA_IN(row * N + H * q, nst) && MAMBA_IN(row * N + H * q + H - 1, nst);
+        xv[r] = dv[r] = zv[r] = 0.0f;
+        if (ok[r]) {
+            xv[r] = IO<T>::to_f(MAMBA_LD(static_cast<const T*>(a.x), row, nrow));
+            dv[r] = IO<T>::to_f(MAMBA_LD(static_cast<const T*>(a.delta), row, nrow));
+            if (a.z) zv[r] = IO<T>::to_f(MAMBA_LD(static_cast<const T*>(a.z), row, nrow));
+            const T* Bb = static_cast<const T*>(a.B) + b * N + H * q;
+            const T* Cb = static_cast<const T*>(a.C) + b * N + H * q;
+#pragma unroll
+            for (int k = 0; k < kBC; ++k) {
+                Braw[r][k] = reinterpret_cast<const uint4*>(Bb)[k];
+                Craw[r][k] = reinterpret_cast<const uint4*>(Cb)[k];
+            }
+            const float4* hp = reinterpret_cast<const float4*>(a.state + row * N + H * q);
+            const float4 h0 = hp[0], h1 = hp[1];
+            hs[r][0] = h0.x; hs[r][1] = h0.y; hs[r][2] = h0.z; hs[r][3] = h0.w;
+            hs[r][4] = h1.x; hs[r][5] = h1.y; hs[r][6] = h1.z; hs[r][7] = h1.w;
+        }
+    }
+    // (2) the update of both rows, the state stored in place, y
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        float acc = 0.0f;
+        if (ok[r]) {
+            // Delta (log2 units on the fast path), Delta (natural units), Delta*u
+            float dt, dtn;
+            if constexpr (ACC) {
+                const float sarg = dv[r] + bias;
+                dt = SP ? softplus_f<true>(sarg) : sarg;
+                dtn = dt;
+            } else {
+                const float tl = fmaf(dv[r], kLog2e, bias * kLog2e);
+                dt = SP ? softplus_log2_fast(tl) : tl;
+                dtn = dt * kLn2;
+            }
+            const float du = dtn * xv[r];
+            float Bv[H], Cv[H];
+#pragma unroll
+            for (int k = 0; k < kBC; ++k) {
+                IO<T>::unpack(Braw[r][k], Bv + (H / kBC) * k);
+                IO<T>::unpack(Craw[r][k], Cv + (H / kBC) * k);
+            }
+            float acc1 = 0.0f;
+#pragma unroll
+            for (int k = 0; k < H; ++k) {
+                const float dA = ACC ? expf(dt * Av[k]) : ex2_approx(dt * Av[k]);
+                const float bin = ZOH ? zoh_weight<ACC>(dA, dtn, Av[k]) * xv[r] : du;
+                hs[r][k] = fmaf(dA, hs[r][k], bin * Bv[k]);
+                if (k & 1) acc1 = fmaf(Cv[k], hs[r][k], acc1);
+                else acc = fmaf(Cv[k], hs[r][k], acc);
+            }
+            acc += acc1;
+            float4* hp = reinterpret_cast<float4*>(a.state + (brow[r] * a.dim + d) * N + H * q);
+            hp[0] = make_float4(hs[r][0], hs[r][1], hs[r][2], hs[r][3]);
+            hp[1] = make_float4(hs[r][4], hs[r][5], hs[r][6], hs[r][7]);
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        if (ok[r] && q == 0) {
+            float o = acc + dsk * xv[r];
+            if (a.z) o *= silu_f<ACC>(zv[r]);
+            MAMBA_ST(static_cast<T*>(a.y), brow[r] * a.dim + d, nrow, IO<T>::from_f(o));
+        }
     }
 }
 
@@ -1997,10 +2020,10 @@ static int state_update_common(int64_t batch, int64_t dim, int64_t dstate, int i
     const bool sp = (flags & MAMBA_FLAG_SOFTPLUS) != 0, zoh = (flags & MAMBA_FLAG_ZOH) != 0;
     // dstate 16 with 16-byte aligned rows: the vectorised two-lane kernel
     const bool vec16 = dstate == 16 && aligned(state, 16) && aligned(A, 16) && aligned(B, 16) &&
-                       aligned(C, 16) && batch <= 65535LL * kStepBatches;
+                       aligned(C, 16) && batch <= 65535LL * kStepBatches * kStepRows;
     if (vec16) {
         const dim3 grid((unsigned)((dim + kStepDims - 1) / kStepDims),
-                        (unsigned)((batch + kStepBatches - 1) / kStepBatches));
+                        (unsigned)((batch + kStepBatches * kStepRows - 1) / (kStepBatches * kStepRows)));
         ProfScope prof(kKindStep, stream);
         if (io_dtype == MAMBA_BF16)
             launch_step16<__nv_bfloat16>(sp, zoh, grid, 2 * kStepDims * kStepBatches, a, stream);
