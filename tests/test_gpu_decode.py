@@ -15,6 +15,8 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("dtype,batch,dim,n,zgate", [
     (synth.F32, 3, 37, 16, True), (synth.F32, 2, 5, 1, False), (synth.F32, 1, 64, 5, True),
     (synth.BF16, 4, 130, 16, True), (synth.BF16, 2, 33, 13, False), (synth.BF16, 1, 8, 4, True),
+    # dstate 16 over two blocks of 8 batch entries, the second with one
+    (synth.BF16, 9, 70, 16, True),
 ])
 def test_decode_small(dtype, batch, dim, n, zgate):
     torch = torch_mod()
