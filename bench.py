@@ -33,6 +33,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -203,6 +205,41 @@ def oracle_on_rows(inp, shape, rows):
     return time.perf_counter() - t0
 
 
+def oracle_on_channels(inp, chs, threads=None):
+    """Seconds the fp64 oracle, as it stands, takes to scan every batch entry
+    of the channels `chs` in one call (batch x len(chs) rows, which the
+    oracle spreads over its threads; inputs widened before the clock
+    starts), and the threads it used."""
+    import oracle
+    dt = inp["dtype"]
+    zs = inp.get("z")
+    u = synth.widen(inp["u"][:, chs], dt)
+    dl = synth.widen(inp["delta"][:, chs], dt)
+    z = None if zs is None else synth.widen(zs[:, chs], dt)
+    Bw, Cw = synth.widen(inp["B"], dt), synth.widen(inp["C"], dt)
+    A = np.asarray(inp["A"], np.float64)[chs]
+    dtb = np.asarray(inp["dt_bias"], np.float64)[chs]
+    dsk = np.asarray(inp["D_skip"], np.float64)[chs]
+    t0 = time.perf_counter()
+    _, _, used = oracle.scan(u, dl, A, Bw, Cw, dt_bias=dtb, D_skip=dsk, z=z, threads=threads)
+    return time.perf_counter() - t0, used
+
+
+def _sample_channels(shape, n, seed):
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(shape.dim, size=int(max(1, min(n, shape.dim))), replace=False))
+
+
+def _oracle_channels_for(inp, shape, seconds, seed, threads=None):
+    """Channels of `shape` (all batch entries each) the oracle scans in about
+    `seconds`."""
+    ncores = threads or os.cpu_count() or 1
+    k0 = max(2, 4 * -(-ncores // shape.batch))   # several rows for every thread
+    secs, _ = oracle_on_channels(inp, _sample_channels(shape, k0, seed), threads)
+    per_ch = max(secs, 1e-4) / k0
+    return int(max(1, min(shape.dim, seconds / per_ch)))
+
+
 def _oracle_rows_for(inp, shape, seconds, seed):
     """Rows of `shape` the oracle scans in about `seconds` on all host cores."""
     ncores = os.cpu_count() or 1
@@ -212,13 +249,40 @@ def _oracle_rows_for(inp, shape, seconds, seed):
 
 
 def oracle_rate(inp, shape, target_s):
-    """Time the fp64 oracle, as it stands, on a seeded sample of rows.
-    Returns (elems/s, threads, rows, seconds)."""
+    """Time the fp64 oracle, as it stands, on a seeded sample of rows: whole
+    channels (every batch entry) of an in-memory workload, sampled rows of a
+    row-wise one.  Returns (elems/s, threads, rows, seconds)."""
+    if inp is not None:
+        n_ch = _oracle_channels_for(inp, shape, target_s, 1234)
+        secs, used = oracle_on_channels(inp, _sample_channels(shape, n_ch, 1235))
+        nrows = shape.batch * n_ch
+        return nrows * shape.seqlen / secs, used, nrows, secs
     nrows = _oracle_rows_for(inp, shape, target_s, 1234)
     rows = synth.sample_rows(1235, shape.batch, shape.dim, nrows)
     secs = oracle_on_rows(inp, shape, rows)
     threads = min(os.cpu_count() or 1, len(rows))
     return len(rows) * shape.seqlen / secs, threads, len(rows), secs
+
+
+def oracle_single_core(seconds):
+    """The fp64 oracle, as it stands, on one host thread: a seeded sample of
+    full-length rows of the Mamba-130M layer workload (B8 D1536 N16 L2048),
+    about `seconds` of work.  Returns the cpu_baseline-style object."""
+    import oracle
+    shape = synth.M130
+    inp = synth.scan_inputs(shape)
+    probe = synth.sample_rows(77, shape.batch, shape.dim, 4)
+    t0 = time.perf_counter()
+    oracle.scan_rows(inp, probe, threads=1)
+    per_row = max(time.perf_counter() - t0, 1e-4) / len(probe)
+    n = int(max(1, min(shape.batch * shape.dim, seconds / per_row)))
+    rows = synth.sample_rows(78, shape.batch, shape.dim, n)
+    t0 = time.perf_counter()
+    oracle.scan_rows(inp, rows, threads=1)
+    secs = time.perf_counter() - t0
+    return {"value": n * shape.seqlen / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} seeded (b,d) rows of {shape.name}, full length {shape.seqlen}, "
+                      f"N={shape.dstate}; {secs:.1f} s on 1 thread"}
 
 
 def config_dict(shape, ws):
@@ -237,15 +301,28 @@ def run_reference(args, shape):
         return 0
     inp = None if shape.rowwise else synth.scan_inputs(shape)
     per_step = max(0.2, 150.0 / max(1, args.steps + args.warmup))
-    nrows = _oracle_rows_for(inp, shape, per_step, 99)
-    rows = synth.sample_rows(100, shape.batch, shape.dim, nrows)
-    for _ in range(args.warmup):
-        oracle_on_rows(inp, shape, rows)
-    secs = sum(oracle_on_rows(inp, shape, rows) for _ in range(args.steps))
+    if inp is not None:   # whole channels, every batch entry, in one oracle call
+        n_ch = _oracle_channels_for(inp, shape, per_step, 99)
+        chs = _sample_channels(shape, n_ch, 100)
+        for _ in range(args.warmup):
+            oracle_on_channels(inp, chs)
+        runs = [oracle_on_channels(inp, chs) for _ in range(args.steps)]
+        secs = sum(r[0] for r in runs)
+        threads = max(r[1] for r in runs)
+        nrows = shape.batch * n_ch
+        sample = (f"{nrows} (b,d) rows per step ({n_ch} seeded channels x all {shape.batch} "
+                  f"batch entries) of the {shape.name} workload, full length {shape.seqlen}, "
+                  f"N={shape.dstate}")
+    else:
+        nrows = _oracle_rows_for(inp, shape, per_step, 99)
+        rows = synth.sample_rows(100, shape.batch, shape.dim, nrows)
+        for _ in range(args.warmup):
+            oracle_on_rows(inp, shape, rows)
+        secs = sum(oracle_on_rows(inp, shape, rows) for _ in range(args.steps))
+        threads = min(os.cpu_count() or 1, nrows)
+        sample = (f"{nrows} seeded (b,d) rows of the {shape.name} workload per step, full "
+                  f"length {shape.seqlen}, N={shape.dstate}")
     value = nrows * shape.seqlen * args.steps / secs
-    threads = min(os.cpu_count() or 1, nrows)
-    sample = (f"{nrows} seeded (b,d) rows of the {shape.name} workload per step, full length "
-              f"{shape.seqlen}, N={shape.dstate}")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup,
@@ -457,8 +534,12 @@ def run_ours(args, shape):
         v, thr, nrows, secs = oracle_rate(inp, shape, args.cpu_seconds)
         line["cpu_baseline"] = {
             "value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
-            "sample": f"{nrows} seeded (b,d) rows of {shape.name}, full length {shape.seqlen}, "
-                      f"N={shape.dstate}; {secs:.1f} s on {thr} threads"}
+            "sample": (f"{nrows} (b,d) rows ({nrows // shape.batch} seeded channels x all "
+                       f"{shape.batch} batch entries) of {shape.name}, full length {shape.seqlen}, "
+                       f"N={shape.dstate}; {secs:.1f} s on {thr} threads") if inp is not None else
+                      (f"{nrows} seeded (b,d) rows of {shape.name}, full length {shape.seqlen}, "
+                       f"N={shape.dstate}; {secs:.1f} s on {thr} threads"),
+            "single_core_m130": oracle_single_core(args.cpu_seconds / 2)}
     if pg:
         pg.barrier()
         pg.destroy_process_group()
