@@ -245,7 +245,11 @@ int mamba_state_update_ex(int64_t batch, int64_t dim, int64_t dstate, mamba_dtyp
  * linear-time sequence modeling with selective state spaces", "What they
  * did": the fused scan recomputes the expanded state in the backward pass):
  * a checkpoint pass keeps the state every 12 steps in scratch memory, and a
- * reverse pass recomputes each 12-step tile from its checkpoint.
+ * reverse pass recomputes each 12-step tile from its checkpoint.  With few
+ * units of 32 channels (batch * ceil(dim / 32) at most a quarter of five per
+ * SM) the reverse pass is cut into time chunks: a summary pass gives each
+ * chunk's own contribution to dJ/dh and its decay, a carry pass composes
+ * them from the last chunk back, and every chunk then runs as its own CTA.
  *
  *   inputs as in mamba_scan_fwd_ex (u, delta, dt_bias, A, B, C, D_skip, z,
  *   initial_state), plus
@@ -451,7 +455,8 @@ int mamba_probe_pipe_rate(int kind, int warps_per_subpartition, int chains, int6
  * 0 = scan, 1 = chunk summary, 2 = chunk carry, 3 = state update,
  * 4 = B/C packing (one per scan or backward call), 5 = backward checkpoint
  * pass, 6 = backward reverse pass, 7 = backward reductions (one timing for
- * the three reduction launches of a call), 8 = causal convolution.
+ * the three reduction launches of a call), 8 = causal convolution, 9 =
+ * backward time-chunk summaries and their carry (one timing per call).
  * Either output may be NULL.  Not meant for use during stream capture.
  */
 int mamba_profile_begin(void);

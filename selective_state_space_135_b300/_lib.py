@@ -32,7 +32,7 @@ MAMBA_FLAG_ZOH = 2
 MAMBA_FLAG_NOALLOC = 4
 
 KIND_NAMES = ("scan", "chunk_summary", "chunk_carry", "state_update", "pack_bc",
-              "bwd_checkpoint", "bwd", "bwd_reduce", "conv1d")
+              "bwd_checkpoint", "bwd", "bwd_reduce", "conv1d", "bwd_summary")
 
 
 class MambaError(RuntimeError):

@@ -25,7 +25,12 @@
 //      partials (one per 32 channels) as whole 16-byte stores;
 //   3. reduction passes add the partials in a fixed order (deterministic
 //      results, no atomics): dB, dC over channel groups, dA, D_skip and
-//      dt_bias gradients over the batch.
+//      dt_bias gradients over the batch (and the time chunks).
+//
+// With few units of 32 channels the reverse pass runs in time chunks, each
+// chunk a CTA of its own, after a summary and a carry pass that give every
+// chunk the gradient entering it from the later ones (see
+// bwd_summary_kernel).
 
 #include "scan_common.cuh"
 
@@ -56,12 +61,17 @@ struct BwdArgs {
     void* dz;
     float* pB;            // [group][batch][L][NP]: dB summed over the group's 32 channels
     float* pC;
-    float* pA;            // [row][NP]
-    float* pD;            // [row]
-    float* pbias;         // [row]
+    float* pA;            // [chunk][row][NP]
+    float* pD;            // [chunk][row]
+    float* pbias;         // [chunk][row]
     float* dh0;           // [row][N] or null
+    // time chunks of the reverse pass (nchunks = 1: whole sequences)
+    float* dloc;          // [chunk][row][NP]: dJ/dh entering the chunk from its own steps
+    float* sdt;           // [chunk][row]: sum of Delta over the chunk
+    float* dcarry;        // [chunk][row][NP]: dJ/dh at the chunk's end, or null (nchunks = 1)
     long long dim, L;
     int batch, N, groups, ntiles;
+    int nchunks, chunk_tiles;   // tiles [c * chunk_tiles, (c + 1) * chunk_tiles) per chunk
     int vec8;   // every (batch, d) row of u, delta, z, dy, du, ddelta, dz is 8-byte aligned
 };
 
@@ -272,6 +282,9 @@ bwd_kernel(const BwdArgs a) {
     float2* partd = reinterpret_cast<float2*>(party + SPL * kBwdTile * 32);
     float4* sbc = reinterpret_cast<float4*>(partd + SPL * kBwdTile * 32);
     const WarpUnit q = warp_unit(a, blockIdx.x);
+    const int cidx = blockIdx.y;   // time chunk (0 with whole sequences)
+    const int k_lo = cidx * a.chunk_tiles;
+    const int k_hi = min(a.ntiles, k_lo + a.chunk_tiles) - 1;
     const int lane = q.lane, N = a.N, n0 = warp * NPW;
     const long long L = a.L;
     // extents for the index checks of debug builds
@@ -297,7 +310,12 @@ bwd_kernel(const BwdArgs a) {
             const int n = n0 + 2 * (j ^ pj) + e;
             const bool on = q.ok && n < N;
             av[e] = on ? MAMBA_LD(a.A, q.d * N + n, a.dim * N) : 0.0f;
-            dv[e] = (on && a.dfinal) ? MAMBA_LD(a.dfinal, q.row * N + n, rows * N) : 0.0f;
+            if (a.dcarry)   // the gradient entering this chunk from the later ones
+                dv[e] = on ? MAMBA_LD(a.dcarry, ((long long)cidx * rows + q.row) * NP + n,
+                                      (long long)a.nchunks * rows * NP)
+                           : 0.0f;
+            else
+                dv[e] = (on && a.dfinal) ? MAMBA_LD(a.dfinal, q.row * N + n, rows * N) : 0.0f;
         }
         A2[j] = make_float2(av[0], av[1]);
         dh2[j] = make_float2(dv[0], dv[1]);
@@ -364,9 +382,9 @@ bwd_kernel(const BwdArgs a) {
                          : make_float2(0.f, 0.f);
         }
     };
-    if (a.ntiles > 0) fetch(a.ntiles - 1);
+    if (k_hi >= k_lo) fetch(k_hi);
 
-    for (int k = a.ntiles - 1; k >= 0; --k) {
+    for (int k = k_hi; k >= k_lo; --k) {
         const long long t0 = (long long)k * kBwdTile;
         const int nv = (int)min((long long)kBwdTile, L - t0);
         // (a) the tile's per-step inputs, B/C rows and checkpoint from the
@@ -402,7 +420,7 @@ bwd_kernel(const BwdArgs a) {
         }
 #pragma unroll
         for (int j = 0; j < NPP; ++j) hs2[j] = ckr[j];
-        if (k > 0) fetch(k - 1);
+        if (k > k_lo) fetch(k - 1);
         __syncthreads();
         // (b) recompute this warp's states and its part of C.h (+ D u), two
         //     entries at a time with packed arithmetic
@@ -564,13 +582,15 @@ bwd_kernel(const BwdArgs a) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int n = n0 + 2 * (j ^ pj) + e;
-                MAMBA_ST(a.pA, q.row * NP + n, rows * NP, e ? dA2[j].y : dA2[j].x);
-                if (a.dh0 && n < N) MAMBA_ST(a.dh0, q.row * N + n, rows * N, e ? dh2[j].y : dh2[j].x);
+                MAMBA_ST(a.pA, ((long long)cidx * rows + q.row) * NP + n,
+                         (long long)a.nchunks * rows * NP, e ? dA2[j].y : dA2[j].x);
+                if (a.dh0 && n < N && cidx == 0)
+                    MAMBA_ST(a.dh0, q.row * N + n, rows * N, e ? dh2[j].y : dh2[j].x);
             }
         }
         if (warp == 0) {
-            MAMBA_ST(a.pD, q.row, rows, dD);
-            MAMBA_ST(a.pbias, q.row, rows, dbias);
+            MAMBA_ST(a.pD, (long long)cidx * rows + q.row, (long long)a.nchunks * rows, dD);
+            MAMBA_ST(a.pbias, (long long)cidx * rows + q.row, (long long)a.nchunks * rows, dbias);
         }
     }
 }
@@ -651,6 +671,102 @@ bwd_reduce_params_kernel(const float* __restrict__ pA, const float* __restrict__
     }
 }
 
+// Time chunks of the reverse pass.  When the units of 32 channels are too
+// few to fill the GPU, every unit's tiles are cut into chunks that run as
+// separate CTAs.  A chunk's reverse walk needs dJ/dh at its end, which its
+// later chunks send back; the recurrence of dh is linear, so, with
+// dloc_c = what chunk c's own steps send into the state before it (walking
+// them last to first from dh = 0: dh += g_t C_t, then dh *= Abar_t) and
+// P_c = exp(A * (sum of Delta over chunk c)), the gradient at the end of
+// chunk c - 1 is dloc_c + P_c * (the gradient at the end of chunk c), from
+// d_final_state at the end of the last chunk.
+
+// dloc_c and the chunk's sum of Delta, for chunks 1 .. nchunks - 1: one lane
+// per channel with all of its entries; grid (units, nchunks - 1).
+template <typename T, int NP, bool SP, bool HZ>
+__global__ void __launch_bounds__(32)
+bwd_summary_kernel(const BwdArgs a) {
+    constexpr bool ACC = IO<T>::kAccurate;
+    const WarpUnit q = warp_unit(a, blockIdx.x);
+    const int cidx = blockIdx.y + 1;
+    const int N = a.N;
+    const long long L = a.L;
+    const long long rows = (long long)a.batch * a.dim, big = rows * L;
+    (void)big;
+    float Av[NP], dh[NP];
+#pragma unroll
+    for (int n = 0; n < NP; ++n) {
+        Av[n] = (q.ok && n < N) ? MAMBA_LD(a.A, q.d * N + n, a.dim * N) : 0.0f;
+        dh[n] = 0.0f;
+    }
+    const float bias = (q.ok && a.dt_bias) ? MAMBA_LD(a.dt_bias, q.d, a.dim) : 0.0f;
+    const T* dl = static_cast<const T*>(a.delta) + q.row * L;
+    const T* dyr = static_cast<const T*>(a.dy) + q.row * L;
+    const T* zr = HZ ? static_cast<const T*>(a.z) + q.row * L : nullptr;
+    const bool vec = a.vec8 != 0;
+    const int k_lo = cidx * a.chunk_tiles;
+    const int k_hi = min(a.ntiles, k_lo + a.chunk_tiles) - 1;
+    float sdt = 0.0f;
+    for (int k = k_hi; k >= k_lo; --k) {
+        const long long t0 = (long long)k * kBwdTile;
+        const int nv = (int)min((long long)kBwdTile, L - t0);
+        float rd[kBwdTile], ry[kBwdTile], rz[kBwdTile];
+        load_tile_row<T>(dl, t0, nv, vec, q.ok, rd, q.row * L, big);
+        load_tile_row<T>(dyr, t0, nv, vec, q.ok, ry, q.row * L, big);
+        if constexpr (HZ) load_tile_row<T>(zr, t0, nv, vec, q.ok, rz, q.row * L, big);
+#pragma unroll
+        for (int i = kBwdTile - 1; i >= 0; --i) {
+            if (i >= nv) continue;
+            const float dt = q.ok ? delta_nat<ACC, SP>(rd[i] + bias) : 0.0f;
+            float g = ry[i];
+            if constexpr (HZ) g = g * rz[i] * sigmoid_f<ACC>(rz[i]);
+            sdt += dt;
+            const long long crow = ((long long)q.b * L + t0 + i) * (NP / 2);
+            const float dtl = dt * kLog2e;
+#pragma unroll
+            for (int j = 0; j < NP / 2; ++j) {
+                const float4 p = MAMBA_LD(a.bc, crow + j, (long long)a.batch * L * (NP / 2));
+                dh[2 * j] = fmaf(g, p.z, dh[2 * j]);
+                dh[2 * j + 1] = fmaf(g, p.w, dh[2 * j + 1]);
+            }
+#pragma unroll
+            for (int n = 0; n < NP; ++n)
+                dh[n] *= ACC ? expf(dt * Av[n]) : ex2_approx(dtl * Av[n]);
+        }
+    }
+    if (q.ok) {
+        const long long at = (long long)cidx * rows + q.row;
+#pragma unroll
+        for (int n = 0; n < NP; ++n)
+            MAMBA_ST(a.dloc, at * NP + n, (long long)a.nchunks * rows * NP, dh[n]);
+        MAMBA_ST(a.sdt, at, (long long)a.nchunks * rows, sdt);
+    }
+}
+
+// dJ/dh at the end of every chunk, last chunk first; one thread per (row, n).
+__global__ void __launch_bounds__(kReduceThreads)
+bwd_chunk_carry_kernel(const BwdArgs a, int NP) {
+    const long long rows = (long long)a.batch * a.dim;
+    const long long i = (long long)blockIdx.x * kReduceThreads + threadIdx.x;
+    if (i >= rows * NP) return;
+    const long long row = i / NP, d = row % a.dim;
+    const int n = (int)(i % NP);
+    const bool on = n < a.N;
+    const long long ext = (long long)a.nchunks * rows * NP;
+    (void)ext;
+    float carry = (on && a.dfinal) ? MAMBA_LD(a.dfinal, row * a.N + n, rows * a.N) : 0.0f;
+    const float An = on ? MAMBA_LD(a.A, d * a.N + n, a.dim * a.N) : 0.0f;
+    for (int c = a.nchunks - 1; c >= 0; --c) {
+        const long long at = ((long long)c * rows + row) * NP + n;
+        MAMBA_ST(a.dcarry, at, ext, carry);
+        if (c > 0) {
+            const float P = expf(An * MAMBA_LD(a.sdt, (long long)c * rows + row,
+                                               (long long)a.nchunks * rows));
+            carry = fmaf(P, carry, MAMBA_LD(a.dloc, at, ext));
+        }
+    }
+}
+
 template <typename T, int NP, bool SP>
 cudaError_t launch_bwd(const BwdArgs& a, bool hz, cudaStream_t st) {
     const long long units = (long long)a.batch * a.groups;
@@ -659,9 +775,17 @@ cudaError_t launch_bwd(const BwdArgs& a, bool hz, cudaStream_t st) {
     auto k = hz ? bwd_kernel<T, NP, SP, true> : bwd_kernel<T, NP, SP, false>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    if (a.nchunks > 1) {
+        ProfScope prof(kKindBwdSummary, st);
+        auto ks = hz ? bwd_summary_kernel<T, NP, SP, true> : bwd_summary_kernel<T, NP, SP, false>;
+        ks<<<dim3((unsigned)units, (unsigned)(a.nchunks - 1)), 32, 0, st>>>(a);
+        const long long n = (long long)a.batch * a.dim * NP;
+        bwd_chunk_carry_kernel<<<(unsigned)((n + kReduceThreads - 1) / kReduceThreads),
+                                 kReduceThreads, 0, st>>>(a, NP);
+    }
     {
         ProfScope prof(kKindBwd, st);
-        k<<<(unsigned)units, 32 * bwd_split<NP>(), smem, st>>>(a);
+        k<<<dim3((unsigned)units, (unsigned)a.nchunks), 32 * bwd_split<NP>(), smem, st>>>(a);
     }
     return cudaGetLastError();
 }
@@ -753,14 +877,33 @@ int bwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int i
     const int np = padded_state(dstate);
     const int groups = (int)((dim + 31) / 32);
     const int ntiles = (int)checkpoint_tiles(seqlen);
+    // time chunks when the units of 32 channels fill at most a quarter of
+    // the reverse pass's CTA slots (five per SM): as many as fill them, of at
+    // least four tiles each.  (Measured on B300: b1 d1536 n16, 48 units,
+    // L = 262144: 118.6 -> 25.1 ms; b2 d5120, 320 units, L = 8192, in two
+    // chunks: 4.85 -> 5.52 ms, the summary pass costing more than the
+    // doubled occupancy gains.)
+    const long long units = batch * groups;
+    const long long slots = 5LL * sm_count(dev);
+    int nchunks = 1, chunk_tiles = ntiles;
+    if (units * 4 <= slots && ntiles >= 16) {
+        const long long want = std::min<long long>(slots / units, ntiles / 4);
+        if (want >= 4) {
+            chunk_tiles = (int)((ntiles + want - 1) / want);
+            nchunks = (ntiles + chunk_tiles - 1) / chunk_tiles;
+        }
+    }
     const size_t rows = (size_t)(batch * dim);
     const size_t sz_bc = (size_t)batch * seqlen * (np / 2) * sizeof(float4);
     const size_t sz_ck = ckpt_in ? 0 : rows * ntiles * np * sizeof(float);
     const size_t sz_p = (size_t)groups * batch * seqlen * np * sizeof(float);
-    const size_t sz_a = rows * np * sizeof(float);
-    const size_t sz_r = rows * sizeof(float);
+    const size_t sz_a = (size_t)nchunks * rows * np * sizeof(float);
+    const size_t sz_r = (size_t)nchunks * rows * sizeof(float);
+    const size_t sz_c = nchunks > 1 ? sz_a : 0;   // dloc and dcarry, each
+    const size_t sz_s = nchunks > 1 ? sz_r : 0;   // sdt
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-    const size_t total = up(sz_bc) + up(sz_ck) + 2 * up(sz_p) + up(sz_a) + 2 * up(sz_r);
+    const size_t total = up(sz_bc) + up(sz_ck) + 2 * up(sz_p) + up(sz_a) + 2 * up(sz_r) +
+                         2 * up(sz_c) + up(sz_s);
     cudaMemPool_t pool = nullptr;
     int rc = get_pool(dev, &pool);
     if (rc != MAMBA_OK) return rc;
@@ -779,7 +922,14 @@ int bwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int i
     a.pC = reinterpret_cast<float*>(p); p += up(sz_p);
     a.pA = reinterpret_cast<float*>(p); p += up(sz_a);
     a.pD = reinterpret_cast<float*>(p); p += up(sz_r);
-    a.pbias = reinterpret_cast<float*>(p);
+    a.pbias = reinterpret_cast<float*>(p); p += up(sz_r);
+    if (nchunks > 1) {
+        a.dloc = reinterpret_cast<float*>(p); p += up(sz_c);
+        a.dcarry = reinterpret_cast<float*>(p); p += up(sz_c);
+        a.sdt = reinterpret_cast<float*>(p);
+    }
+    a.nchunks = nchunks;
+    a.chunk_tiles = chunk_tiles;
     a.u = u; a.delta = delta; a.z = z; a.dy = dy;
     a.dt_bias = dt_bias; a.A = A; a.D_skip = D_skip;
     a.h0 = initial_state; a.dfinal = d_final_state;
@@ -820,8 +970,10 @@ int bwd_common(int64_t batch, int64_t dim, int64_t dstate, int64_t seqlen, int i
                 a.pB, a.pC, dB, dC, groups, (int)batch, seqlen, (int)dstate, np);
         const long long npar = dim * np;
         const int g2 = (int)std::max<long long>(1, std::min<long long>((npar + kReduceThreads - 1) / kReduceThreads, cap));
+        // partials of every (chunk, batch entry), added in that order
         bwd_reduce_params_kernel<<<g2, kReduceThreads, 0, stream>>>(
-            a.pA, a.pD, a.pbias, dA, dD_skip, ddt_bias, (int)batch, dim, (int)dstate, np);
+            a.pA, a.pD, a.pbias, dA, dD_skip, ddt_bias, (int)(batch * nchunks), dim, (int)dstate,
+            np);
         e = cudaGetLastError();
     }
     cudaFreeAsync(scratch, stream);

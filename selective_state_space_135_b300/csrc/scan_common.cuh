@@ -187,7 +187,8 @@ inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 // Kinds of launch timed by mamba_profile_begin/end.
 enum LaunchKind {
     kKindScan = 0, kKindSummary = 1, kKindCarry = 2, kKindStep = 3, kKindPack = 4,
-    kKindBwdCheckpoint = 5, kKindBwd = 6, kKindBwdReduce = 7, kKindConv = 8, kKinds = 9
+    kKindBwdCheckpoint = 5, kKindBwd = 6, kKindBwdReduce = 7, kKindConv = 8,
+    kKindBwdSummary = 9, kKinds = 10
 };
 
 // While timing is on, brackets the launches of its scope with CUDA events

@@ -4,11 +4,14 @@ reverse-mode gradient, through the C ABI.
 Every gradient (du, ddelta, dz, dA, dB, dC, dD_skip, ddt_bias, the initial
 state's) is compared element by element on the same seeded inputs: fp32 and
 bf16 I/O, dstate 4, 5 and 16, channel counts that leave a partial group of
-32 (up to 97 groups), lengths that leave a partial 16-step tile, every nullable input absent
-or present, softplus on and off, an initial state and a final-state
-gradient.  Tolerances: fp32 I/O max |err| <= 1e-4 max(1, rms(ref)) (fp32
-accumulation over the sequence and the channels); bf16 I/O as the forward
-(2e-2 of the reference rms, bf16-stored outputs beyond their own rounding).
+32 (up to 97 groups), lengths that leave a partial 12-step tile, every
+nullable input absent or present, softplus on and off, an initial state and
+a final-state gradient.  Most of these shapes have few units of 32 channels,
+so the reverse pass runs in time chunks (from 4 up to 67 of them) with the
+chunk summaries and their carry.  Tolerances: fp32 I/O max |err| <= 1e-4
+max(1, rms(ref)) (fp32 accumulation over the sequence and the channels);
+bf16 I/O as the forward (2e-2 of the reference rms, bf16-stored outputs
+beyond their own rounding).
 """
 
 import numpy as np
@@ -87,6 +90,11 @@ SHAPES = [
     # 97 groups of 32 channels (the last partial): the dB / dC reduction
     # splits its sum over groups into four parts from 96 groups on
     (synth.BF16, 1, 3104, 16, 100),
+    # two units over 4000 steps: the reverse pass in 67 time chunks of five
+    # tiles, with the chunk summaries and the carry between them; the same
+    # in fp32 over 10 chunks
+    (synth.BF16, 1, 64, 16, 4000),
+    (synth.F32, 1, 48, 16, 500),
 ]
 
 
