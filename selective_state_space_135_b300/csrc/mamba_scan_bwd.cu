@@ -682,22 +682,38 @@ bwd_reduce_params_kernel(const float* __restrict__ pA, const float* __restrict__
 // d_final_state at the end of the last chunk.
 
 // dloc_c and the chunk's sum of Delta, for chunks 1 .. nchunks - 1: one lane
-// per channel with all of its entries; grid (units, nchunks - 1).
+// per channel; the NP entries split over NP / 4 warps of four entries each;
+// grid (units, nchunks - 1).  Per 12-step tile, last to first, as in the
+// reverse pass: the tile's Delta and g = dy silu(z) (warp 0, then shared)
+// and its packed B/C rows are staged in shared memory, with the next tile's
+// global loads issued before the walk.
+template <int NP>
+__host__ __device__ constexpr int bwd_summary_warps() {
+    return NP >= 8 ? NP / 4 : 1;
+}
 template <typename T, int NP, bool SP, bool HZ>
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(32 * bwd_summary_warps<NP>())
 bwd_summary_kernel(const BwdArgs a) {
     constexpr bool ACC = IO<T>::kAccurate;
+    constexpr int SW = bwd_summary_warps<NP>();
+    constexpr int NW = NP / SW;   // entries per warp: 4
+    constexpr int kRowsPerThread = (kBwdTile * (NP / 2) + 32 * SW - 1) / (32 * SW);
+    __shared__ float2 sdg[kBwdTile][32];           // (Delta, g) per step and lane
+    __shared__ float4 sbc[kBwdTile * (NP / 2)];    // the tile's packed B/C rows
+    const int warp = threadIdx.x >> 5;
     const WarpUnit q = warp_unit(a, blockIdx.x);
+    const int lane = q.lane;
     const int cidx = blockIdx.y + 1;
-    const int N = a.N;
+    const int N = a.N, n0 = warp * NW;
     const long long L = a.L;
     const long long rows = (long long)a.batch * a.dim, big = rows * L;
     (void)big;
-    float Av[NP], dh[NP];
+    float Av[NW], dh[NW];
 #pragma unroll
-    for (int n = 0; n < NP; ++n) {
-        Av[n] = (q.ok && n < N) ? MAMBA_LD(a.A, q.d * N + n, a.dim * N) : 0.0f;
-        dh[n] = 0.0f;
+    for (int j = 0; j < NW; ++j) {
+        const int n = n0 + j;
+        Av[j] = (q.ok && n < N) ? MAMBA_LD(a.A, q.d * N + n, a.dim * N) : 0.0f;
+        dh[j] = 0.0f;
     }
     const float bias = (q.ok && a.dt_bias) ? MAMBA_LD(a.dt_bias, q.d, a.dim) : 0.0f;
     const T* dl = static_cast<const T*>(a.delta) + q.row * L;
@@ -706,40 +722,71 @@ bwd_summary_kernel(const BwdArgs a) {
     const bool vec = a.vec8 != 0;
     const int k_lo = cidx * a.chunk_tiles;
     const int k_hi = min(a.ntiles, k_lo + a.chunk_tiles) - 1;
+    float rd[kBwdTile], ry[kBwdTile], rz[kBwdTile];
+    float4 bcr[kRowsPerThread];
+    auto fetch = [&](int kk) {
+        const long long t0 = (long long)kk * kBwdTile;
+        const int nv = (int)min((long long)kBwdTile, L - t0);
+        if (warp == 0) {
+            load_tile_row<T>(dl, t0, nv, vec, q.ok, rd, q.row * L, big);
+            load_tile_row<T>(dyr, t0, nv, vec, q.ok, ry, q.row * L, big);
+            if constexpr (HZ) load_tile_row<T>(zr, t0, nv, vec, q.ok, rz, q.row * L, big);
+        }
+#pragma unroll
+        for (int r = 0; r < kRowsPerThread; ++r) {
+            const int e = r * 32 * SW + threadIdx.x;
+            const int i = e / (NP / 2);
+            bcr[r] = (e < kBwdTile * (NP / 2) && i < nv)
+                         ? MAMBA_LD(a.bc, (q.b * L + t0 + i) * (NP / 2) + (e % (NP / 2)),
+                                    (long long)a.batch * L * (NP / 2))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
     float sdt = 0.0f;
+    if (k_hi >= k_lo) fetch(k_hi);
     for (int k = k_hi; k >= k_lo; --k) {
         const long long t0 = (long long)k * kBwdTile;
         const int nv = (int)min((long long)kBwdTile, L - t0);
-        float rd[kBwdTile], ry[kBwdTile], rz[kBwdTile];
-        load_tile_row<T>(dl, t0, nv, vec, q.ok, rd, q.row * L, big);
-        load_tile_row<T>(dyr, t0, nv, vec, q.ok, ry, q.row * L, big);
-        if constexpr (HZ) load_tile_row<T>(zr, t0, nv, vec, q.ok, rz, q.row * L, big);
+        if (warp == 0) {
+#pragma unroll
+            for (int i = 0; i < kBwdTile; ++i) {
+                const float dt = (q.ok && i < nv) ? delta_nat<ACC, SP>(rd[i] + bias) : 0.0f;
+                float g = ry[i];
+                if constexpr (HZ) g = g * rz[i] * sigmoid_f<ACC>(rz[i]);
+                sdt += dt;
+                sdg[i][lane] = make_float2(dt, g);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kRowsPerThread; ++r) {
+            const int e = r * 32 * SW + threadIdx.x;
+            if (e < kBwdTile * (NP / 2)) sbc[e] = bcr[r];
+        }
+        if (k > k_lo) fetch(k - 1);
+        __syncthreads();
 #pragma unroll
         for (int i = kBwdTile - 1; i >= 0; --i) {
             if (i >= nv) continue;
-            const float dt = q.ok ? delta_nat<ACC, SP>(rd[i] + bias) : 0.0f;
-            float g = ry[i];
-            if constexpr (HZ) g = g * rz[i] * sigmoid_f<ACC>(rz[i]);
-            sdt += dt;
-            const long long crow = ((long long)q.b * L + t0 + i) * (NP / 2);
-            const float dtl = dt * kLog2e;
+            const float2 dg = sdg[i][lane];
+            const float dtl = dg.x * kLog2e;
 #pragma unroll
-            for (int j = 0; j < NP / 2; ++j) {
-                const float4 p = MAMBA_LD(a.bc, crow + j, (long long)a.batch * L * (NP / 2));
-                dh[2 * j] = fmaf(g, p.z, dh[2 * j]);
-                dh[2 * j + 1] = fmaf(g, p.w, dh[2 * j + 1]);
+            for (int j = 0; j < NW / 2; ++j) {
+                const float4 p = sbc[i * (NP / 2) + n0 / 2 + j];
+                dh[2 * j] = fmaf(dg.y, p.z, dh[2 * j]);
+                dh[2 * j + 1] = fmaf(dg.y, p.w, dh[2 * j + 1]);
             }
 #pragma unroll
-            for (int n = 0; n < NP; ++n)
-                dh[n] *= ACC ? expf(dt * Av[n]) : ex2_approx(dtl * Av[n]);
+            for (int j = 0; j < NW; ++j)
+                dh[j] *= ACC ? expf(dg.x * Av[j]) : ex2_approx(dtl * Av[j]);
         }
+        __syncthreads();   // shared memory is rewritten by the next tile
     }
     if (q.ok) {
         const long long at = (long long)cidx * rows + q.row;
 #pragma unroll
-        for (int n = 0; n < NP; ++n)
-            MAMBA_ST(a.dloc, at * NP + n, (long long)a.nchunks * rows * NP, dh[n]);
-        MAMBA_ST(a.sdt, at, (long long)a.nchunks * rows, sdt);
+        for (int j = 0; j < NW; ++j)
+            MAMBA_ST(a.dloc, at * NP + n0 + j, (long long)a.nchunks * rows * NP, dh[j]);
+        if (warp == 0) MAMBA_ST(a.sdt, at, (long long)a.nchunks * rows, sdt);
     }
 }
 
@@ -778,7 +825,8 @@ cudaError_t launch_bwd(const BwdArgs& a, bool hz, cudaStream_t st) {
     if (a.nchunks > 1) {
         ProfScope prof(kKindBwdSummary, st);
         auto ks = hz ? bwd_summary_kernel<T, NP, SP, true> : bwd_summary_kernel<T, NP, SP, false>;
-        ks<<<dim3((unsigned)units, (unsigned)(a.nchunks - 1)), 32, 0, st>>>(a);
+        ks<<<dim3((unsigned)units, (unsigned)(a.nchunks - 1)), 32 * bwd_summary_warps<NP>(), 0,
+             st>>>(a);
         const long long n = (long long)a.batch * a.dim * NP;
         bwd_chunk_carry_kernel<<<(unsigned)((n + kReduceThreads - 1) / kReduceThreads),
                                  kReduceThreads, 0, st>>>(a, NP);
